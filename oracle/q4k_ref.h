@@ -1,0 +1,85 @@
+/*
+ * Q4_K matmul oracle: plain, slow, obviously correct CPU code.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * loads this code; only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code with the CUDA path.
+ *
+ * What it computes (the method): the pages are serving READMEs that only name
+ * the operation - a GGUF target "dequantizes Q4_K into the matrix-multiply
+ * operand" on every prefill pass (sparkinfer-server README, "Serve a GGUF instead
+ * of NVFP4"); decode projections run over the same weights (ninfer serving docs,
+ * "Determinism"); the routed MoE down projection ends in a weighted combine
+ * (sparkinfer-server README, "Determinism").  The bit layout of a Q4_K block is
+ * not on the pages; it is the public GGUF Q4_K definition:
+ *
+ *   bytes [0,2)    d     IEEE binary16, little-endian
+ *   bytes [2,4)    dmin  IEEE binary16
+ *   bytes [4,16)   scales[12]: eight 6-bit (sc_j, m_j) pairs
+ *                    j < 4 : sc_j = scales[j] & 63,   m_j = scales[j+4] & 63
+ *                    j >= 4: sc_j = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4
+ *                            m_j  = (scales[j+4] >> 4) | (scales[j]   >> 6) << 4
+ *   bytes [16,144) qs[128]: for g = 0..3, l = 0..31, byte qs[32g+l] holds the
+ *                  code of weight 64g+l in its low nibble and of weight
+ *                  64g+32+l in its high nibble.
+ *
+ *   weight 32s+l of the block:  w = d*sc_s*q - dmin*m_s
+ *
+ * Dequantization is done in fp32: d*sc_s, (d*sc_s)*q and dmin*m_s are exact in
+ * fp32 (at most 21 significant bits), so the only rounding is the final
+ * subtraction.  Matrix products accumulate in fp64 in increasing k; each product
+ * of an fp32 weight and a bf16 activation is exact in fp64.
+ *
+ * A weight matrix W is N x K (K % 256 == 0) stored as N rows of K/256 blocks,
+ * rows contiguous; y[m][n] = sum_k x[m][k] * W[n][k].
+ */
+#ifndef Q4K_REF_H
+#define Q4K_REF_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+float q4k_ref_f16_to_f32(uint16_t h);
+float q4k_ref_bf16_to_f32(uint16_t b);
+uint16_t q4k_ref_f32_to_bf16(float f);
+
+/* (sc_j, m_j) for j = 0..7 from the 12-byte field */
+void q4k_ref_scale_min(const uint8_t *scales, int j, int *sc, int *m);
+
+/* one 144-byte block -> 256 fp32 weights */
+void q4k_ref_dequant_block(const uint8_t *blk, float *out);
+
+/* whole matrix -> N x K fp32 / bf16; returns 0, or -1 on a bad shape */
+int q4k_ref_dequant(const uint8_t *w, int64_t N, int64_t K, float *out);
+int q4k_ref_dequant_bf16(const uint8_t *w, int64_t N, int64_t K, uint16_t *out);
+
+/* y[M][N] (fp64) = x[M][K] (bf16) * W^T, fp64 accumulation in increasing k */
+int q4k_ref_gemm(const uint8_t *w, int64_t N, int64_t K, const uint16_t *x, int64_t M, double *y);
+/* same result, rows of W split across `threads` pthreads (for timing) */
+int q4k_ref_gemm_mt(const uint8_t *w, int64_t N, int64_t K, const uint16_t *x, int64_t M, double *y,
+                    int threads);
+
+/* MoE routing: stable counting sort of the T*topk (token, slot) items by expert.
+ * offsets[E+1] (offsets[e]..offsets[e+1] are expert e's items), perm[T*topk]
+ * holds item indices t*topk+j in sorted order.  Returns the number of items
+ * whose expert id is outside [0,E) (those are left out of perm). */
+int64_t q4k_ref_moe_route(const int32_t *ids, int64_t T, int32_t topk, int32_t E, int32_t *offsets,
+                          int32_t *perm);
+
+/* MoE per-slot outputs out[T][topk][N] (fp64).  w_experts is [E][N][K/256]
+ * blocks.  x_per_slot = 0: x is [T][K] and every slot of token t reads x[t];
+ * x_per_slot = 1: x is [T][topk][K].  A slot whose expert id is outside [0,E)
+ * gets zeros. */
+int q4k_ref_moe_slots(const uint8_t *w_experts, int32_t E, int64_t N, int64_t K, const uint16_t *x,
+                      int x_per_slot, const int32_t *ids, int64_t T, int32_t topk, double *out,
+                      int threads);
+
+/* y[T][N] = sum_{j=0..topk-1} gates[t][j] * out[t][j][:], in j order, fp64 */
+void q4k_ref_moe_combine(const double *out, const float *gates, int64_t T, int32_t topk, int64_t N, double *y);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
