@@ -1,0 +1,540 @@
+#!/usr/bin/env python
+"""Benchmark of the Q4_K matmul hot path on GB300.
+
+Default workload (`--workload decode`): one decode step = the gate/up projection
+GEMV (K 5120 -> N 17408) followed by the down projection GEMV (K 17408 -> N
+5120), bf16 activations, fp32 outputs, Q4_K weights drawn from N(0, 0.02^2).
+The metric is effective Q4_K weight bandwidth: weight bytes streamed per second.
+
+Other workloads (for measurement, not the headline line): `verify` (M-token
+speculative-verify GEMM, K 5120 -> N 17408, --m, default 4), `prefill` (M x K
+5120 -> N 17408 then M x K 17408 -> N 5120, --m, default 4096, TFLOP/s) and
+`moe` (128 experts, top-8: gate, up and down with the weighted combine, --m
+tokens, default 2048).
+
+Timing: W warm-up steps, then exactly K steps between a barrier plus
+cudaDeviceSynchronize on both sides, timed with CUDA events on the launching
+stream.  Each step's kernels are replayed from a CUDA graph; consecutive steps
+cycle through R weight sets whose total exceeds the 129 MB L2, so the weights
+always come from HBM.  SM clocks and throttle reasons are sampled through NVML
+during the timed region.  `e2e` repeats the metric through the public API with
+the activations copied from pinned host memory and the outputs copied back every
+step.  `--impl reference` times the plain-C oracle on the host cores instead.
+
+Under torchrun each rank runs the same workload on its own GPU (independent
+replicas, weak scaling); the reported time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Q4_K matmul effective weight GB/s (decode) and TFLOP/s (prefill) vs roofline"
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+L2_BYTES = 129 * 10 ** 6
+
+
+# ------------------------------------------------------------------ helpers
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), \
+        int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_sha(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel's source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)[kernel]
+        if d["source_sha256"] != source_sha(d["source"]):
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples SM clock, max clock and clock-event reasons via NVML (read only)."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, cuda_index: int):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            ok = False
+            try:
+                import torch
+                props = torch.cuda.get_device_properties(cuda_index)
+                bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+            if not ok:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[cuda_index]) if vis and vis.split(",")[0].isdigit() else cuda_index
+                if nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+                    return
+            self._nvml, self._h = nv, h
+            m = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+        except OSError:
+            self._nvml = None
+
+    def _run(self):
+        nv, h = self._nvml, self._h
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if get_reasons(h, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._nvml is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b and n != "gpu_idle"],
+                "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------- workloads
+
+class Workload:
+    """Holds the host inputs of one workload and knows how to run one step."""
+
+    def __init__(self, name: str, m: int):
+        import numpy as np
+        import synth
+        self.name, self.m = name, m
+        self.np = np
+        self.mats = []   # list of (tag, N, K, M, blocks, x) for dense GEMM steps
+        self.moe = None
+        if name == "decode":
+            self.mats = [("gate_up", 17408, 5120, 1, synth.weights(synth.seed(1, 0), 17408, 5120),
+                          synth.normal_bf16(synth.seed(1, 1), 5120).reshape(1, 5120)),
+                         ("down", 5120, 17408, 1, synth.weights(synth.seed(1, 5), 5120, 17408),
+                          synth.normal_bf16(synth.seed(1, 6), 17408).reshape(1, 17408))]
+            self.unit, self.config = "GB/s", {"workload": "decode GEMV M=1: K5120->N17408 then K17408->N5120"}
+        elif name == "verify":
+            self.mats = [("verify", 17408, 5120, m, synth.weights(synth.seed(2, 0), 17408, 5120),
+                          synth.normal_bf16(synth.seed(2, 1), m * 5120).reshape(m, 5120))]
+            self.unit, self.config = "GB/s", {"workload": f"speculative-verify GEMM M={m}: K5120->N17408"}
+        elif name == "prefill":
+            self.mats = [("prefill_up", 17408, 5120, m, synth.weights(synth.seed(3, 0), 17408, 5120, 0.02, 0.01,
+                                                                       10.0, synth.seed(3, 4)),
+                          synth.normal_bf16(synth.seed(3, 1), m * 5120).reshape(m, 5120)),
+                         ("prefill_down", 5120, 17408, m, synth.weights(synth.seed(3, 5), 5120, 17408, 0.02, 0.01,
+                                                                         10.0, synth.seed(3, 9)),
+                          synth.normal_bf16(synth.seed(3, 6), m * 17408).reshape(m, 17408))]
+            self.unit, self.config = "TFLOP/s", {"workload": f"prefill GEMM M={m}: K5120->N17408 then K17408->N5120"}
+        elif name == "moe":
+            E, topk = 128, 8
+            ids, gates = synth.routing(synth.seed(4, 2) + m, synth.seed(4, 3) + m, m, E, topk)
+            mk = lambda s, N, K: np.concatenate(  # noqa: E731
+                [synth.weights(synth.seed(4, s) + 1000 * (e + 1), N, K) for e in range(E)])
+            self.moe = dict(E=E, topk=topk, T=m, ids=ids, gates=gates,
+                            gate=mk(0, 768, 2048), up=mk(7, 768, 2048), down=mk(5, 2048, 768),
+                            x=synth.normal_bf16(synth.seed(4, 1), m * 2048).reshape(m, 2048),
+                            xd=synth.normal_bf16(synth.seed(4, 6), m * topk * 768).reshape(m * topk, 768))
+            self.unit, self.config = "GB/s", {"workload": f"MoE 128 experts top-8 T={m}: gate+up K2048->N768 "
+                                                          "per slot, down K768->N2048 with weighted combine"}
+        else:
+            raise SystemExit(f"unknown workload {name}")
+
+    # algorithmic quantities per step
+    def weight_bytes(self) -> float:
+        if self.moe:
+            touched = len(set(self.moe["ids"].reshape(-1).tolist()))
+            return touched * (2 * 768 * 2048 + 2048 * 768) * 144 / 256
+        return float(sum(N * K * 144 // 256 for _, N, K, *_ in self.mats))
+
+    def flops(self) -> float:
+        if self.moe:
+            items = self.moe["T"] * self.moe["topk"]
+            return 2.0 * items * 3 * 768 * 2048
+        return float(sum(2 * M * N * K for _, N, K, M, *_ in self.mats))
+
+    def value(self, seconds_per_step: float) -> float:
+        if self.unit == "TFLOP/s":
+            return self.flops() / seconds_per_step / 1e12
+        return self.weight_bytes() / seconds_per_step / 1e9
+
+
+class GpuRunner:
+    """Device buffers (R rotating weight sets) and per-step launch functions."""
+
+    def __init__(self, wl: Workload, device):
+        import torch
+        import q4_weight_quantized_gb300 as q4k
+        self.torch, self.q4k, self.wl, self.dev = torch, q4k, wl, device
+        np = wl.np
+
+        def d(a):
+            a = np.ascontiguousarray(a)
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
+
+        per_set = wl.weight_bytes() if not wl.moe else sum(wl.moe[k].nbytes for k in ("gate", "up", "down"))
+        self.R = max(2, int(4 * L2_BYTES // per_set) + 1)
+        if wl.moe:
+            self.R = max(2, min(self.R, 6))
+        self.sets, self.x, self.y, self.ws = [], [], [], []
+        if wl.moe:
+            mo = wl.moe
+            base = {k: d(mo[k]) for k in ("gate", "up", "down")}
+            for r in range(self.R):
+                self.sets.append(base if r == 0 else {k: v.clone() for k, v in base.items()})
+            self.ids, self.gates = d(mo["ids"]), d(mo["gates"])
+            self.xg, self.xd = d(mo["x"]), d(mo["xd"])
+            T, topk = mo["T"], mo["topk"]
+            self.y_gate = torch.empty((T, topk, 768), dtype=torch.float32, device=device)
+            self.y_up = torch.empty((T, topk, 768), dtype=torch.float32, device=device)
+            self.y_down = torch.empty((T, 2048), dtype=torch.float32, device=device)
+            wsb = max(q4k.q4k_moe_workspace_size(mo["E"], 768, 2048, T, topk, 0),
+                      q4k.q4k_moe_workspace_size(mo["E"], 2048, 768, T, topk, 1))
+            self.moe_ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+            self.moe_wsb = wsb
+        else:
+            base = [d(b) for (_, _, _, _, b, _) in wl.mats]
+            for r in range(self.R):
+                self.sets.append(base if r == 0 else [t.clone() for t in base])
+            for (_, N, K, M, _, x) in wl.mats:
+                self.x.append(d(x))
+                self.y.append(torch.empty((M, N), dtype=torch.float32, device=device))
+                wsb = q4k.q4k_gemm_workspace_size(M, N, K)
+                self.ws.append((torch.empty(max(wsb, 1), dtype=torch.uint8, device=device), wsb))
+
+    def launches_per_step(self) -> int:
+        if self.wl.moe:
+            return 3 * 2 + 1  # route + grouped GEMM for gate, up, down; + combine
+        return sum(1 if M <= 16 else -(-M // 16) for (_, _, _, M, _, _) in self.wl.mats)
+
+    def step(self, r: int, mark=None):
+        """Enqueue one step using weight set r.  mark(i) is called before
+        matrix i and after the last one (to record events)."""
+        q4k, wl = self.q4k, self.wl
+        if wl.moe:
+            mo, s = wl.moe, self.sets[r]
+            E, T, topk = mo["E"], mo["T"], mo["topk"]
+            if mark:
+                mark(0)
+            q4k.q4k_moe_grouped_gemm(s["gate"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk, self.y_gate,
+                                     0, self.moe_ws, self.moe_wsb)
+            q4k.q4k_moe_grouped_gemm(s["up"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk, self.y_up, 0,
+                                     self.moe_ws, self.moe_wsb)
+            q4k.q4k_moe_grouped_gemm(s["down"], E, 2048, 768, self.xd, 1, self.ids, self.gates, T, topk, self.y_down,
+                                     1, self.moe_ws, self.moe_wsb)
+            if mark:
+                mark(1)
+            return
+        for i, (_, N, K, M, _, _) in enumerate(wl.mats):
+            if mark:
+                mark(i)
+            if M == 1:
+                q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i])
+            else:
+                ws, wsb = self.ws[i]
+                q4k.q4k_gemm(self.sets[r][i], N, K, self.x[i], M, K, self.y[i], N, ws if wsb else None, wsb)
+        if mark:
+            mark(len(wl.mats))
+
+
+def run_gpu(args, rank, local_rank, world):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from q4_weight_quantized_gb300.build import build_library
+    import q4_weight_quantized_gb300 as q4k
+
+    build_library()
+    q4k.load()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    wl = Workload(args.workload, args.m)
+    gr = GpuRunner(wl, device)
+    stream = torch.cuda.Stream(device)
+    n_marks = (len(wl.mats) + 1) if not wl.moe else 2
+
+    # warm the host-side state (descriptors, attributes) before capture
+    with torch.cuda.stream(stream):
+        for r in range(gr.R):
+            gr.step(r)
+    torch.cuda.synchronize()
+    q4k.q4k_check_device(stream)
+
+    # one graph per weight set; external event nodes time the kernels inside
+    graphs, gevents = [], []
+    try:
+        ev_kw = dict(enable_timing=True, external=True)
+        torch.cuda.Event(**ev_kw)
+        ext = True
+    except TypeError:
+        ev_kw, ext = dict(enable_timing=True), False
+    for r in range(gr.R):
+        g = torch.cuda.CUDAGraph()
+        evs = [torch.cuda.Event(**ev_kw) for _ in range(n_marks)] if ext else None
+        with torch.cuda.graph(g, stream=stream):
+            gr.step(r, mark=(lambda i, evs=evs: evs[i].record()) if ext else None)
+        graphs.append(g)
+        gevents.append(evs)
+
+    # warm-up steps
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % gr.R].replay()
+    torch.cuda.synchronize()
+
+    # timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with clocks:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(args.steps):
+                graphs[i % gr.R].replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1)
+    q4k.q4k_check_device(stream)
+
+    # per-kernel durations from the last replay of every graph
+    kernel_ms = None
+    if ext:
+        per = [[gevents[r][i].elapsed_time(gevents[r][i + 1]) for r in range(gr.R)] for i in range(n_marks - 1)]
+        kernel_ms = [statistics.mean(p) for p in per]
+
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API: activations from pinned host memory,
+    # outputs back to pinned host memory, every step
+    e2e = None
+    if not wl.moe:
+        hx = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory() for (*_, x) in wl.mats]
+        hy = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in gr.y]
+        e2e_steps = min(args.steps, 2000)
+        with torch.cuda.stream(stream):
+            for i in range(10):
+                for j in range(len(wl.mats)):
+                    gr.x[j].copy_(hx[j], non_blocking=True)
+                gr.step(i % gr.R)
+                for j in range(len(wl.mats)):
+                    hy[j].copy_(gr.y[j], non_blocking=True)
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(e2e_steps):
+                for j in range(len(wl.mats)):
+                    gr.x[j].copy_(hx[j], non_blocking=True)
+                gr.step(i % gr.R)
+                for j in range(len(wl.mats)):
+                    hy[j].copy_(gr.y[j], non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": wl.value(ems / 1e3 / e2e_steps) * world, "unit": wl.unit,
+               "h2d_bytes_per_step": int(sum(x.nbytes for (*_, x) in wl.mats)),
+               "d2h_bytes_per_step": int(sum(y.numel() * 4 for y in gr.y)), "steps": e2e_steps}
+
+    hbm, bf16, bf16_s, src = peaks()
+    sec_per_step = ms / 1e3 / args.steps
+    line = {
+        "metric": METRIC, "value": wl.value(sec_per_step) * world, "unit": wl.unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x Q4_K -> fp32",
+        "data": "synthetic (seeded N(0,0.02^2) weights quantized to Q4_K; N(0,1) bf16 activations)",
+        "config": dict(wl.config, l2="rotating %d weight sets, %.0f MB total > 129 MB L2" %
+                       (gr.R, gr.R * (wl.weight_bytes() if not wl.moe else sum(
+                           wl.moe[k].nbytes for k in ("gate", "up", "down"))) / 1e6),
+                       parallelism="replicas x%d" % world, timing="CUDA graph per step, CUDA events"),
+        "gpu_launches": gr.launches_per_step() * args.steps,
+    }
+    # roofline of the dominant kernel
+    if kernel_ms is not None and not wl.moe:
+        i_dom = int(np.argmax(kernel_ms))
+        tag, N, K, M, *_ = wl.mats[i_dom]
+        if wl.unit == "TFLOP/s":
+            algo = 2.0 * M * N * K
+            ach = algo / (kernel_ms[i_dom] / 1e3) / 1e12
+            line["roofline"] = {"bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
+                                "frac": ach / bf16, "traffic": profiled_traffic(tag), "kernel": tag,
+                                "kernel_us": kernel_ms[i_dom] * 1e3, "peak_source": src + " (burst)"}
+        else:
+            algo = N * K * 144 / 256 + M * K * 2 + M * N * 4
+            ach = algo / (kernel_ms[i_dom] / 1e3) / 1e9
+            line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                                "traffic": profiled_traffic(tag), "kernel": tag,
+                                "kernel_us": kernel_ms[i_dom] * 1e3, "algorithmic_bytes": algo,
+                                "peak_source": src, "frac_of_nominal_8tbs": ach / 8000.0}
+        line["kernels_us"] = {wl.mats[i][0]: kernel_ms[i] * 1e3 for i in range(len(kernel_ms))}
+    line["clocks"] = clocks.summary()
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and args.workload == "decode" and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def cpu_baseline(wl: Workload, budget_s: float = 8.0, rows_fraction: float = 1.0):
+    """Times the oracle (as it stands) on the host cores over the same inputs."""
+    import oracle
+    oracle.build()
+    np = wl.np
+    threads = os.cpu_count() or 1
+    done_bytes, t_total, reps = 0.0, 0.0, 0
+    while t_total < budget_s and reps < 50:
+        for (_, N, K, M, blocks, x) in wl.mats:
+            n = max(1, int(N * rows_fraction))
+            sub = blocks if n == N else np.ascontiguousarray(blocks[:n])
+            t = time.perf_counter()
+            oracle.gemm(sub, n, K, x, threads=threads)
+            t_total += time.perf_counter() - t
+            done_bytes += n * K * 144 / 256
+        reps += 1
+    return {"value": done_bytes / t_total / 1e9, "unit": wl.unit, "cores": threads, "kind": "oracle",
+            "sample": f"{reps} full decode steps (both matrices, all rows), {t_total:.1f} s, plain C, "
+                      f"fp64 accumulate, rows split over {threads} pthreads"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle on the host cores, same metric and workload;
+    each step is a bounded row sample of the decode step."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = Workload(args.workload if args.workload in ("decode", "verify") else "decode", args.m)
+    np = wl.np
+    threads = os.cpu_count() or 1
+    # calibrate a row sample so that warm-up + steps take about two minutes
+    t = time.perf_counter()
+    for (_, N, K, M, blocks, x) in wl.mats:
+        oracle.gemm(np.ascontiguousarray(blocks[:256]), 256, K, x, threads=threads)
+    per_row = (time.perf_counter() - t) / 256 / len(wl.mats)
+    budget_per_step = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(min(N for _, N, *_ in wl.mats), budget_per_step / max(per_row, 1e-9) / len(wl.mats))))
+    subs = [(np.ascontiguousarray(b[:rows]), K, x) for (_, N, K, M, b, x) in wl.mats]
+
+    def step():
+        nbytes = 0
+        for (b, K, x) in subs:
+            oracle.gemm(b, rows, K, x, threads=threads)
+            nbytes += rows * K * 144 / 256
+        return nbytes
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    total = 0.0
+    for _ in range(args.steps):
+        total += step()
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    sample = f"{rows} rows of each matrix per step ({args.steps} steps), plain C oracle, {threads} pthreads"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 dequant, fp64 accumulate",
+            "data": "synthetic (seeded, same inputs as the GPU arm)", "config": wl.config,
+            "cpu_baseline": {"value": value, "unit": wl.unit, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["decode", "verify", "prefill", "moe"], default="decode")
+    ap.add_argument("--m", type=int, default=None, help="tokens (verify: 4, prefill: 4096, moe: 2048)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    args = ap.parse_args()
+    if args.m is None:
+        args.m = {"decode": 1, "verify": 4, "prefill": 4096, "moe": 2048}[args.workload]
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, local_rank, world = env_rank()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * q4k — matrix products against GGUF Q4_K block-quantized weights on GB300 (sm_103a).
+ *
+ * The operation.  A GGUF serving target "dequantizes Q4_K into the matrix-multiply
+ * operand" on every prefill pass, a fixed cost that dominates at 128 tokens and is
+ * amortized by 4k (sparkinfer-server README, "Serve a GGUF instead of NVFP4").
+ * Decode runs the same projections with one token per lane, and speculative
+ * verification with 1 + draft tokens per lane (ninfer serving docs, "Start the
+ * server": --draft-tokens N, MTP 1..5, DFlash 1..15; "Determinism": decode kernels
+ * are chosen by the step's token count).  A routed MoE layer ends in a weighted
+ * combine of its experts' down projections (sparkinfer-server README,
+ * "Determinism").  This library computes exactly those products:
+ *
+ *     y[m][n] = sum_k x[m][k] * w[n][k]
+ *
+ * with w an N x K matrix stored as GGUF Q4_K blocks, x bf16 activations and y fp32.
+ *
+ * Q4_K block (144 bytes, 256 consecutive weights of one row; public GGUF format):
+ *     [0,2) d (fp16)  [2,4) dmin (fp16)  [4,16) scales[12]  [16,144) qs[128]
+ *     eight 6-bit (sc_j, m_j) pairs:  j < 4: sc = scales[j] & 63, m = scales[j+4] & 63
+ *                 j >= 4: sc = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4
+ *                          m = (scales[j+4] >> 4) | (scales[j]   >> 6) << 4
+ *     qs[32g+l]: low nibble = code of weight 64g+l, high nibble = weight 64g+32+l
+ *     weight 32s+l = d*sc_s*q - dmin*m_s
+ *
+ * Matrix layout.  Row n of w (output feature n) is K/256 consecutive blocks;
+ * rows are consecutive, so row n starts at byte n*q4k_row_bytes(K).  K must be a
+ * positive multiple of 256.  x is row-major [M][ldx] bf16 (uint16 bit patterns),
+ * y is row-major [M][ldy] fp32.
+ *
+ * Conventions for every call.
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library keeps
+ *     no pointer after it returns.  Scratch memory, where a call needs it, is the
+ *     caller's `ws` buffer; no call allocates device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and enqueue their kernels in order on it.
+ *   - Outputs are overwritten (never accumulated into).
+ *   - Arguments are validated on the host before anything is launched; a call that
+ *     returns an error has enqueued nothing.  Q4K_ERR_NULL: a required pointer is
+ *     NULL.  Q4K_ERR_SHAPE: a size is out of range (K % 256 != 0, N or M < 1,
+ *     ldx < K, ldy < N, ...).  Q4K_ERR_ALIGN: a pointer or leading dimension breaks
+ *     the alignment stated for it.  Q4K_ERR_WORKSPACE: ws is smaller than the size
+ *     query returns.  Q4K_ERR_DEVICE: the current device is not compute capability
+ *     10.3.  Q4K_ERR_CUDA: a CUDA runtime call failed (q4k_last_cuda_error() gives
+ *     the cudaError_t, per thread).
+ *   - Faults inside a kernel surface at the caller's next synchronization, as with
+ *     any CUDA library.  No kernel spins without a bound: a wait that runs past
+ *     its limit records Q4K_ERR_TIMEOUT in a device status word and the kernel
+ *     returns; q4k_check_device() reports and clears it.
+ *   - Every result is run-to-run deterministic: no floating-point atomics, fixed
+ *     reduction orders.
+ */
+#ifndef Q4K_H
+#define Q4K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q4K_OK = 0,
+    Q4K_ERR_NULL = 1,
+    Q4K_ERR_SHAPE = 2,
+    Q4K_ERR_ALIGN = 3,
+    Q4K_ERR_WORKSPACE = 4,
+    Q4K_ERR_DEVICE = 5,
+    Q4K_ERR_CUDA = 6,
+    Q4K_ERR_TIMEOUT = 7
+} q4k_status;
+
+/* Static English text for a status code; never NULL. */
+const char *q4k_status_string(int status);
+
+/* The cudaError_t behind this thread's most recent Q4K_ERR_CUDA (0 if none). */
+int q4k_last_cuda_error(void);
+
+/* Bytes of one Q4_K row of K weights: K/256*144; 0 if K is not a positive
+ * multiple of 256. */
+size_t q4k_row_bytes(int64_t K);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int q4k_version(void);
+
+/* Synchronizes `stream`, then reads and clears the device status word that the
+ * kernels set when a bounded wait gives up.  Returns Q4K_OK, Q4K_ERR_TIMEOUT, or
+ * Q4K_ERR_CUDA if the synchronization itself failed. */
+q4k_status q4k_check_device(void *stream);
+
+/* ----------------------------------------------------------------- dequant --
+ * Standalone dequantization of an N x K Q4_K matrix:
+ *     out[n][k] = d*sc_s*q - dmin*m_s   (fp32, computed as fp32 multiplies and one
+ *                                        final fp32 subtraction: bit-exact)
+ * q4k_dequant_bf16 stores the round-to-nearest-even bf16 of that fp32 value.
+ * This is the "dequantize Q4_K into the matrix-multiply operand" step of the
+ * sparkinfer-server README ("Serve a GGUF instead of NVFP4") on its own.
+ *   w    device, N*q4k_row_bytes(K) bytes, 16-byte aligned
+ *   out  device, N*K elements, row-major, 16-byte aligned
+ * Errors: NULL, SHAPE (N < 1, bad K), ALIGN, DEVICE, CUDA. */
+q4k_status q4k_dequant(const void *w, int64_t N, int64_t K, float *out, void *stream);
+q4k_status q4k_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *out, void *stream);
+
+/* -------------------------------------------------------------------- GEMV --
+ * Decode projection, one token:  y[n] = sum_k x[k] * w[n][k]   (n < N, k < K)
+ * Same as q4k_gemm with M = 1 and the same bits.  The decode path of the pages
+ * carries no floating-point atomics (sparkinfer-server README, "Determinism");
+ * neither does this one.
+ *   w  device Q4_K blocks, 16-byte aligned;  x  device bf16[K], 16-byte aligned;
+ *   y  device fp32[N], 4-byte aligned.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA. */
+q4k_status q4k_gemv(const void *w, int64_t N, int64_t K, const uint16_t *x, float *y, void *stream);
+
+/* -------------------------------------------------------------------- GEMM --
+ * y[m][n] = sum_k x[m*ldx + k] * w[n][k]  for m < M, n < N; y[m*ldy + n].
+ *   M <= 16 : the small-M path (decode and speculative verification, 1 + drafts
+ *             tokens per lane; ninfer serving docs "Determinism"): exact integer
+ *             tensor-core products per 32-weight sub-block, fp32 scaling and
+ *             accumulation.  Row m of the result does not depend on M (the same
+ *             bits as q4k_gemv on row m alone).
+ *   M >  16 : the prefill path (sparkinfer-server README, "Serve a GGUF instead of
+ *             NVFP4"): each weight tile is dequantized to bf16 in shared memory and
+ *             multiplied on the tcgen05 tensor cores with fp32 accumulation in
+ *             tensor memory.
+ *   w   device Q4_K blocks, 16-byte aligned
+ *   x   device bf16, 16-byte aligned, ldx >= K and ldx % 8 == 0
+ *   y   device fp32, ldy >= N; 4-byte aligned for M <= 16, 16-byte aligned with
+ *       ldy % 4 == 0 for M > 16
+ *   ws  device scratch of at least q4k_gemm_workspace_size(M, N, K) bytes,
+ *       256-byte aligned (may be NULL when that size is 0).  Its contents need not
+ *       be initialized and are garbage afterwards.
+ * Errors: NULL, SHAPE (M < 1, N < 1, bad K, ldx < K, ldy < N), ALIGN, WORKSPACE,
+ * DEVICE, CUDA. */
+size_t q4k_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M, int64_t ldx, float *y,
+                    int64_t ldy, void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------- MoE --
+ * Routed-expert layer over E experts, each an N x K Q4_K matrix; the pages' MoE
+ * models route each token to its top-k experts and combine the experts' outputs
+ * weighted by the gates (sparkinfer-server README, "Determinism": the routed MoE
+ * down-projection combine, done there with fp32 atomicAdd; here in slot order,
+ * with no atomics).
+ *
+ * q4k_moe_route: stable counting sort of the T*topk (token t, slot j) items by
+ * expert id.  Item i = t*topk + j.
+ *   topk_ids  device int32[T*topk]
+ *   offsets   device int32[E+1]: items of expert e are perm[offsets[e] .. offsets[e+1])
+ *   perm      device int32[T*topk]: item indices, grouped by expert, increasing
+ *             within an expert.  Items whose id is outside [0,E) are left out
+ *             (offsets[E] counts the valid items; perm beyond it is -1).
+ * This is the routing step of q4k_moe_grouped_gemm exposed on its own.
+ * Errors: NULL, SHAPE (T < 1, topk < 1, E < 1 or E > 1024, topk > E,
+ * T*topk >= 2^31), ALIGN (a pointer not 4-byte aligned), DEVICE, CUDA. */
+q4k_status q4k_moe_route(const int32_t *topk_ids, int64_t T, int32_t topk, int32_t n_experts, int32_t *offsets,
+                         int32_t *perm, void *stream);
+
+typedef enum {
+    Q4K_MOE_X_PER_TOKEN = 0, /* x is [T][K]: every slot of token t multiplies x[t] */
+    Q4K_MOE_X_PER_SLOT = 1   /* x is [T][topk][K]: slot (t,j) multiplies x[t][j] */
+} q4k_moe_x_mode;
+
+typedef enum {
+    Q4K_MOE_Y_PER_SLOT = 0, /* y is [T][topk][N]: y[t][j] = x_row . w_{ids[t][j]}^T */
+    Q4K_MOE_Y_COMBINE = 1   /* y is [T][N]: y[t] = sum_{j=0..topk-1} gates[t][j] * out[t][j],
+                               summed in increasing j */
+} q4k_moe_y_mode;
+
+/* q4k_moe_grouped_gemm: every (token, slot) item multiplies its activation row by
+ * its expert's matrix; one call covers all experts.
+ *   w_experts  device, E*N*q4k_row_bytes(K) bytes: expert e's matrix starts at byte
+ *              e*N*q4k_row_bytes(K); 16-byte aligned
+ *   x          device bf16 rows of K (dense, ld = K), 16-byte aligned
+ *   topk_ids   device int32[T][topk]; ids outside [0,E) give zero output rows and
+ *              are not an error (they cannot be checked without a synchronization)
+ *   gates      device fp32[T][topk]; required for Q4K_MOE_Y_COMBINE, else ignored
+ *   y          device fp32, dense, 16-byte aligned
+ *   ws         device scratch, >= q4k_moe_workspace_size(...) bytes, 256-byte aligned;
+ *              holds the routing permutation and, for Q4K_MOE_Y_COMBINE, the
+ *              per-slot fp32 rows; contents need not be initialized
+ * Errors: NULL, SHAPE (as q4k_moe_route, plus N < 1, bad K, E*N >= 2^31, an
+ * unknown mode, N % 4 != 0 with Q4K_MOE_Y_COMBINE), ALIGN, WORKSPACE, DEVICE,
+ * CUDA.  q4k_moe_workspace_size returns 0 for arguments that would give SHAPE. */
+size_t q4k_moe_workspace_size(int32_t n_experts, int64_t N, int64_t K, int64_t T, int32_t topk, int y_mode);
+q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_t N, int64_t K, const uint16_t *x,
+                                int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk,
+                                float *y, int y_mode, void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4K_H */

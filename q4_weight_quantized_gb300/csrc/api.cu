@@ -1,0 +1,266 @@
+// C-ABI of the q4k library: argument validation, device checks, TMA descriptor
+// construction and dispatch to the kernels.  Declarations and the contract of
+// every entry point are in include/q4k.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "q4k.h"
+#include "q4k_internal.h"
+
+namespace q4k {
+
+__device__ unsigned int g_status_word;  // kernels OR Q4K_DEV_* bits here
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+q4k_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return Q4K_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+bool g_dev_ready[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool k_ok(int64_t K) { return K > 0 && K % kQK == 0 && K <= (int64_t)1 << 30; }
+
+}  // namespace
+
+cudaError_t device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo di = {};
+        di.device = dev;
+        if ((e = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+        int optin = 0;
+        if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+        di.smem_optin = (size_t)optin;
+        if (di.cc_major == 10 && di.cc_minor == 3) {
+            void *p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return e;
+            di.status = static_cast<unsigned int *>(p);
+        }
+        g_dev[dev] = di;
+        g_dev_ready[dev] = true;
+    }
+    *out = g_dev[dev];
+    return cudaSuccess;
+}
+
+// Weight matrix as a 2-D uint32 tensor: dims {K/256*36, N}, row pitch K/256*144
+// bytes; tiles of box_rows rows x box_words words, no swizzle, zero fill outside.
+cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K, int box_rows, int box_words) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return cudaErrorNotSupported;
+    const int64_t KB = K / kQK;
+    cuuint64_t dims[2] = {(cuuint64_t)(KB * (kBlockBytes / 4)), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(KB * kBlockBytes)};
+    cuuint32_t box[2] = {(cuuint32_t)box_words, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(w), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace q4k
+
+using namespace q4k;
+
+namespace {
+
+// Common device gate: a cc 10.3 device must be current.
+q4k_status check_device(DeviceInfo *di) {
+    cudaError_t e = device_info(di);
+    if (e != cudaSuccess) {
+        if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver || e == cudaErrorInvalidDevice) {
+            t_last_cuda_error = (int)e;
+            return Q4K_ERR_DEVICE;
+        }
+        return cuda_fail(e);
+    }
+    if (di->cc_major != 10 || di->cc_minor != 3 || di->status == nullptr) return Q4K_ERR_DEVICE;
+    return Q4K_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *q4k_status_string(int status) {
+    switch (status) {
+        case Q4K_OK: return "ok";
+        case Q4K_ERR_NULL: return "a required pointer is NULL";
+        case Q4K_ERR_SHAPE: return "a size argument is out of range";
+        case Q4K_ERR_ALIGN: return "a pointer or leading dimension is misaligned";
+        case Q4K_ERR_WORKSPACE: return "the workspace is too small";
+        case Q4K_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
+        case Q4K_ERR_CUDA: return "a CUDA runtime call failed";
+        case Q4K_ERR_TIMEOUT: return "a kernel gave up waiting on a barrier";
+        default: return "unknown status";
+    }
+}
+
+int q4k_last_cuda_error(void) { return t_last_cuda_error; }
+
+size_t q4k_row_bytes(int64_t K) { return k_ok(K) ? (size_t)(K / kQK) * kBlockBytes : 0; }
+
+int q4k_version(void) { return 100; }
+
+q4k_status q4k_check_device(void *stream) {
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v))) != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(e);
+        return Q4K_ERR_TIMEOUT;
+    }
+    return Q4K_OK;
+}
+
+static q4k_status dequant_common(const void *w, int64_t N, int64_t K, void *out, int out_align, bool bf16,
+                                 void *stream) {
+    if (!w || !out) return Q4K_ERR_NULL;
+    if (N < 1 || !k_ok(K) || N > ((int64_t)1 << 31) - 1) return Q4K_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(out, (uintptr_t)out_align)) return Q4K_ERR_ALIGN;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = bf16 ? launch_dequant_bf16(w, N, K, static_cast<uint16_t *>(out), s)
+                         : launch_dequant_f32(w, N, K, static_cast<float *>(out), s);
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+q4k_status q4k_dequant(const void *w, int64_t N, int64_t K, float *out, void *stream) {
+    return dequant_common(w, N, K, out, 16, false, stream);
+}
+
+q4k_status q4k_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *out, void *stream) {
+    return dequant_common(w, N, K, out, 16, true, stream);
+}
+
+size_t q4k_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+    (void)M; (void)N; (void)K;
+    return 0;
+}
+
+q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M, int64_t ldx, float *y,
+                    int64_t ldy, void *ws, size_t ws_bytes, void *stream) {
+    if (!w || !x || !y) return Q4K_ERR_NULL;
+    if (M < 1 || N < 1 || !k_ok(K) || ldx < K || ldy < N) return Q4K_ERR_SHAPE;
+    if (N > ((int64_t)1 << 31) - 1 || M > ((int64_t)1 << 31) - 1) return Q4K_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(x, 16) || (ldx % 8) != 0 || !aligned(y, 4)) return Q4K_ERR_ALIGN;
+    if (M > 16 && (!aligned(y, 16) || (ldy % 4) != 0)) return Q4K_ERR_ALIGN;
+    const size_t need = q4k_gemm_workspace_size(M, N, K);
+    if (need > 0 && (!ws || ws_bytes < need)) return Q4K_ERR_WORKSPACE;
+    if (ws && !aligned(ws, 256)) return Q4K_ERR_ALIGN;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    for (int64_t m0 = 0; m0 < M && e == cudaSuccess; m0 += 16) {
+        const int64_t mc = (M - m0) < 16 ? (M - m0) : 16;
+        e = launch_smallm(di, w, N, K, x + m0 * ldx, mc, ldx, y + m0 * ldy, ldy, s);
+    }
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+q4k_status q4k_gemv(const void *w, int64_t N, int64_t K, const uint16_t *x, float *y, void *stream) {
+    return q4k_gemm(w, N, K, x, 1, K, y, N, nullptr, 0, stream);
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+static bool moe_shape_ok(int32_t E, int64_t N, int64_t K, int64_t T, int32_t topk) {
+    if (E < 1 || E > 1024 || N < 1 || !k_ok(K) || T < 1 || topk < 1 || topk > E) return false;
+    if (T * (int64_t)topk >= ((int64_t)1 << 31) || (int64_t)E * N >= ((int64_t)1 << 31)) return false;
+    return true;
+}
+
+q4k_status q4k_moe_route(const int32_t *topk_ids, int64_t T, int32_t topk, int32_t n_experts, int32_t *offsets,
+                         int32_t *perm, void *stream) {
+    if (!topk_ids || !offsets || !perm) return Q4K_ERR_NULL;
+    if (T < 1 || topk < 1 || n_experts < 1 || n_experts > 1024 || topk > n_experts ||
+        T * (int64_t)topk >= ((int64_t)1 << 31))
+        return Q4K_ERR_SHAPE;
+    if (!aligned(topk_ids, 4) || !aligned(offsets, 4) || !aligned(perm, 4)) return Q4K_ERR_ALIGN;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, nullptr, 0,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+size_t q4k_moe_workspace_size(int32_t n_experts, int64_t N, int64_t K, int64_t T, int32_t topk, int y_mode) {
+    if (!moe_shape_ok(n_experts, N, K, T, topk)) return 0;
+    size_t b = align256((size_t)(n_experts + 1) * 4) + align256((size_t)(T * topk) * 4);
+    if (y_mode == Q4K_MOE_Y_COMBINE) b += align256((size_t)(T * topk) * (size_t)N * 4);
+    return b;
+}
+
+q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_t N, int64_t K, const uint16_t *x,
+                                int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk,
+                                float *y, int y_mode, void *ws, size_t ws_bytes, void *stream) {
+    if (!w_experts || !x || !topk_ids || !y || !ws) return Q4K_ERR_NULL;
+    if (y_mode == Q4K_MOE_Y_COMBINE && !gates) return Q4K_ERR_NULL;
+    if (!moe_shape_ok(n_experts, N, K, T, topk)) return Q4K_ERR_SHAPE;
+    if ((x_mode != Q4K_MOE_X_PER_TOKEN && x_mode != Q4K_MOE_X_PER_SLOT) ||
+        (y_mode != Q4K_MOE_Y_PER_SLOT && y_mode != Q4K_MOE_Y_COMBINE))
+        return Q4K_ERR_SHAPE;
+    if (y_mode == Q4K_MOE_Y_COMBINE && N % 4 != 0) return Q4K_ERR_SHAPE;
+    if (!aligned(w_experts, 16) || !aligned(x, 16) || !aligned(y, 16) || !aligned(topk_ids, 4) || !aligned(ws, 256) ||
+        (gates && !aligned(gates, 4)))
+        return Q4K_ERR_ALIGN;
+    if (ws_bytes < q4k_moe_workspace_size(n_experts, N, K, T, topk, y_mode)) return Q4K_ERR_WORKSPACE;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    int32_t *offsets = reinterpret_cast<int32_t *>(p);
+    p += align256((size_t)(n_experts + 1) * 4);
+    int32_t *perm = reinterpret_cast<int32_t *>(p);
+    p += align256((size_t)(T * topk) * 4);
+    float *slot_out = y_mode == Q4K_MOE_Y_COMBINE ? reinterpret_cast<float *>(p) : y;
+    cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm,
+                                     y_mode == Q4K_MOE_Y_PER_SLOT ? y : nullptr, N, s);
+    if (e == cudaSuccess)
+        e = launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, T, topk, slot_out, s);
+    if (e == cudaSuccess && y_mode == Q4K_MOE_Y_COMBINE)
+        e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+}  // extern "C"

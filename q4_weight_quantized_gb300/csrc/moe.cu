@@ -1,0 +1,160 @@
+// MoE routing permutation and the weighted combine.
+//
+// The pages' MoE models route each token to its top-k experts, and the routed
+// down projection ends in a combine whose fp32 atomicAdd order is one of the two
+// sources of run-to-run nondeterminism they report (sparkinfer-server README,
+// "Determinism").  Here the (token, slot) items are grouped by expert with a
+// stable counting sort, every item's output row is written by exactly one CTA,
+// and the combine sums each token's slots in slot order: the result does not
+// depend on scheduling.
+#include <cuda_runtime.h>
+
+#include "q4k_internal.h"
+#include "q4k_ptx.cuh"
+
+namespace q4k {
+namespace {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+// One CTA.  Histogram (integer atomics in shared memory: order-independent),
+// exclusive scan, then a stable scatter in chunks of 1024 items: within a chunk,
+// an item's position is its expert's running base + the count of same-expert
+// items in earlier warps + its rank among same-expert lanes of its own warp.
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__restrict__ ids, int n_items, int E,
+                                                              int32_t *__restrict__ offsets,
+                                                              int32_t *__restrict__ perm, float *__restrict__ zero_rows,
+                                                              int64_t row_len) {
+    extern __shared__ int route_smem[];
+    int *base = route_smem;         // [E + 1]: running fill position per expert
+    int *wc = route_smem + E + 1;   // [32][E]: per-warp counts, then per-warp bases
+    __shared__ int warp_tot[kRouteWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e <= E; e += kRouteThreads) base[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_items; i += kRouteThreads) {
+        const int e = ids[i];
+        if (e >= 0 && e < E) atomicAdd(&base[e], 1);
+    }
+    __syncthreads();
+    // exclusive scan of base[0..E) (E <= 1024 = one value per thread)
+    const int v = tid < E ? base[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tot[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        warp_tot[lane] = wi - w;  // exclusive over warps
+    }
+    __syncthreads();
+    const int excl = incl - v + warp_tot[warp];
+    if (tid < E) {
+        base[tid] = excl;
+        offsets[tid] = excl;
+    }
+    if (tid == E - 1) {
+        base[E] = excl + v;
+        offsets[E] = excl + v;
+    }
+    __syncthreads();
+    const int n_valid = base[E];
+
+    for (int c0 = 0; c0 < n_items; c0 += kRouteThreads) {
+        for (int k = tid; k < kRouteWarps * E; k += kRouteThreads) wc[k] = 0;
+        __syncthreads();
+        const int i = c0 + tid;
+        int e = -1;
+        if (i < n_items) {
+            e = ids[i];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) wc[warp * E + e] = __popc(peers);
+        __syncthreads();
+        for (int ex = tid; ex < E; ex += kRouteThreads) {
+            int run = base[ex];
+            for (int w = 0; w < kRouteWarps; ++w) {
+                const int t = wc[w * E + ex];
+                wc[w * E + ex] = run;
+                run += t;
+            }
+            base[ex] = run;
+        }
+        __syncthreads();
+        if (e >= 0) perm[wc[warp * E + e] + rank] = i;
+        __syncthreads();
+    }
+    for (int k = n_valid + tid; k < n_items; k += kRouteThreads) perm[k] = -1;
+    if (zero_rows && n_valid < n_items) {
+        // items with an id outside [0, E) get zero output rows (one warp per item)
+        for (int it = warp; it < n_items; it += kRouteWarps) {
+            const int e = ids[it];
+            if (e < 0 || e >= E)
+                for (int64_t k = lane; k < row_len; k += 32) zero_rows[(int64_t)it * row_len + k] = 0.0f;
+        }
+    }
+}
+
+// y[t][n] = sum_{j < topk} g[t][j] * out[(t*topk + j)][n], j in increasing order;
+// items whose expert id is invalid contribute nothing.
+__global__ void combine_kernel(const float *__restrict__ out, const float *__restrict__ gates,
+                               const int32_t *__restrict__ ids, int E, int64_t T, int topk, int64_t N,
+                               float *__restrict__ y) {
+    const int64_t n4 = N / 4;
+    const int64_t total = T * n4;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = q / n4, c = (q % n4) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < topk; ++j) {
+            const int e = __ldg(ids + t * topk + j);
+            if (e < 0 || e >= E) continue;
+            const float g = __ldg(gates + t * topk + j);
+            const float4 o = __ldg(reinterpret_cast<const float4 *>(out + (t * topk + j) * N + c));
+            acc.x = fmaf(g, o.x, acc.x);
+            acc.y = fmaf(g, o.y, acc.y);
+            acc.z = fmaf(g, o.z, acc.z);
+            acc.w = fmaf(g, o.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(y + t * N + c) = acc;
+    }
+}
+
+}  // namespace
+
+size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kRouteWarps * E * 4; }
+
+cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
+                             float *zero_rows, int64_t row_len, cudaStream_t s) {
+    const size_t smem = route_smem_bytes(E);
+    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    route_kernel<<<1, kRouteThreads, smem, s>>>(ids, (int)n_items, E, offsets, perm, zero_rows, row_len);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,
+                               int64_t T, int topk, int64_t N, float *y, cudaStream_t s) {
+    const int64_t total = T * (N / 4);
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)di.sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    combine_kernel<<<(int)blocks, 256, 0, s>>>(out, gates, ids, E, T, topk, N, y);
+    return cudaGetLastError();
+}
+
+}  // namespace q4k

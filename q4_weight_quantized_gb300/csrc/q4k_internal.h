@@ -1,0 +1,54 @@
+// Host-side launchers shared between the library's translation units.  Each
+// returns a cudaError_t from the launch; arguments were validated by the C-ABI
+// layer (api.cu) before any of these is called.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace q4k {
+
+constexpr int kQK = 256;          // weights per Q4_K block
+constexpr int kBlockBytes = 144;  // bytes per Q4_K block
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int cc_major, cc_minor;
+    size_t smem_optin;
+    unsigned int *status;  // device address of the status word
+};
+
+// Current device's cached properties (first call per device queries them).
+cudaError_t device_info(DeviceInfo *out);
+
+cudaError_t launch_dequant_f32(const void *w, int64_t N, int64_t K, float *out, cudaStream_t s);
+cudaError_t launch_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *out, cudaStream_t s);
+
+// M in [1, 16]
+cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
+                          int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
+
+// MoE: all experts stacked as E*N rows; rows of x and of out are chosen through
+// the routing permutation (perm/offsets from launch_moe_route).
+cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
+                              const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
+                              int64_t T, int topk, float *out, cudaStream_t s);
+
+// Stable counting sort of items by expert (E <= 1024); when zero_rows is given,
+// rows of row_len floats belonging to items with invalid ids are zeroed.
+size_t route_smem_bytes(int E);
+cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
+                             float *zero_rows, int64_t row_len, cudaStream_t s);
+
+// y[t] = sum_j gates[t][j] * out[t*topk+j] in slot order (N % 4 == 0)
+cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,
+                               int64_t T, int topk, int64_t N, float *y, cudaStream_t s);
+
+// TMA descriptor of a Q4_K matrix viewed as uint32 words: dims {K/256*36, N},
+// row pitch K/256*144 bytes, box {box_words, box_rows}, zero fill outside.
+cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K, int box_rows, int box_words);
+
+}  // namespace q4k

@@ -1,0 +1,336 @@
+"""GPU parity: the CUDA path (through the C-ABI) against the oracle.
+
+Bars: dequantization is bit-exact; the small-M path (M <= 16) is within
+max|y - y_ref| / max|y_ref| <= 2e-3; the prefill and MoE tensor-core paths are
+within 1e-2; routing is bit-exact.  Full-size workloads are checked on sampled
+output rows (the oracle computes those rows one by one), in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import q4_weight_quantized_gb300 as q4k
+from tests import gpu_util as G
+from tests.golden import load_blocks
+
+pytestmark = pytest.mark.gpu
+
+TOL_SMALL = 2e-3
+TOL_TC = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from q4_weight_quantized_gb300.build import build_library
+    build_library()
+    q4k.load()
+    assert torch.cuda.is_available()
+    yield
+    q4k.q4k_check_device()
+
+
+def gpu_dequant(blocks, N, K, bf16=False):
+    w = G.dev(blocks)
+    out = torch.empty((N, K), dtype=torch.int16 if bf16 else torch.float32, device="cuda")
+    (q4k.q4k_dequant_bf16 if bf16 else q4k.q4k_dequant)(w, N, K, out)
+    torch.cuda.synchronize()
+    o = G.host(out)
+    return o.view(np.uint16) if bf16 else o
+
+
+def gpu_gemm(blocks, N, K, x, ldx=None, ldy=None, w_dev=None):
+    M = x.shape[0]
+    ldx = ldx or K
+    ldy = ldy or N
+    xp = np.zeros((M, ldx), np.uint16)
+    xp[:, :K] = x
+    w = w_dev if w_dev is not None else G.dev(blocks)
+    xd = G.dev(xp)
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    ws_bytes = q4k.q4k_gemm_workspace_size(M, N, K)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    q4k.q4k_gemm(w, N, K, xd, M, ldx, y, ldy, ws, ws_bytes)
+    torch.cuda.synchronize()
+    out = G.host(y)
+    if ldy > N:
+        assert np.all(np.isnan(out[:, N:])), "wrote past N in the padded rows"
+    return out[:, :N]
+
+
+# ----------------------------------------------------------------- dequant
+
+def test_dequant_tiny_bitexact(ref):
+    cfg, N, K = G.TINY
+    b = G.weights(cfg, 0, N, K)
+    got = gpu_dequant(b, N, K)
+    want = ref.dequant(b, N, K)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    got16 = gpu_dequant(b, N, K, bf16=True)
+    assert np.array_equal(got16, ref.dequant_bf16(b, N, K))
+
+
+def test_dequant_outliers_ragged_bitexact(ref):
+    N, K = 37, 2304
+    b = G.weights(3, 0, N, K, outliers=True)
+    assert np.array_equal(gpu_dequant(b, N, K).view(np.uint32), ref.dequant(b, N, K).view(np.uint32))
+    assert np.array_equal(gpu_dequant(b, N, K, True), ref.dequant_bf16(b, N, K))
+
+
+def test_dequant_golden_blocks(ref):
+    blocks = np.stack([f["block"] for f in load_blocks()])
+    N = blocks.shape[0]
+    got = gpu_dequant(blocks, N, 256)
+    want = ref.dequant(blocks, N, 256)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_dequant_nan_inf_headers(ref):
+    blk = load_blocks()[1]["block"].copy()
+    nan_blk, inf_blk = blk.copy(), blk.copy()
+    nan_blk[0:2] = [0x00, 0x7E]
+    inf_blk[2:4] = [0x00, 0x7C]
+    blocks = np.stack([nan_blk, inf_blk])
+    got = gpu_dequant(blocks, 2, 256)
+    want = ref.dequant(blocks, 2, 256)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+def test_dequant_full_size_bitexact(ref):
+    cfg, N, K = G.DECODE_DOWN
+    b = G.weights(cfg, 0, N, K)
+    got = gpu_dequant(b, N, K)
+    rows = G.sample_rows(N, 64)
+    want = ref.dequant(G.rows_of(b, rows), len(rows), K)
+    assert np.array_equal(got[rows].view(np.uint32), want.view(np.uint32))
+
+
+# ------------------------------------------------------------- GEMV / small-M
+
+def test_gemv_tiny(ref):
+    cfg, N, K = G.TINY
+    b = G.weights(cfg, 0, N, K)
+    x = G.activations(cfg, 1, 1, K)
+    w, xd = G.dev(b), G.dev(x)
+    y = torch.empty(N, dtype=torch.float32, device="cuda")
+    q4k.q4k_gemv(w, N, K, xd, y)
+    torch.cuda.synchronize()
+    assert G.rel_err(G.host(y), ref.gemm(b, N, K, x)[0]) <= TOL_SMALL
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 9, 15, 16])
+def test_smallm_ragged(ref, M):
+    N, K = 200, 1280          # N: 6 full 32-row tiles + a tail of 8; K: 5 blocks (ragged last stage)
+    b = G.weights(2, 0, N, K, outliers=True)
+    x = G.activations(2, 1, M, K)
+    assert G.rel_err(gpu_gemm(b, N, K, x), ref.gemm(b, N, K, x)) <= TOL_SMALL
+
+
+def test_smallm_strided_and_edges(ref):
+    for (N, K, M) in [(1, 256, 1), (3, 256, 16), (33, 768, 7), (64, 512, 16)]:
+        b = G.weights(2, 2, N, K)
+        x = G.activations(2, 3, M, K)
+        assert G.rel_err(gpu_gemm(b, N, K, x, ldx=K + 8, ldy=N + 5), ref.gemm(b, N, K, x)) <= TOL_SMALL
+
+
+def test_one_hot_column_exact(ref):
+    N, K = 64, 512
+    b = G.weights(2, 4, N, K)
+    w = ref.dequant(b, N, K)
+    for k in (0, 37, 300, 511):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80
+        y = gpu_gemm(b, N, K, x)[0]
+        assert np.array_equal(y, w[:, k]), k
+
+
+def test_batch_invariance_and_determinism():
+    N, K = 17408, 5120
+    b = G.weights(2, 0, N, K)
+    w = G.dev(b)
+    x = G.activations(2, 1, 16, K)
+    y16 = gpu_gemm(b, N, K, x, w_dev=w)
+    y16b = gpu_gemm(b, N, K, x, w_dev=w)
+    assert np.array_equal(y16.view(np.uint32), y16b.view(np.uint32)), "not run-to-run deterministic"
+    y4 = gpu_gemm(b, N, K, x[:4], w_dev=w)
+    assert np.array_equal(y4.view(np.uint32), y16[:4].view(np.uint32))
+    for m in (0, 5, 15):
+        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+
+
+@pytest.mark.parametrize("shape", [G.DECODE_UP, G.DECODE_DOWN], ids=["gate_up", "down"])
+def test_decode_gemv_full_size(ref, shape):
+    cfg, N, K = shape
+    b = G.weights(cfg, 0, N, K)
+    x = G.activations(cfg, 1, 1, K)
+    y = gpu_gemm(b, N, K, x)
+    rows = G.sample_rows(N, 256)
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x)
+    assert G.rel_err(y[:, rows], want) <= TOL_SMALL
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_verify_gemm_full_size(ref, M):
+    cfg, N, K = 2, 17408, 5120
+    b = G.weights(cfg, 0, N, K)
+    x = G.activations(cfg, 1, M, K)
+    y = gpu_gemm(b, N, K, x)
+    rows = G.sample_rows(N, 128)
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=8)
+    assert G.rel_err(y[:, rows], want) <= TOL_SMALL
+
+
+# ------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("M", [17, 40, 128])
+def test_prefill_small(ref, M):
+    N, K = 320, 2048
+    b = G.weights(3, 0, N, K, outliers=True)
+    x = G.activations(3, 1, M, K)
+    assert G.rel_err(gpu_gemm(b, N, K, x), ref.gemm(b, N, K, x, threads=8)) <= TOL_TC
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (1024, 5120, 17408), (4096, 17408, 5120)])
+def test_prefill_full_size(ref, M, N, K):
+    b = G.weights(3, 0, N, K, outliers=True)
+    x = G.activations(3, 1, M, K)
+    y = gpu_gemm(b, N, K, x)
+    rows = G.sample_rows(N, 24)
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=16)
+    assert G.rel_err(y[:, rows], want) <= TOL_TC
+
+
+# ---------------------------------------------------------------------- MoE
+
+def test_moe_route_bitexact(ref, syn):
+    for T in (1, 16, 2048):
+        ids, _ = syn.routing(syn.seed(4, 2) + T, syn.seed(4, 3), T, G.MOE_E, G.MOE_TOPK)
+        off, perm = torch.empty(G.MOE_E + 1, dtype=torch.int32, device="cuda"), \
+            torch.empty(T * G.MOE_TOPK, dtype=torch.int32, device="cuda")
+        q4k.q4k_moe_route(G.dev(ids), T, G.MOE_TOPK, G.MOE_E, off, perm)
+        torch.cuda.synchronize()
+        want_off, want_perm, bad = ref.moe_route(ids, G.MOE_E)
+        assert bad == 0
+        assert np.array_equal(G.host(off), want_off)
+        assert np.array_equal(G.host(perm), want_perm)
+
+
+def test_moe_route_invalid_ids(ref):
+    rng = np.random.default_rng(1)
+    T, topk, E = 300, 4, 37
+    ids = rng.integers(-3, E + 3, (T, topk)).astype(np.int32)
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * topk, dtype=torch.int32, device="cuda")
+    q4k.q4k_moe_route(G.dev(ids), T, topk, E, off, perm)
+    torch.cuda.synchronize()
+    want_off, want_perm, _ = ref.moe_route(ids, E)
+    assert np.array_equal(G.host(off), want_off) and np.array_equal(G.host(perm), want_perm)
+
+
+def run_moe(w_blocks, E, N, K, x, x_mode, ids, gates, y_mode, w_dev=None):
+    T, topk = ids.shape
+    w = w_dev if w_dev is not None else G.dev(w_blocks)
+    ws_bytes = q4k.q4k_moe_workspace_size(E, N, K, T, topk, y_mode)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    shape = (T, N) if y_mode == q4k.Q4K_MOE_Y_COMBINE else (T, topk, N)
+    y = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    q4k.q4k_moe_grouped_gemm(w, E, N, K, G.dev(x), x_mode, G.dev(ids), G.dev(gates), T, topk, y, y_mode, ws,
+                             ws_bytes)
+    torch.cuda.synchronize()
+    return G.host(y)
+
+
+@pytest.fixture(scope="module")
+def moe_up():
+    N, K = G.MOE_UP
+    return G.moe_experts(4, 0, N, K)
+
+
+@pytest.fixture(scope="module")
+def moe_down():
+    N, K = G.MOE_DOWN
+    return G.moe_experts(4, 5, N, K)
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_moe_gate_up_per_slot(ref, syn, moe_up, T):
+    N, K = G.MOE_UP
+    ids, gates = syn.routing(syn.seed(4, 2) + T, syn.seed(4, 3) + T, T, G.MOE_E, G.MOE_TOPK)
+    x = G.activations(4, 1, T, K)
+    y = run_moe(moe_up, G.MOE_E, N, K, x, q4k.Q4K_MOE_X_PER_TOKEN, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT)
+    want = ref.moe_slots(moe_up, G.MOE_E, N, K, x, False, ids, threads=8)
+    assert G.rel_err(y, want) <= TOL_SMALL
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_moe_down_combine(ref, syn, moe_down, T):
+    N, K = G.MOE_DOWN
+    ids, gates = syn.routing(syn.seed(4, 2) + T, syn.seed(4, 3) + T, T, G.MOE_E, G.MOE_TOPK)
+    x = G.activations(4, 6, T * G.MOE_TOPK, K)
+    y = run_moe(moe_down, G.MOE_E, N, K, x, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_COMBINE)
+    want = ref.moe(moe_down, G.MOE_E, N, K, x, True, ids, gates, threads=8)
+    assert G.rel_err(y, want) <= TOL_SMALL
+
+
+def test_moe_t2048_sampled(ref, syn, moe_up, moe_down):
+    T, E, topk = 2048, G.MOE_E, G.MOE_TOPK
+    ids, gates = syn.routing(syn.seed(4, 2) + T, syn.seed(4, 3) + T, T, E, topk)
+    tok = G.sample_rows(T, 40, seed=3)
+    # gate/up, per-slot rows
+    N, K = G.MOE_UP
+    x = G.activations(4, 1, T, K)
+    y = run_moe(moe_up, E, N, K, x, q4k.Q4K_MOE_X_PER_TOKEN, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT)
+    want = ref.moe_slots(moe_up, E, N, K, x[tok], False, ids[tok], threads=16)
+    assert G.rel_err(y[tok], want) <= TOL_TC
+    # down with the weighted combine
+    N, K = G.MOE_DOWN
+    xs = G.activations(4, 6, T * topk, K).reshape(T, topk, K)
+    y = run_moe(moe_down, E, N, K, xs.reshape(T * topk, K), q4k.Q4K_MOE_X_PER_SLOT, ids, gates,
+                q4k.Q4K_MOE_Y_COMBINE)
+    want = ref.moe(moe_down, E, N, K, xs[tok].reshape(-1, K), True, ids[tok], gates[tok], threads=16)
+    assert G.rel_err(y[tok], want) <= TOL_TC
+
+
+def test_moe_special_cases(ref, syn):
+    # every token routed to experts 0..7 in order: per-slot output j equals a dense GEMM with expert j
+    E, N, K, T, topk = 12, 96, 512, 5, 8
+    w = np.concatenate([G.weights(4, 30 + e, N, K) for e in range(E)])
+    ids = np.tile(np.arange(topk, dtype=np.int32), (T, 1))
+    gates = np.full((T, topk), 1.0 / topk, np.float32)
+    x = G.activations(4, 7, T, K)
+    y = run_moe(w, E, N, K, x, q4k.Q4K_MOE_X_PER_TOKEN, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT)
+    for j in range(topk):
+        dense = gpu_gemm(w[j * N:(j + 1) * N], N, K, x)
+        assert G.rel_err(y[:, j], dense) <= TOL_SMALL
+    # one-hot gates: the combine returns the chosen slot
+    ids2, _ = syn.routing(77, 78, T, E, topk)
+    onehot = np.zeros((T, topk), np.float32)
+    pick = np.arange(T) % topk
+    onehot[np.arange(T), pick] = 1.0
+    xs = G.activations(4, 8, T * topk, K)
+    yc = run_moe(w, E, N, K, xs, q4k.Q4K_MOE_X_PER_SLOT, ids2, onehot, q4k.Q4K_MOE_Y_COMBINE)
+    ys = run_moe(w, E, N, K, xs, q4k.Q4K_MOE_X_PER_SLOT, ids2, onehot, q4k.Q4K_MOE_Y_PER_SLOT)
+    assert np.array_equal(yc, ys[np.arange(T), pick])
+    # invalid ids: zero per-slot rows, and no contribution to the combine
+    ids3 = ids2.copy()
+    ids3[0, 0] = -1
+    ids3[2, 5] = E
+    ys3 = run_moe(w, E, N, K, xs, q4k.Q4K_MOE_X_PER_SLOT, ids3, onehot, q4k.Q4K_MOE_Y_PER_SLOT)
+    assert np.all(ys3[0, 0] == 0) and np.all(ys3[2, 5] == 0)
+    want = ref.moe(w, E, N, K, xs, True, ids3, onehot)
+    yc3 = run_moe(w, E, N, K, xs, q4k.Q4K_MOE_X_PER_SLOT, ids3, onehot, q4k.Q4K_MOE_Y_COMBINE)
+    assert G.rel_err(yc3, want) <= TOL_SMALL
+
+
+def test_moe_determinism(syn, moe_up):
+    N, K = G.MOE_UP
+    T = 16
+    ids, gates = syn.routing(5, 6, T, G.MOE_E, G.MOE_TOPK)
+    x = G.activations(4, 1, T, K)
+    w = G.dev(moe_up)
+    a = run_moe(moe_up, G.MOE_E, N, K, x, 0, ids, gates, 0, w_dev=w)
+    b = run_moe(moe_up, G.MOE_E, N, K, x, 0, ids, gates, 0, w_dev=w)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
