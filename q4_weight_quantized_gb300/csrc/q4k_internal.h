@@ -51,4 +51,8 @@ cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const flo
 // row pitch K/256*144 bytes, box {box_words, box_rows}, zero fill outside.
 cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K, int box_rows, int box_words);
 
+// TMA descriptor of bf16 activations [rows][ld] viewed as uint64 (4 activations
+// each): dims {K/4, rows}, box {box_elems, 1} = one row segment of 4*box_elems.
+cudaError_t make_act_tmap(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_elems);
+
 }  // namespace q4k

@@ -7,12 +7,15 @@
 // streaming the 0.5625-byte-per-weight Q4_K matrix from HBM once, so the kernel
 // is built around keeping HBM busy and the per-weight instruction count low:
 //
-//   * TMA streams the raw blocks: a CTA owns R = 32 consecutive weight rows; each
-//     pipeline stage is one 2-D bulk-tensor copy of 32 rows x 4 blocks (18 KiB)
-//     into shared memory, issued by a producer warp and completed on an mbarrier.
-//     Rows past N and blocks past K/256 are zero-filled by the copy and decode to
-//     zero weights.
-//   * Four consumer warps each take one block of the stage.  A lane turns one
+//   * A CTA owns 32 consecutive weight rows; its four warps split the K blocks
+//     (warp w takes blocks w, w+4, ...).  Every warp streams its own blocks with
+//     TMA into a private ring of shared-memory slots: one 2-D bulk-tensor copy of
+//     32 rows x 1 block (4.5 KiB) plus one 512-byte copy per token of the
+//     matching 256 activations, completed on the slot's mbarrier.  The warp
+//     refills a slot as soon as it has consumed it, so the copies of the next
+//     slots stay in flight while it computes, and no warp waits for another.
+//     Rows past N are zero-filled by the copy and decode to zero weights.
+//   * A lane turns one
 //     32-bit word of codes into four bf16x2 registers holding 128+q exactly
 //     (one byte permute and one LOP3 per pair: 0x4300 is bf16 128.0, whose last
 //     seven mantissa bits count units), and feeds them as the A operand of a
@@ -29,6 +32,11 @@
 //     order).  No atomics anywhere: the result is run-to-run deterministic, and
 //     since neither the split nor the order depends on M, row m of an M-token
 //     call equals a 1-token call on row m bit for bit.
+//
+// The MoE grouped GEMM runs the same kernel with one grid layer per expert: the
+// token slots of a chunk are the (token, k-slot) items routed to that expert,
+// their activation rows are gathered by the same per-row copies, and each
+// output row goes to its item's slot.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -38,24 +46,28 @@
 namespace q4k {
 namespace {
 
-constexpr int kRows = 32;                          // weight rows per CTA
-constexpr int kRowTiles = kRows / 16;              // 16-row MMA tiles per CTA
-constexpr int kBlocksPerStage = 4;                 // one block per consumer warp
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + producer warp
-constexpr int kStageRowBytes = kBlocksPerStage * kBlockBytes;  // 576
-constexpr int kStageBytes = kRows * kStageRowBytes;            // 18432
-constexpr int kStageWords = kStageRowBytes / 4;                // 144 (TMA box inner dim, uint32)
+constexpr int kRows = 32;                  // weight rows per CTA
+constexpr int kRowTiles = kRows / 16;      // 16-row MMA tiles per CTA
+constexpr int kWarps = 4;                  // split the CTA's K blocks
+constexpr int kThreads = kWarps * 32;
+constexpr int kBlkWBytes = kRows * kBlockBytes;  // 4608: one block column of the CTA's rows
+constexpr int kBlkWords = kBlockBytes / 4;       // 36 (TMA box inner dim, uint32)
+constexpr int kXBlkBytes = kQK * 2;              // 512: one token's activations for one block
 constexpr int kTableRowBytes = 80;  // 8 x (dsc, bias) + 16 pad: conflict-free 16-byte reads
-constexpr int kTableBytes = kConsumerWarps * kRows * kTableRowBytes;
-constexpr int kStages = 2;
+constexpr int kTableBytes = kRows * kTableRowBytes;
+constexpr int kRedBytes = kWarps * 16 * kRows * 4 + 16 * kRows * 4;  // per-warp + final partials
 
-constexpr size_t smem_bytes() {
-    return (size_t)kStages * kStageBytes + kTableBytes + 2 * kStages * 8 + 16;
+__host__ __device__ constexpr int slot_bytes(int nx) { return (kBlkWBytes + nx * kXBlkBytes + 127) / 128 * 128; }
+// per warp: [ring of `slots` slots][scale table]
+__host__ __device__ constexpr int warp_bytes(int nx, int slots) { return slots * slot_bytes(nx) + kTableBytes; }
+// CTA: [warp regions][barriers][reduction buffer (MoE only; dense reuses the rings)]
+__host__ __device__ constexpr int bars_off(int nx, int slots) { return kWarps * warp_bytes(nx, slots); }
+__host__ __device__ constexpr int red_off(int nx, int slots) { return bars_off(nx, slots) + kWarps * slots * 8 + 64; }
+__host__ __device__ constexpr int smem_total(int nx, int slots, bool moe) {
+    return red_off(nx, slots) + (moe ? kRedBytes : 0);
 }
 
-static_assert(kConsumerWarps * kRows * 16 * 4 + kRows * 16 * 4 <= kStages * kStageBytes,
-              "reduction buffers alias the stage buffers");
+static_assert(kRedBytes <= kWarps * 2 * slot_bytes(1), "dense reduction buffers alias the rings");
 
 __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t &lo23, uint32_t &hi01,
                                             uint32_t &hi23) {
@@ -67,11 +79,19 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t
     hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
 }
 
-// Decode one row's block header (d, dmin, 12 scale bytes) into 8 (d*sc, bias) pairs.
+// byte i of w as an fp32 2^23 + byte (exponent 150, the byte in the low mantissa bits)
+__device__ __forceinline__ float byte_magic(uint32_t w, int i) {
+    return __uint_as_float(prmt(w, 0x4B000000u, 0x7440u | (uint32_t)i));
+}
+
+// Decode one row's block header (d, dmin, 12 scale bytes) into 8 (d*sc, bias)
+// pairs, bias = 128*d*sc + dmin*m.  d*sc and dmin*m are exact: fma(2^23+b, d,
+// -2^23*d) rounds d*b, which has at most 17 significant bits.
 __device__ __forceinline__ void decode_scales(const uint8_t *blk, float *table_row) {
     const uint4 h = *reinterpret_cast<const uint4 *>(blk);
     const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
     const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+    const float nd = -8388608.0f * d, ndm = -8388608.0f * dmin;
     const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
     const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
     const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
@@ -79,11 +99,10 @@ __device__ __forceinline__ void decode_scales(const uint8_t *blk, float *table_r
     float v[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const uint32_t sc = ((j < 4 ? sc_lo : sc_hi) >> (8 * (j & 3))) & 0xFFu;
-        const uint32_t m = ((j < 4 ? m_lo : m_hi) >> (8 * (j & 3))) & 0xFFu;
-        const float dsc = d * (float)sc;
+        const float dsc = fmaf(byte_magic(j < 4 ? sc_lo : sc_hi, j & 3), d, nd);
+        const float dm = fmaf(byte_magic(j < 4 ? m_lo : m_hi, j & 3), dmin, ndm);
         v[2 * j] = dsc;
-        v[2 * j + 1] = fmaf(dmin, (float)m, 128.0f * dsc);
+        v[2 * j + 1] = fmaf(128.0f, dsc, dm);
     }
     float4 *dst = reinterpret_cast<float4 *>(table_row);
 #pragma unroll
@@ -94,8 +113,6 @@ __device__ __forceinline__ void decode_scales(const uint8_t *blk, float *table_r
 // output row.  Dense: slot n is token n.  MoE: slot n of expert e's list is the
 // (token, k-slot) item perm[offsets[e] + n].
 struct RowArgs {
-    const uint16_t *x;
-    int64_t ldx;          // dense: activation row stride; MoE: K
     float *y;
     int64_t ldy;          // dense: output row stride; MoE: N
     int M;                // dense: number of tokens (<= 16)
@@ -105,30 +122,41 @@ struct RowArgs {
     const int32_t *offsets;
 };
 
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Activation row and output offset of token slot n (-1 if the slot is empty).
+template <bool MOE>
+__device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, int n, int &xrow, long long &yoff) {
+    xrow = -1;
+    yoff = -1;
+    if (n < cnt) {
+        if constexpr (MOE) {
+            const int item = __ldg(ra.perm + off0 + n);
+            xrow = ra.x_per_slot ? item : item / ra.topk;
+            yoff = (long long)item * ra.ldy;
+        } else {
+            xrow = n;
+            yoff = (long long)n * ra.ldy;
+        }
+    }
+}
 
-template <int NT, bool MOE>
-__global__ void __launch_bounds__(kThreads, 4) smallm_kernel(const __grid_constant__ CUtensorMap tmW, RowArgs ra, int N,
-                                                          int KB, unsigned int *status) {
+// NT: 8-token MMA tiles (1 or 2).  ONE: exactly one token (the epilogue keeps
+// only the accumulators that hold it).  SLOTS: ring depth per warp.
+template <int NT, bool MOE, bool ONE, int SLOTS>
+__global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                          const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
+                                                          int KB, int nx, unsigned int *status) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *stages = smem;
-    float *tables = reinterpret_cast<float *>(smem + kStages * kStageBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes + kTableBytes);
-    // MoE keeps its reduction buffers apart from the stages (the pipeline runs on
-    // into the next token chunk while a chunk is reduced)
-    float *moe_red = reinterpret_cast<float *>(smem + kStages * kStageBytes + kTableBytes + 2 * kStages * 8 + 16);
     __shared__ int abort_flag;
-    __shared__ long long xoff_s[16], yoff_s[16];
+    __shared__ long long yoff_s[16];
 
     constexpr int kPerChunk = 8 * NT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = lane & 3, r = lane >> 2;
     const int S = gridDim.x;       // K split = cluster size (always 1 for MoE)
     const int split = blockIdx.x;  // == cluster rank
     const int row0 = blockIdx.y * kRows;
-    const int n_stage_total = (KB + kBlocksPerStage - 1) / kBlocksPerStage;
-    const int st0 = (int)((int64_t)n_stage_total * split / S);
-    const int st1 = (int)((int64_t)n_stage_total * (split + 1) / S);
-    const int nst = st1 - st0;
+    const int kb0 = (int)((int64_t)KB * split / S), kb1 = (int)((int64_t)KB * (split + 1) / S);
+    const int nblk = kb1 - kb0 > warp ? (kb1 - kb0 - warp + kWarps - 1) / kWarps : 0;  // this warp's blocks
 
     int off0 = 0, cnt = ra.M, tma_row = row0;
     if constexpr (MOE) {
@@ -139,180 +167,169 @@ __global__ void __launch_bounds__(kThreads, 4) smallm_kernel(const __grid_consta
         tma_row = e * N + row0;
     }
     const int chunks = (cnt + kPerChunk - 1) / kPerChunk;
-    const int total_it = chunks * nst;
+    const int total = chunks * nblk;  // this warp's (chunk, block) iterations
 
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, kConsumerWarps);
-        }
+    const int sbytes = slot_bytes(nx);
+    uint8_t *region = smem + warp * warp_bytes(nx, SLOTS);
+    float *table = reinterpret_cast<float *>(region + SLOTS * sbytes);
+    const uint32_t bar0 = smem_u32(smem + bars_off(nx, SLOTS)) + warp * SLOTS * 8;
+    if (threadIdx.x == 0) abort_flag = 0;
+    if (lane == 0) {
+        for (int i = 0; i < SLOTS; ++i) mbar_init(bar0 + 8 * i, 1);
         fence_mbar_init();
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
     }
     __syncthreads();
 
-    float acc[kRowTiles][NT][4];
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------- producer warp
+    // issue the copies of iteration `it` (chunk it / nblk, block it % nblk) into its slot
+    auto issue = [&](int it) {
+        const int ch = it / nblk, kb = kb0 + warp + kWarps * (it % nblk);
+        const int slot = it % SLOTS;
+        const int nvalid = min(kPerChunk, cnt - ch * kPerChunk);
+        int xrow;
+        long long unused;
+        slot_rows<MOE>(ra, off0, cnt, ch * kPerChunk + lane, xrow, unused);
+        const uint32_t dst = smem_u32(region + slot * sbytes);
         if (lane == 0) {
-            prefetch_tmap(&tmW);
-            for (int it = 0; it < total_it; ++it) {
-                const int slot = it % kStages;
-                if (it >= kStages && !mbar_wait(empty0 + 8 * slot, ((it / kStages) - 1) & 1, status)) {
-                    atomicExch(&abort_flag, 1);
-                    break;
-                }
-                if (*(volatile int *)&abort_flag) break;
-                mbar_arrive_expect_tx(full0 + 8 * slot, kStageBytes);
-                tma_load_2d(smem_u32(stages + slot * kStageBytes), &tmW, (st0 + it % nst) * kStageWords, tma_row,
-                            full0 + 8 * slot);
-            }
+            mbar_arrive_expect_tx(bar0 + 8 * slot, kBlkWBytes + nvalid * kXBlkBytes);
+            tma_load_2d(dst, &tmW, kb * kBlkWords, tma_row, bar0 + 8 * slot);
         }
-    } else {
-        // ------------------------------------------------------ consumer warps
-        const int c = lane & 3, r = lane >> 2;
-        const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
-        const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-        float *table = tables + warp * (kRows * kTableRowBytes / 4);
-        for (int ch = 0; ch < chunks; ++ch) {
-            if (threadIdx.x < kPerChunk) {
-                const int n = ch * kPerChunk + threadIdx.x;
-                long long xo = -1, yo = -1;
-                if (n < cnt) {
-                    if constexpr (MOE) {
-                        const int item = __ldg(ra.perm + off0 + n);
-                        xo = (long long)(ra.x_per_slot ? item : item / ra.topk) * ra.ldx;
-                        yo = (long long)item * ra.ldy;
-                    } else {
-                        xo = (long long)n * ra.ldx;
-                        yo = (long long)n * ra.ldy;
+        __syncwarp();
+        if (lane < nvalid) tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes, &tmX, kb * (kQK / 4), xrow, bar0 + 8 * slot);
+    };
+
+    for (int it = 0; it < SLOTS && it < total; ++it) issue(it);
+
+    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[kRowTiles][NT][4];
+    bool aborted = false;
+    int it = 0;
+    for (int ch = 0; ch < chunks; ++ch) {
+#pragma unroll
+        for (int rt = 0; rt < kRowTiles; ++rt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[rt][nt][q] = 0.0f;
+        const int nvalid = min(kPerChunk, cnt - ch * kPerChunk);
+        bool live[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) live[nt] = nt * 8 + r < nvalid;
+
+        for (int j = 0; j < nblk && !aborted; ++j, ++it) {
+            const int slot = it % SLOTS;
+            // every lane observes the copy's completion; the decision to go on is warp-uniform
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * slot, (it / SLOTS) & 1, status))) {
+                aborted = true;
+                if (lane == 0) atomicExch(&abort_flag, 1);
+                break;
+            }
+            const uint8_t *wst = region + slot * sbytes;
+            const uint8_t *xs = wst + kBlkWBytes;
+            decode_scales(wst + lane * kBlockBytes, table + lane * (kTableRowBytes / 4));
+            __syncwarp();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                // activations for sub-blocks 2g (xl) and 2g+1 (xh), per 8-token tile
+                uint32_t xl[NT][4], xh[NT][4];
+                float sl[NT][4], sh[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+                    if (live[nt]) {
+                        const uint8_t *xp = xs + (nt * 8 + r) * kXBlkBytes + 128 * g + 16 * c;
+                        a = *reinterpret_cast<const uint4 *>(xp);
+                        b = *reinterpret_cast<const uint4 *>(xp + 64);
+                    }
+                    xl[nt][0] = a.x; xl[nt][1] = a.y; xl[nt][2] = a.z; xl[nt][3] = a.w;
+                    xh[nt][0] = b.x; xh[nt][1] = b.y; xh[nt][2] = b.z; xh[nt][3] = b.w;
+                    mma_bf16_16816(sl[nt], ones, xl[nt][0], xl[nt][1], zero4);
+                    mma_bf16_16816(sl[nt], ones, xl[nt][2], xl[nt][3], sl[nt]);
+                    mma_bf16_16816(sh[nt], ones, xh[nt][0], xh[nt][1], zero4);
+                    mma_bf16_16816(sh[nt], ones, xh[nt][2], xh[nt][3], sh[nt]);
+                }
+#pragma unroll
+                for (int rt = 0; rt < kRowTiles; ++rt) {
+                    const int rA = rt * 16 + r, rB = rA + 8;
+                    const uint2 wa = *reinterpret_cast<const uint2 *>(wst + rA * kBlockBytes + 16 + 32 * g + 8 * c);
+                    const uint2 wb = *reinterpret_cast<const uint2 *>(wst + rB * kBlockBytes + 16 + 32 * g + 8 * c);
+                    uint32_t alo0[4], alo1[4], ahi0[4], ahi1[4];
+                    // word 0 (elements 8c..8c+3) feeds MMA 0, word 1 (8c+4..8c+7) MMA 1
+                    unpack_word(wa.x, alo0[0], alo0[2], ahi0[0], ahi0[2]);
+                    unpack_word(wb.x, alo0[1], alo0[3], ahi0[1], ahi0[3]);
+                    unpack_word(wa.y, alo1[0], alo1[2], ahi1[0], ahi1[2]);
+                    unpack_word(wb.y, alo1[1], alo1[3], ahi1[1], ahi1[3]);
+                    const float4 sa = *reinterpret_cast<const float4 *>(table + rA * (kTableRowBytes / 4) + 4 * g);
+                    const float4 sb = *reinterpret_cast<const float4 *>(table + rB * (kTableRowBytes / 4) + 4 * g);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float cl[4], chh[4];
+                        mma_bf16_16816(cl, alo0, xl[nt][0], xl[nt][1], zero4);
+                        mma_bf16_16816(cl, alo1, xl[nt][2], xl[nt][3], cl);
+                        mma_bf16_16816(chh, ahi0, xh[nt][0], xh[nt][1], zero4);
+                        mma_bf16_16816(chh, ahi1, xh[nt][2], xh[nt][3], chh);
+                        float *a4 = acc[rt][nt];
+                        // sub-block 2g, then 2g+1; accumulators 1 and 3 hold odd tokens
+                        a4[0] = fmaf(sa.x, cl[0], a4[0]); a4[0] = fmaf(-sa.y, sl[nt][0], a4[0]);
+                        a4[2] = fmaf(sb.x, cl[2], a4[2]); a4[2] = fmaf(-sb.y, sl[nt][2], a4[2]);
+                        a4[0] = fmaf(sa.z, chh[0], a4[0]); a4[0] = fmaf(-sa.w, sh[nt][0], a4[0]);
+                        a4[2] = fmaf(sb.z, chh[2], a4[2]); a4[2] = fmaf(-sb.w, sh[nt][2], a4[2]);
+                        if constexpr (!ONE) {
+                            a4[1] = fmaf(sa.x, cl[1], a4[1]); a4[1] = fmaf(-sa.y, sl[nt][1], a4[1]);
+                            a4[3] = fmaf(sb.x, cl[3], a4[3]); a4[3] = fmaf(-sb.y, sl[nt][3], a4[3]);
+                            a4[1] = fmaf(sa.z, chh[1], a4[1]); a4[1] = fmaf(-sa.w, sh[nt][1], a4[1]);
+                            a4[3] = fmaf(sb.z, chh[3], a4[3]); a4[3] = fmaf(-sb.w, sh[nt][3], a4[3]);
+                        }
                     }
                 }
-                xoff_s[threadIdx.x] = xo;
-                yoff_s[threadIdx.x] = yo;
             }
-            consumer_bar();
-            long long xrow[NT];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) xrow[nt] = xoff_s[nt * 8 + r];
+            // the slot is consumed: order the reads before the copy that refills it
+            __syncwarp();
+            fence_proxy_async_smem();
+            if (it + SLOTS < total) issue(it + SLOTS);
+        }
+        if constexpr (MOE) {
+            // reduce this chunk across the warps (warp order) and store it
+            float *red_w = reinterpret_cast<float *>(smem + red_off(nx, SLOTS));  // [4][16][kRows]
+            float *mine = red_w + warp * 16 * kRows;
 #pragma unroll
             for (int rt = 0; rt < kRowTiles; ++rt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[rt][nt][i] = 0.0f;
-
-            for (int i = 0; i < nst; ++i) {
-                const int it = ch * nst + i;
-                const int slot = it % kStages;
-                // every lane observes the stage's completion; the decision to go on is warp-uniform
-                const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * slot, (it / kStages) & 1, status));
-                if (!ok && lane == 0) atomicExch(&abort_flag, 1);
-                if (__any_sync(0xFFFFFFFFu, *(volatile int *)&abort_flag != 0)) break;
-                const int kb = (st0 + i) * kBlocksPerStage + warp;
-                if (kb < KB) {
-                    const uint8_t *stage = stages + slot * kStageBytes + warp * kBlockBytes;
-                    decode_scales(stage + lane * kStageRowBytes, table + lane * (kTableRowBytes / 4));
-                    __syncwarp();
-#pragma unroll 1
-                    for (int g = 0; g < 4; ++g) {
-                        // activations for sub-blocks 2g (xl) and 2g+1 (xh), per 8-token tile
-                        uint32_t xl[NT][4], xh[NT][4];
-                        float sl[NT][4], sh[NT][4];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-                            if (xrow[nt] >= 0) {
-                                const uint16_t *xp = ra.x + xrow[nt] + (int64_t)kb * kQK + 64 * g + 8 * c;
-                                a = __ldg(reinterpret_cast<const uint4 *>(xp));
-                                b = __ldg(reinterpret_cast<const uint4 *>(xp + 32));
-                            }
-                            xl[nt][0] = a.x; xl[nt][1] = a.y; xl[nt][2] = a.z; xl[nt][3] = a.w;
-                            xh[nt][0] = b.x; xh[nt][1] = b.y; xh[nt][2] = b.z; xh[nt][3] = b.w;
-                            mma_bf16_16816(sl[nt], ones, xl[nt][0], xl[nt][1], zero4);
-                            mma_bf16_16816(sl[nt], ones, xl[nt][2], xl[nt][3], sl[nt]);
-                            mma_bf16_16816(sh[nt], ones, xh[nt][0], xh[nt][1], zero4);
-                            mma_bf16_16816(sh[nt], ones, xh[nt][2], xh[nt][3], sh[nt]);
-                        }
-#pragma unroll
-                        for (int rt = 0; rt < kRowTiles; ++rt) {
-                            const int rA = rt * 16 + r, rB = rA + 8;
-                            const uint2 wa =
-                                *reinterpret_cast<const uint2 *>(stage + rA * kStageRowBytes + 16 + 32 * g + 8 * c);
-                            const uint2 wb =
-                                *reinterpret_cast<const uint2 *>(stage + rB * kStageRowBytes + 16 + 32 * g + 8 * c);
-                            uint32_t alo0[4], alo1[4], ahi0[4], ahi1[4];
-                            // word 0 (elements 8c..8c+3) feeds MMA 0, word 1 (8c+4..8c+7) MMA 1
-                            unpack_word(wa.x, alo0[0], alo0[2], ahi0[0], ahi0[2]);
-                            unpack_word(wb.x, alo0[1], alo0[3], ahi0[1], ahi0[3]);
-                            unpack_word(wa.y, alo1[0], alo1[2], ahi1[0], ahi1[2]);
-                            unpack_word(wb.y, alo1[1], alo1[3], ahi1[1], ahi1[3]);
-                            const float4 sa =
-                                *reinterpret_cast<const float4 *>(table + rA * (kTableRowBytes / 4) + 4 * g);
-                            const float4 sb =
-                                *reinterpret_cast<const float4 *>(table + rB * (kTableRowBytes / 4) + 4 * g);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                float cl[4], chh[4];
-                                mma_bf16_16816(cl, alo0, xl[nt][0], xl[nt][1], zero4);
-                                mma_bf16_16816(cl, alo1, xl[nt][2], xl[nt][3], cl);
-                                mma_bf16_16816(chh, ahi0, xh[nt][0], xh[nt][1], zero4);
-                                mma_bf16_16816(chh, ahi1, xh[nt][2], xh[nt][3], chh);
-                                float *a4 = acc[rt][nt];
-                                // sub-block 2g
-                                a4[0] = fmaf(sa.x, cl[0], a4[0]); a4[0] = fmaf(-sa.y, sl[nt][0], a4[0]);
-                                a4[1] = fmaf(sa.x, cl[1], a4[1]); a4[1] = fmaf(-sa.y, sl[nt][1], a4[1]);
-                                a4[2] = fmaf(sb.x, cl[2], a4[2]); a4[2] = fmaf(-sb.y, sl[nt][2], a4[2]);
-                                a4[3] = fmaf(sb.x, cl[3], a4[3]); a4[3] = fmaf(-sb.y, sl[nt][3], a4[3]);
-                                // sub-block 2g+1
-                                a4[0] = fmaf(sa.z, chh[0], a4[0]); a4[0] = fmaf(-sa.w, sh[nt][0], a4[0]);
-                                a4[1] = fmaf(sa.z, chh[1], a4[1]); a4[1] = fmaf(-sa.w, sh[nt][1], a4[1]);
-                                a4[2] = fmaf(sb.z, chh[2], a4[2]); a4[2] = fmaf(-sb.w, sh[nt][2], a4[2]);
-                                a4[3] = fmaf(sb.z, chh[3], a4[3]); a4[3] = fmaf(-sb.w, sh[nt][3], a4[3]);
-                            }
-                        }
-                    }
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int rA = rt * 16 + r, tk = nt * 8 + 2 * c;
+                    mine[tk * kRows + rA] = acc[rt][nt][0];
+                    mine[(tk + 1) * kRows + rA] = acc[rt][nt][1];
+                    mine[tk * kRows + rA + 8] = acc[rt][nt][2];
+                    mine[(tk + 1) * kRows + rA + 8] = acc[rt][nt][3];
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            if (threadIdx.x < kPerChunk) {
+                int xr;
+                long long yo;
+                slot_rows<MOE>(ra, off0, cnt, ch * kPerChunk + threadIdx.x, xr, yo);
+                yoff_s[threadIdx.x] = yo;
             }
-            if constexpr (MOE) {
-                // reduce this chunk across the consumer warps (warp order) and store it
-                float *red_w = moe_red;  // [4][16][kRows]
-                float *mine = red_w + warp * 16 * kRows;
-#pragma unroll
-                for (int rt = 0; rt < kRowTiles; ++rt)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int rA = rt * 16 + r, tk = nt * 8 + 2 * c;
-                        mine[tk * kRows + rA] = acc[rt][nt][0];
-                        mine[(tk + 1) * kRows + rA] = acc[rt][nt][1];
-                        mine[tk * kRows + rA + 8] = acc[rt][nt][2];
-                        mine[(tk + 1) * kRows + rA + 8] = acc[rt][nt][3];
-                    }
-                consumer_bar();
-                const int valid = min(kPerChunk, cnt - ch * kPerChunk);
-                for (int e2 = threadIdx.x; e2 < valid * kRows; e2 += 128) {
+            __syncthreads();
+            if (!*(volatile int *)&abort_flag) {
+                for (int e2 = threadIdx.x; e2 < nvalid * kRows; e2 += kThreads) {
                     float v = red_w[e2];
 #pragma unroll
-                    for (int w = 1; w < kConsumerWarps; ++w) v += red_w[w * 16 * kRows + e2];
+                    for (int w = 1; w < kWarps; ++w) v += red_w[w * 16 * kRows + e2];
                     const int tk = e2 / kRows, rr = e2 % kRows;
                     if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = v;
                 }
-                consumer_bar();  // red_w and the token table are reused by the next chunk
             }
+            __syncthreads();  // red_w and the token table are reused by the next chunk
         }
     }
     if constexpr (MOE) return;
 
-    __syncthreads();  // all stages consumed: the stage buffers become reduction space
+    __syncthreads();  // all slots consumed: the rings become reduction space
     // per-warp partials, laid out [token][row] so that the final stores coalesce
-    float *red_w = reinterpret_cast<float *>(stages);  // [4][16][kRows]
-    float *red = red_w + kConsumerWarps * 16 * kRows;   // [16][kRows]
-    if (warp < kConsumerWarps) {
-        const int c = lane & 3, r = lane >> 2;
+    float *red_w = reinterpret_cast<float *>(smem);  // [4][16][kRows]
+    float *red = red_w + kWarps * 16 * kRows;         // [16][kRows]
+    {
         float *mine = red_w + warp * 16 * kRows;
 #pragma unroll
         for (int rt = 0; rt < kRowTiles; ++rt)
@@ -325,12 +342,13 @@ __global__ void __launch_bounds__(kThreads, 4) smallm_kernel(const __grid_consta
                 mine[(tk + 1) * kRows + rA + 8] = acc[rt][nt][3];
             }
     }
+    if (threadIdx.x < 16) yoff_s[threadIdx.x] = (long long)threadIdx.x * ra.ldy;
     __syncthreads();
     const int elems = cnt * kRows;
     for (int e = threadIdx.x; e < elems; e += kThreads) {
         float v = red_w[e];
 #pragma unroll
-        for (int w = 1; w < kConsumerWarps; ++w) v += red_w[w * 16 * kRows + e];
+        for (int w = 1; w < kWarps; ++w) v += red_w[w * 16 * kRows + e];
         red[e] = v;
     }
     if (S > 1) {
@@ -354,17 +372,14 @@ __global__ void __launch_bounds__(kThreads, 4) smallm_kernel(const __grid_consta
     }
 }
 
-}  // namespace
-
-namespace {
-
-template <int NT, bool MOE>
-cudaError_t launch_cfg(int S, int tiles, int E, size_t smem, cudaStream_t s, const CUtensorMap &tm,
-                       const RowArgs &ra, int N, int KB, unsigned int *status) {
+template <int NT, bool MOE, bool ONE, int SLOTS>
+cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
+                       const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
+    const int smem = smem_total(nx, SLOTS, MOE);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, tiles, E);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -373,21 +388,20 @@ cudaError_t launch_cfg(int S, int tiles, int E, size_t smem, cudaStream_t s, con
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = S > 1 ? 1 : 0;
-    cudaError_t e = cudaFuncSetAttribute(smallm_kernel<NT, MOE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, smallm_kernel<NT, MOE>, tm, ra, N, KB, status);
+    e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, ra, N, KB, nx, status);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-int split_for(const DeviceInfo &di, int64_t units, int KB) {
-    // Split K across a cluster only when the row tiles cannot fill the GPU at the
-    // design occupancy of 4 CTAs per SM.  Depends on (N, K, device), never on M.
-    const int n_stage_total = (KB + kBlocksPerStage - 1) / kBlocksPerStage;
-    int64_t S = (4 * (int64_t)di.sm_count) / (units > 0 ? units : 1);
+// Split K across a cluster only when the row tiles cannot fill the GPU at the
+// four CTAs per SM that fit for M <= 4.  Depends on (N, K, device), never on M.
+int split_for(const DeviceInfo &di, int64_t tiles, int KB) {
+    int64_t S = (4 * (int64_t)di.sm_count) / (tiles > 0 ? tiles : 1);
     if (S > 8) S = 8;
-    if (S > n_stage_total) S = n_stage_total;
+    if (S > KB / kWarps) S = KB / kWarps;  // keep at least one block per warp
     if (S < 1) S = 1;
     return (int)S;
 }
@@ -396,35 +410,41 @@ int split_for(const DeviceInfo &di, int64_t units, int KB) {
 
 cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                           int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
-    CUtensorMap tm;
-    cudaError_t e = make_weight_tmap(&tm, w, N, K, kRows, kStageWords);
+    CUtensorMap tmW, tmX;
+    cudaError_t e = make_weight_tmap(&tmW, w, N, K, kRows, kBlkWords);
+    if (e != cudaSuccess) return e;
+    e = make_act_tmap(&tmX, x, M, K, ldx, kQK / 4);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const int tiles = (int)((N + kRows - 1) / kRows);
     const int S = split_for(di, tiles, KB);
     RowArgs ra = {};
-    ra.x = x; ra.ldx = ldx; ra.y = y; ra.ldy = ldy; ra.M = (int)M;
-    const size_t smem = smem_bytes();
-    if (M <= 8) return launch_cfg<1, false>(S, tiles, 1, smem, s, tm, ra, (int)N, KB, di.status);
-    return launch_cfg<2, false>(S, tiles, 1, smem, s, tm, ra, (int)N, KB, di.status);
+    ra.y = y; ra.ldy = ldy; ra.M = (int)M;
+    const int nx = (int)M;
+    if (M == 1) return launch_cfg<1, false, true, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
+    if (M <= 4) return launch_cfg<1, false, false, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
+    if (M <= 8) return launch_cfg<1, false, false, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
+    return launch_cfg<2, false, false, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
 }
 
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               int64_t T, int topk, float *out, cudaStream_t s) {
-    CUtensorMap tm;
+    CUtensorMap tmW, tmX;
     // all experts stacked: E*N rows of the same pitch
-    cudaError_t e = make_weight_tmap(&tm, w_experts, (int64_t)E * N, K, kRows, kStageWords);
+    cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kRows, kBlkWords);
+    if (e != cudaSuccess) return e;
+    e = make_act_tmap(&tmX, x, x_per_slot ? T * topk : T, K, K, kQK / 4);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const int tiles = (int)((N + kRows - 1) / kRows);
     RowArgs ra = {};
-    ra.x = x; ra.ldx = K; ra.y = out; ra.ldy = N; ra.M = 0;
+    ra.y = out; ra.ldy = N; ra.M = 0;
     ra.x_per_slot = x_per_slot; ra.topk = topk; ra.perm = perm; ra.offsets = offsets;
-    const size_t smem = smem_bytes() + kConsumerWarps * 16 * kRows * 4;
     const int64_t items = T * topk;
-    if (items <= 64 * (int64_t)E) return launch_cfg<1, true>(1, tiles, E, smem, s, tm, ra, (int)N, KB, di.status);
-    return launch_cfg<2, true>(1, tiles, E, smem, s, tm, ra, (int)N, KB, di.status);
+    if (items <= 64 * (int64_t)E)
+        return launch_cfg<1, true, false, 3>(1, tiles, E, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
+    return launch_cfg<2, true, false, 2>(1, tiles, E, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
 }
 
 }  // namespace q4k
