@@ -109,6 +109,28 @@ cudaError_t make_act_tmap(CUtensorMap *m, const void *x, int64_t rows, int64_t K
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Activations [rows][ld] bf16 for the tensor-core path: dims {K, rows}, box {64,
+// box_rows}, 128-byte swizzle (the K-major operand layout tcgen05.mma reads).
+cudaError_t make_act_tmap_sw128(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_rows) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace q4k
 
 using namespace q4k;
@@ -210,11 +232,8 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
     q4k_status st = check_device(&di);
     if (st != Q4K_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaSuccess;
-    for (int64_t m0 = 0; m0 < M && e == cudaSuccess; m0 += 16) {
-        const int64_t mc = (M - m0) < 16 ? (M - m0) : 16;
-        e = launch_smallm(di, w, N, K, x + m0 * ldx, mc, ldx, y + m0 * ldy, ldy, s);
-    }
+    const cudaError_t e = M <= 16 ? launch_smallm(di, w, N, K, x, M, ldx, y, ldy, s)
+                                  : launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 

@@ -1,0 +1,272 @@
+// Prefill Q4_K GEMM on the tcgen05 tensor cores.
+//
+// A GGUF target dequantizes Q4_K "into the matrix-multiply operand on every
+// prefill pass"; that fixed cost dominates at 128 tokens and is amortized by 4k
+// (sparkinfer-server README, "Serve a GGUF instead of NVFP4").  This kernel does
+// exactly that, tile by tile, without ever writing a dequantized matrix to HBM:
+//
+//   * A CTA owns 128 weight rows x BN tokens (BN = 256, or 128 for short
+//     prompts).  The weight rows are the MMA's M dimension, the tokens its N.
+//   * Warp 0 (TMA): per 256-wide K block, one bulk-tensor copy of the raw Q4_K
+//     tile (128 rows x 144 bytes) into one of two raw slots; per 64-wide K
+//     stage, one copy of the activation tile (BN tokens x 64 bf16) with the
+//     128-byte swizzle that the tensor core's K-major layout expects.
+//   * Warps 2-5 (dequant): thread t owns weight row t.  For each 64-wide stage
+//     (one Q4_K group: sub-blocks 2g and 2g+1) it turns 32 code bytes into 64
+//     bf16 weights, w = bf16(d*sc) * q - bf16(dmin*m) (one bf16 FMA per pair
+//     after an exact 128+q -> q subtraction), and stores them in the swizzled
+//     K-major layout; a proxy fence publishes them to the tensor core.
+//   * Warp 1 (MMA): one elected thread issues four 128 x BN x 16 tcgen05.mma per
+//     stage into an fp32 accumulator in tensor memory and commits each stage's
+//     completion to the barrier that frees the stage.
+//   * Warps 2-5 then read the accumulator (tcgen05.ld, one 32-lane quarter per
+//     warp) and store fp32 rows of y with coalesced 128-byte writes.
+// Every wait is bounded; the accumulator is a plain sum per output element in a
+// fixed order, so the result is run-to-run deterministic.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "q4k_internal.h"
+#include "q4k_ptx.cuh"
+
+namespace q4k {
+namespace {
+
+constexpr int kTileRows = 128;                    // weight rows per CTA (MMA M)
+constexpr int kStageK = 64;                       // K per pipeline stage (one swizzle row of bf16)
+constexpr int kABytes = kTileRows * kStageK * 2;  // 16 KiB dequantized operand per stage
+constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K tile per block
+constexpr int kThreads = 192;
+
+template <int BN>
+struct Cfg {
+    static constexpr int NS = BN == 256 ? 3 : 4;  // pipeline stages
+    static constexpr int XB = BN * kStageK * 2;   // activation bytes per stage
+    static constexpr int x_off = 0;
+    static constexpr int a_off = NS * XB;
+    static constexpr int raw_off = a_off + NS * kABytes;
+    static constexpr int bar_off = raw_off + 2 * kRawBytes;
+    static constexpr int n_bars = 2 * NS + 5;
+    static constexpr int misc_off = bar_off + n_bars * 8;
+    static constexpr int bytes = misc_off + 16 + 1024;  // + slack to align the base to 1024
+};
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<__nv_bfloat162 *>(&u); }
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
+
+// 128+q pairs (natural element order) of one 32-bit word of codes
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t &lo23, uint32_t &hi01,
+                                            uint32_t &hi23) {
+    const uint32_t t01 = prmt(w, 0u, 0x4140u);
+    const uint32_t t23 = prmt(w, 0u, 0x4342u);
+    lo01 = lop3_and_or(t01, 0x000F000Fu, 0x43004300u);
+    lo23 = lop3_and_or(t23, 0x000F000Fu, 0x43004300u);
+    hi01 = lop3_and_or(t01 >> 4, 0x000F000Fu, 0x43004300u);
+    hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                              const __grid_constant__ CUtensorMap tmX, float *y,
+                                                              int64_t ldy, int M, int N, int KB,
+                                                              unsigned int *status) {
+    using C = Cfg<BN>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *xs = base + C::x_off;
+    uint8_t *as = base + C::a_off;
+    uint8_t *raw = base + C::raw_off;
+    const uint32_t bar = smem_u32(base + C::bar_off);
+    const uint32_t full0 = bar, empty0 = bar + 8 * NS, rfull0 = bar + 16 * NS, rempty0 = rfull0 + 16,
+                   accfull = rempty0 + 16;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + C::misc_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::misc_off + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTileRows;
+    const int m0 = blockIdx.y * BN;
+    const int total = KB * 4;  // 64-wide stages
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full0 + 8 * s, 1 + 4);  // producer (+ tx bytes) and the four dequant warps
+            mbar_init(empty0 + 8 * s, 1);     // tcgen05.commit
+        }
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(rfull0 + 8 * r, 1);
+            mbar_init(rempty0 + 8 * r, 4);
+        }
+        mbar_init(accfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), BN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------- TMA
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
+            mbar_arrive_expect_tx(rfull0, kRawBytes);
+            tma_load_2d(smem_u32(raw), &tmW, 0, n0, rfull0);
+            for (int i = 0; i < total && !*abort_flag; ++i) {
+                const int kb = i >> 2, g = i & 3, s = i % NS;
+                if (g == 0 && kb + 1 < KB) {  // raw tile of the next block, one block ahead
+                    const int r = (kb + 1) & 1;
+                    if (kb + 1 >= 2 && !mbar_wait(rempty0 + 8 * r, (((kb + 1) >> 1) - 1) & 1, status)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
+                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kb + 1) * (kBlockBytes / 4), n0,
+                                rfull0 + 8 * r);
+                }
+                if (i >= NS && !mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(full0 + 8 * s, C::XB);
+                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, kb * kQK + kStageK * g, m0, full0 + 8 * s);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16_f32(kTileRows, BN);
+            bool ok = true;
+            for (int i = 0; i < total; ++i) {
+                const int s = i % NS;
+                if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kABytes));
+                const uint64_t bd = umma_desc_sw128(smem_u32(xs + s * C::XB));
+#pragma unroll
+                for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
+                    umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
+                umma_commit(empty0 + 8 * s);
+            }
+            if (ok) umma_commit(accfull);
+        }
+    } else {
+        // ---------------------------------------------------- dequant warps
+        const int t = threadIdx.x - 64;  // weight row within the tile
+        const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
+        bool ok = true;
+        for (int kb = 0; kb < KB && ok; ++kb) {
+            const int r = kb & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(rfull0 + 8 * r, (kb >> 1) & 1, status))) {
+                ok = false;
+                break;
+            }
+            const uint8_t *rowp = raw + r * kRawBytes + t * kBlockBytes;
+            const uint4 h = *reinterpret_cast<const uint4 *>(rowp);
+            const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
+            const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+            const uint32_t sc_lo = h.y & 0x3F3F3F3Fu, m_lo = h.z & 0x3F3F3F3Fu;
+            const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+            const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+            for (int g = 0; g < 4; ++g) {
+                const int i = kb * 4 + g, s = i % NS;
+                if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status))) {
+                    ok = false;
+                    break;
+                }
+                // scales of sub-blocks 2g (low nibbles) and 2g+1 (high nibbles)
+                const uint32_t scw = g < 2 ? sc_lo : sc_hi, mw = g < 2 ? m_lo : m_hi;
+                const int b0 = (2 * g) & 3, b1 = (2 * g + 1) & 3;
+                const float dsc0 = d * (float)((scw >> (8 * b0)) & 0xFFu), dm0 = dmin * (float)((mw >> (8 * b0)) & 0xFFu);
+                const float dsc1 = d * (float)((scw >> (8 * b1)) & 0xFFu), dm1 = dmin * (float)((mw >> (8 * b1)) & 0xFFu);
+                const __nv_bfloat162 s0 = __floats2bfloat162_rn(dsc0, dsc0), n0v = __floats2bfloat162_rn(-dm0, -dm0);
+                const __nv_bfloat162 s1 = __floats2bfloat162_rn(dsc1, dsc1), n1v = __floats2bfloat162_rn(-dm1, -dm1);
+                const uint4 qa = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g);
+                const uint4 qb = *reinterpret_cast<const uint4 *>(rowp + 32 + 32 * g);
+                const uint32_t wds[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                uint8_t *arow = as + s * kABytes + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // chunk j: elements 8j..8j+7 of each sub-block
+                    uint32_t lo[4], hi[4];
+                    unpack_word(wds[2 * j], lo[0], lo[1], hi[0], hi[1]);
+                    unpack_word(wds[2 * j + 1], lo[2], lo[3], hi[2], hi[3]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        lo[q] = as_u32(__hfma2(__hsub2(as_bf2(lo[q]), k128), s0, n0v));
+                        hi[q] = as_u32(__hfma2(__hsub2(as_bf2(hi[q]), k128), s1, n1v));
+                    }
+                    *reinterpret_cast<uint4 *>(arow + ((j ^ (t & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4 *>(arow + (((j + 4) ^ (t & 7)) << 4)) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+                fence_proxy_async_smem();  // make the stores visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full0 + 8 * s);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rempty0 + 8 * r);
+        }
+        if (!ok && lane == 0) *abort_flag = 1;
+        // ------------------------------------------------------- epilogue
+        if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(accfull, 0, status))) {
+            tc_fence_after();
+            const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+            const int n = n0 + 32 * q + lane;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
+                tmem_ld_wait();
+                if (n < N) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = m0 + 32 * cc + j;
+                        if (m < M) y[(int64_t)m * ldy + n] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, BN);
+    }
+}
+
+template <int BN>
+cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
+                      int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
+    CUtensorMap tmW, tmX;
+    cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
+    if (e != cudaSuccess) return e;
+    e = make_act_tmap_sw128(&tmX, x, M, K, ldx, BN);
+    if (e != cudaSuccess) return e;
+    const int smem = Cfg<BN>::bytes;
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), 1);
+    gemm_tc_kernel<BN><<<grid, kThreads, smem, s>>>(tmW, tmX, y, ldy, (int)M, (int)N, (int)(K / kQK), di.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
+                           int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
+    if (M <= 128) return launch_bn<128>(di, w, N, K, x, M, ldx, y, ldy, s);
+    return launch_bn<256>(di, w, N, K, x, M, ldx, y, ldy, s);
+}
+
+}  // namespace q4k

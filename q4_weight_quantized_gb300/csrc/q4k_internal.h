@@ -31,6 +31,10 @@ cudaError_t launch_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *o
 cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                           int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
 
+// M > 16: per-tile dequantization into shared memory + tcgen05 MMA (gemm_tc.cu)
+cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
+                           int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
+
 // MoE: all experts stacked as E*N rows; rows of x and of out are chosen through
 // the routing permutation (perm/offsets from launch_moe_route).
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
@@ -54,5 +58,8 @@ cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K
 // TMA descriptor of bf16 activations [rows][ld] viewed as uint64 (4 activations
 // each): dims {K/4, rows}, box {box_elems, 1} = one row segment of 4*box_elems.
 cudaError_t make_act_tmap(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_elems);
+
+// bf16 activations [rows][ld], box {64, box_rows}, 128-byte swizzle (tcgen05 operand)
+cudaError_t make_act_tmap_sw128(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_rows);
 
 }  // namespace q4k
