@@ -187,6 +187,37 @@ q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_
                                 int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk,
                                 float *y, int y_mode, void *ws, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------- allocation-free MoE --
+ * No counterpart on the pages: an addition for callers that cannot provide a
+ * workspace - code that must not call cudaMalloc/cudaFree (they synchronize the
+ * whole device), engines that hand all device memory to their own pools at
+ * start-up, and foreign-language callers that only pass buffers they own.
+ *
+ * q4k_moe_grouped_gemm_noalloc computes exactly what q4k_moe_grouped_gemm
+ * computes (same arguments, same kernels, same bits) but takes no workspace:
+ * its scratch is a fixed array of Q4K_MOE_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library keeps allocated until the
+ * process exits.  It allocates nothing itself.
+ *   - The first call on a device looks up that device's scratch address
+ *     (cudaGetSymbolAddress, with the device current).  Make that first call
+ *     before capturing a stream into a CUDA graph.
+ *   - Every call on a device shares the one array.  Calls whose kernels can
+ *     overlap on the GPU (different streams without ordering between them) race
+ *     on it and give wrong results; order them on one stream.
+ *   - The array keeps the last call's contents; nothing in it needs to start at
+ *     zero, because each call writes every scratch byte it later reads.
+ *   - A request whose scratch need, q4k_moe_workspace_size(n_experts, N, K, T,
+ *     topk, y_mode), exceeds Q4K_MOE_NOALLOC_SCRATCH_BYTES fails with
+ *     Q4K_ERR_WORKSPACE before anything is launched.  With Q4K_MOE_Y_PER_SLOT the
+ *     need is only the routing (about 4*(E + T*topk) bytes); with
+ *     Q4K_MOE_Y_COMBINE it adds 4*T*topk*N bytes (for example T = 64, topk = 8,
+ *     N = 2048 needs 4 MiB).
+ * Other errors are those of q4k_moe_grouped_gemm. */
+#define Q4K_MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+q4k_status q4k_moe_grouped_gemm_noalloc(const void *w_experts, int32_t n_experts, int64_t N, int64_t K,
+                                        const uint16_t *x, int x_mode, const int32_t *topk_ids, const float *gates,
+                                        int64_t T, int32_t topk, float *y, int y_mode, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,8 +26,11 @@ QK = 256
 EXPORTS = (
     "q4k_status_string", "q4k_last_cuda_error", "q4k_row_bytes", "q4k_version", "q4k_check_device",
     "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
-    "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm",
+    "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_noalloc",
 )
+
+# fixed scratch capacity of q4k_moe_grouped_gemm_noalloc (Q4K_MOE_NOALLOC_SCRATCH_BYTES)
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class Q4KError(RuntimeError):
@@ -64,6 +67,7 @@ def load(path: str | None = None):
         "q4k_moe_route": ([P, i64, i32, i32, P, P, P], st),
         "q4k_moe_workspace_size": ([i32, i64, i64, i64, i32, st], sz),
         "q4k_moe_grouped_gemm": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P, sz, P], st),
+        "q4k_moe_grouped_gemm_noalloc": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -155,3 +159,14 @@ def q4k_moe_grouped_gemm(w_experts, n_experts: int, N: int, K: int, x, x_mode: i
     _check(load().q4k_moe_grouped_gemm(_ptr(w_experts), n_experts, N, K, _ptr(x), x_mode, _ptr(topk_ids),
                                        _ptr(gates), T, topk, _ptr(y), y_mode, _ptr(ws), ws_bytes, _stream(stream)),
            "q4k_moe_grouped_gemm")
+
+
+def q4k_moe_grouped_gemm_noalloc(w_experts, n_experts: int, N: int, K: int, x, x_mode: int, topk_ids, gates,
+                                 T: int, topk: int, y, y_mode: int, stream=None) -> None:
+    """q4k_moe_grouped_gemm without a workspace: for callers that cannot allocate.
+    Its scratch is a fixed array inside the library (MOE_NOALLOC_SCRATCH_BYTES per
+    GPU); calls that overlap on the GPU share it and race, so keep them on one
+    stream, and make the first call on a device before any CUDA graph capture."""
+    _check(load().q4k_moe_grouped_gemm_noalloc(_ptr(w_experts), n_experts, N, K, _ptr(x), x_mode, _ptr(topk_ids),
+                                               _ptr(gates), T, topk, _ptr(y), y_mode, _stream(stream)),
+           "q4k_moe_grouped_gemm_noalloc")
