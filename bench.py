@@ -360,7 +360,8 @@ def run_gpu(args, rank, local_rank, world):
     # per-kernel durations from the last replay of every graph
     kernel_ms = None
     if ext:
-        per = [[gevents[r][i].elapsed_time(gevents[r][i + 1]) for r in range(gr.R)] for i in range(n_marks - 1)]
+        replayed = range(min(gr.R, args.steps))  # graphs whose events were recorded in the timed region
+        per = [[gevents[r][i].elapsed_time(gevents[r][i + 1]) for r in replayed] for i in range(n_marks - 1)]
         kernel_ms = [statistics.mean(p) for p in per]
 
     if world > 1:

@@ -21,6 +21,11 @@
 //     completion to the barrier that frees the stage.
 //   * Warps 2-5 then read the accumulator (tcgen05.ld, one 32-lane quarter per
 //     warp) and store fp32 rows of y with coalesced 128-byte writes.
+//   * When the output has too few tiles to occupy the GPU (short prompts on the
+//     narrow down projection), a thread-block cluster splits K: each CTA parks
+//     its partial tile in its idle stage buffers and every rank sums one slice of
+//     columns over the cluster's distributed shared memory, in rank order - no
+//     workspace, no atomics.
 // Every wait is bounded; the accumulator is a plain sum per output element in a
 // fixed order, so the result is run-to-run deterministic.
 #include <cuda.h>
@@ -87,7 +92,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileRows;
     const int m0 = blockIdx.y * BN;
-    const int total = KB * 4;  // 64-wide stages
+    // split K over a cluster of gridDim.z CTAs: this CTA takes blocks [kbeg, kbeg + KBs)
+    const int S = gridDim.z, split = blockIdx.z;
+    const int kbeg = (int)((int64_t)KB * split / S);
+    const int KBs = (int)((int64_t)KB * (split + 1) / S) - kbeg;
+    const int total = KBs * 4;  // 64-wide stages
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -117,17 +126,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
             mbar_arrive_expect_tx(rfull0, kRawBytes);
-            tma_load_2d(smem_u32(raw), &tmW, 0, n0, rfull0);
+            tma_load_2d(smem_u32(raw), &tmW, kbeg * (kBlockBytes / 4), n0, rfull0);
             for (int i = 0; i < total && !*abort_flag; ++i) {
                 const int kb = i >> 2, g = i & 3, s = i % NS;
-                if (g == 0 && kb + 1 < KB) {  // raw tile of the next block, one block ahead
+                if (g == 0 && kb + 1 < KBs) {  // raw tile of the next block, one block ahead
                     const int r = (kb + 1) & 1;
                     if (kb + 1 >= 2 && !mbar_wait(rempty0 + 8 * r, (((kb + 1) >> 1) - 1) & 1, status)) {
                         *abort_flag = 1;
                         break;
                     }
                     mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
-                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kb + 1) * (kBlockBytes / 4), n0,
+                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kbeg + kb + 1) * (kBlockBytes / 4), n0,
                                 rfull0 + 8 * r);
                 }
                 if (i >= NS && !mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status)) {
@@ -135,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     break;
                 }
                 mbar_arrive_expect_tx(full0 + 8 * s, C::XB);
-                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, kb * kQK + kStageK * g, m0, full0 + 8 * s);
+                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, full0 + 8 * s);
             }
         }
     } else if (warp == 1) {
@@ -165,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int t = threadIdx.x - 64;  // weight row within the tile
         const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
         bool ok = true;
-        for (int kb = 0; kb < KB && ok; ++kb) {
+        for (int kb = 0; kb < KBs && ok; ++kb) {
             const int r = kb & 1;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(rfull0 + 8 * r, (kb >> 1) & 1, status))) {
                 ok = false;
@@ -221,13 +230,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(accfull, 0, status))) {
             tc_fence_after();
             const int q = warp & 3;  // tensor-memory lane quarter this warp may read
-            const int n = n0 + 32 * q + lane;
+            const int rl = 32 * q + lane, n = n0 + rl;
+            // with a K split, the partial tile goes to this CTA's (now idle) stage
+            // buffers, column-major [BN][128], for the cluster reduction below
+            float *part = reinterpret_cast<float *>(base);
 #pragma unroll 1
             for (int cc = 0; cc < BN / 32; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
                 tmem_ld_wait();
-                if (n < N) {
+                if (S > 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) part[(32 * cc + j) * kTileRows + rl] = __uint_as_float(v[j]);
+                } else if (n < N) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int m = m0 + 32 * cc + j;
@@ -236,6 +251,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             }
         }
+    }
+    if (S > 1) {
+        // every rank's partial is in its shared memory; rank r sums the columns
+        // [r*BN/S, (r+1)*BN/S) over the ranks in rank order and stores them
+        cluster_sync();
+        if (!*abort_flag) {
+            const int r = (int)cluster_ctarank();
+            const int c0 = BN * r / S, c1 = BN * (r + 1) / S;
+            const uint32_t pbase = smem_u32(base);
+            for (int e = threadIdx.x; e < (c1 - c0) * kTileRows; e += kThreads) {
+                const int c = c0 + e / kTileRows, rr = e % kTileRows;
+                const uint32_t off = pbase + 4u * (uint32_t)(c * kTileRows + rr);
+                float v = 0.0f;
+                for (int qr = 0; qr < S; ++qr) v += ld_shared_cluster_f32(map_shared_rank(off, qr));
+                const int m = m0 + c, n = n0 + rr;
+                if (m < M && n < N) y[(int64_t)m * ldy + n] = v;
+            }
+        }
+        cluster_sync();  // keep every partial alive until all ranks have read it
     }
     tc_fence_before();
     __syncthreads();
@@ -254,10 +288,34 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     e = make_act_tmap_sw128(&tmX, x, M, K, ldx, BN);
     if (e != cudaSuccess) return e;
     const int smem = Cfg<BN>::bytes;
+    static_assert(Cfg<BN>::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers");
     e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), 1);
-    gemm_tc_kernel<BN><<<grid, kThreads, smem, s>>>(tmW, tmX, y, ldy, (int)M, (int)N, (int)(K / kQK), di.status);
+    const int KB = (int)(K / kQK);
+    const int64_t tiles = ((N + kTileRows - 1) / kTileRows) * ((M + BN - 1) / BN);
+    // Split K over a cluster when the output tiles leave more than half of the
+    // SMs idle (one CTA per SM); at least four K blocks per split.
+    int S = 1;
+    if (2 * tiles <= di.sm_count) {
+        int64_t want = di.sm_count / tiles;
+        if (want > 8) want = 8;
+        if (want > KB / 4) want = KB / 4;
+        if (want > 1) S = (int)want;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = S;
+    cfg.attrs = attr;
+    cfg.numAttrs = S > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmW, tmX, y, ldy, (int)M, (int)N, KB, di.status);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

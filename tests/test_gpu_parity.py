@@ -146,6 +146,16 @@ def test_one_hot_column_exact(ref):
         assert np.array_equal(y, w[:, k]), k
 
 
+def test_prefill_deterministic():
+    M, N, K = 128, 5120, 17408   # the cluster split-K path
+    b = G.weights(3, 0, N, K, outliers=True)
+    w = G.dev(b)
+    x = G.activations(3, 1, M, K)
+    a = gpu_gemm(b, N, K, x, w_dev=w)
+    c = gpu_gemm(b, N, K, x, w_dev=w)
+    assert np.array_equal(a.view(np.uint32), c.view(np.uint32))
+
+
 def test_batch_invariance_and_determinism():
     N, K = 17408, 5120
     b = G.weights(2, 0, N, K)
@@ -193,7 +203,16 @@ def test_prefill_small(ref, M):
     assert G.rel_err(gpu_gemm(b, N, K, x), ref.gemm(b, N, K, x, threads=8)) <= TOL_TC
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (1024, 5120, 17408), (4096, 17408, 5120)])
+@pytest.mark.parametrize("M,N,K", [(200, 1000, 4096), (33, 640, 4096)])
+def test_prefill_split_k_ragged(ref, M, N, K):
+    # few output tiles: K is split over a thread-block cluster; ragged M and N
+    b = G.weights(3, 2, N, K, outliers=True)
+    x = G.activations(3, 3, M, K)
+    assert G.rel_err(gpu_gemm(b, N, K, x), ref.gemm(b, N, K, x, threads=16)) <= TOL_TC
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (128, 5120, 17408), (1024, 5120, 17408),
+                                   (4096, 17408, 5120)])
 def test_prefill_full_size(ref, M, N, K):
     b = G.weights(3, 0, N, K, outliers=True)
     x = G.activations(3, 1, M, K)
