@@ -261,6 +261,16 @@ class GpuRunner:
             return 3 * 2 + 1  # route + grouped GEMM for gate, up, down; + combine
         return sum(1 if M <= 16 else -(-M // 16) for (_, _, _, M, _, _) in self.wl.mats)
 
+    def step_one(self, r: int, i: int):
+        """Enqueue only matrix i of the step, with weight set r."""
+        q4k, wl = self.q4k, self.wl
+        _, N, K, M, _, _ = wl.mats[i]
+        if M == 1:
+            q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i])
+        else:
+            ws, wsb = self.ws[i]
+            q4k.q4k_gemm(self.sets[r][i], N, K, self.x[i], M, K, self.y[i], N, ws if wsb else None, wsb)
+
     def step(self, r: int, mark=None):
         """Enqueue one step using weight set r.  mark(i) is called before
         matrix i and after the last one (to record events)."""
@@ -308,7 +318,6 @@ def run_gpu(args, rank, local_rank, world):
     wl = Workload(args.workload, args.m)
     gr = GpuRunner(wl, device)
     stream = torch.cuda.Stream(device)
-    n_marks = (len(wl.mats) + 1) if not wl.moe else 2
 
     # warm the host-side state (descriptors, attributes) before capture
     with torch.cuda.stream(stream):
@@ -317,21 +326,13 @@ def run_gpu(args, rank, local_rank, world):
     torch.cuda.synchronize()
     q4k.q4k_check_device(stream)
 
-    # one graph per weight set; external event nodes time the kernels inside
-    graphs, gevents = [], []
-    try:
-        ev_kw = dict(enable_timing=True, external=True)
-        torch.cuda.Event(**ev_kw)
-        ext = True
-    except TypeError:
-        ev_kw, ext = dict(enable_timing=True), False
+    # one graph per weight set for the timed steps (nothing else in them)
+    graphs = []
     for r in range(gr.R):
         g = torch.cuda.CUDAGraph()
-        evs = [torch.cuda.Event(**ev_kw) for _ in range(n_marks)] if ext else None
         with torch.cuda.graph(g, stream=stream):
-            gr.step(r, mark=(lambda i, evs=evs: evs[i].record()) if ext else None)
+            gr.step(r)
         graphs.append(g)
-        gevents.append(evs)
 
     # warm-up steps
     with torch.cuda.stream(stream):
@@ -357,12 +358,27 @@ def run_gpu(args, rank, local_rank, world):
     ms = t0.elapsed_time(t1)
     q4k.q4k_check_device(stream)
 
-    # per-kernel durations from the last replay of every graph
+    # per-kernel durations: each kernel of the step alone, R launches over the R
+    # weight sets per graph, replayed back to back and timed with CUDA events on
+    # the launching stream (average launch duration, launch gaps included)
     kernel_ms = None
-    if ext:
-        replayed = range(min(gr.R, args.steps))  # graphs whose events were recorded in the timed region
-        per = [[gevents[r][i].elapsed_time(gevents[r][i + 1]) for r in replayed] for i in range(n_marks - 1)]
-        kernel_ms = [statistics.mean(p) for p in per]
+    if not wl.moe:
+        kernel_ms = []
+        for i in range(len(wl.mats)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(gr.R):
+                    gr.step_one(r, i)
+            reps = max(3, min(200, args.steps // gr.R))
+            with torch.cuda.stream(stream):
+                g.replay()
+                k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                k0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                k1.record(stream)
+            torch.cuda.synchronize()
+            kernel_ms.append(k0.elapsed_time(k1) / (reps * gr.R))
 
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=device)
@@ -415,7 +431,8 @@ def run_gpu(args, rank, local_rank, world):
         "config": dict(wl.config, l2="rotating %d weight sets, %.0f MB total > 129 MB L2" %
                        (gr.R, gr.R * (wl.weight_bytes() if not wl.moe else sum(
                            wl.moe[k].nbytes for k in ("gate", "up", "down"))) / 1e6),
-                       parallelism="replicas x%d" % world, timing="CUDA graph per step, CUDA events"),
+                       parallelism="replicas x%d" % world,
+                       timing="CUDA graph per step, CUDA events; kernel times from per-kernel graphs"),
         "gpu_launches": gr.launches_per_step() * args.steps,
     }
     # roofline of the dominant kernel

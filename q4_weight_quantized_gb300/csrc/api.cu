@@ -259,14 +259,22 @@ q4k_status q4k_moe_route(const int32_t *topk_ids, int64_t T, int32_t topk, int32
     DeviceInfo di;
     q4k_status st = check_device(&di);
     if (st != Q4K_OK) return st;
-    cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, nullptr, 0,
+    cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, nullptr, 0, nullptr, nullptr,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 
+// Many items per expert (32 or more on average): tensor-core tiles of up to 256
+// expert-sorted tokens; otherwise the small-M kernel over each expert's few tokens.
+static bool moe_uses_tc(int32_t E, int64_t T, int32_t topk) { return T * (int64_t)topk >= 32 * (int64_t)E; }
+
+// workspace: [offsets E+1][perm T*topk][tile list][tile count][expert-sorted
+// activations (tensor-core path only)][per-slot rows (combine only)]
 size_t q4k_moe_workspace_size(int32_t n_experts, int64_t N, int64_t K, int64_t T, int32_t topk, int y_mode) {
     if (!moe_shape_ok(n_experts, N, K, T, topk)) return 0;
-    size_t b = align256((size_t)(n_experts + 1) * 4) + align256((size_t)(T * topk) * 4);
+    size_t b = align256((size_t)(n_experts + 1) * 4) + align256((size_t)(T * topk) * 4) +
+               align256((size_t)moe_max_tiles(n_experts, T * topk) * sizeof(int4)) + 256;
+    if (moe_uses_tc(n_experts, T, topk)) b += align256((size_t)(T * topk) * (size_t)K * 2);
     if (y_mode == Q4K_MOE_Y_COMBINE) b += align256((size_t)(T * topk) * (size_t)N * 4);
     return b;
 }
@@ -294,11 +302,25 @@ q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_
     p += align256((size_t)(n_experts + 1) * 4);
     int32_t *perm = reinterpret_cast<int32_t *>(p);
     p += align256((size_t)(T * topk) * 4);
+    int4 *tiles = reinterpret_cast<int4 *>(p);
+    p += align256((size_t)moe_max_tiles(n_experts, T * topk) * sizeof(int4));
+    int *n_tiles = reinterpret_cast<int *>(p);
+    p += 256;
+    const bool tc = moe_uses_tc(n_experts, T, topk);
+    uint16_t *x_sorted = nullptr;
+    if (tc) {
+        x_sorted = reinterpret_cast<uint16_t *>(p);
+        p += align256((size_t)(T * topk) * (size_t)K * 2);
+    }
     float *slot_out = y_mode == Q4K_MOE_Y_COMBINE ? reinterpret_cast<float *>(p) : y;
     cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm,
-                                     y_mode == Q4K_MOE_Y_PER_SLOT ? y : nullptr, N, s);
+                                     y_mode == Q4K_MOE_Y_PER_SLOT ? y : nullptr, N, tc ? tiles : nullptr,
+                                     tc ? n_tiles : nullptr, s);
+    if (e == cudaSuccess && tc)
+        e = launch_moe_gather(di, x, x_mode, topk, perm, offsets, n_experts, T * topk, K, x_sorted, s);
     if (e == cudaSuccess)
-        e = launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, T, topk, slot_out, s);
+        e = tc ? launch_moe_tc(di, w_experts, n_experts, N, K, x_sorted, T * topk, perm, tiles, n_tiles, slot_out, s)
+               : launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, T, topk, slot_out, s);
     if (e == cudaSuccess && y_mode == Q4K_MOE_Y_COMBINE)
         e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);

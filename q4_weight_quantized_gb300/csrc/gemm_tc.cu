@@ -71,10 +71,19 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t
     hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
 }
 
-template <int BN>
+// MoE mode: the CTA's token tile comes from the routing's tile list; its
+// activation rows are rows [first, first + count) of the expert-sorted
+// activation copy, and output column j goes to the row of item perm[first + j].
+struct GatherArgs {
+    const int32_t *perm;
+    const int4 *tiles;  // (expert, first item, item count, -)
+    const int *n_tiles;
+};
+
+template <int BN, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
-                                                              int64_t ldy, int M, int N, int KB,
+                                                              int64_t ldy, int M, int N, int KB, GatherArgs ga,
                                                               unsigned int *status) {
     using C = Cfg<BN>;
     constexpr int NS = C::NS;
@@ -91,7 +100,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileRows;
-    const int m0 = blockIdx.y * BN;
+    int m0 = blockIdx.y * BN;
+    int wrow0 = n0;  // first weight row of the tile in the tensor map
+    int mma_n = BN;  // MMA N (tokens): BN, or the tile's item count rounded up to 16
+    __shared__ int orow_s[GATHER ? BN : 1];
+    if constexpr (GATHER) {
+        if ((int)blockIdx.y >= __ldg(ga.n_tiles)) return;  // beyond the routing's tiles: leave before any barrier
+        const int4 tl = __ldg(ga.tiles + blockIdx.y);
+        m0 = tl.y;  // rows of the expert-sorted activations
+        M = tl.y + tl.z;
+        wrow0 = tl.x * N + n0;
+        mma_n = (tl.z + 15) & ~15;
+        for (int j = threadIdx.x; j < tl.z; j += kThreads) orow_s[j] = __ldg(ga.perm + tl.y + j);
+    }
     // split K over a cluster of gridDim.z CTAs: this CTA takes blocks [kbeg, kbeg + KBs)
     const int S = gridDim.z, split = blockIdx.z;
     const int kbeg = (int)((int64_t)KB * split / S);
@@ -126,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
             mbar_arrive_expect_tx(rfull0, kRawBytes);
-            tma_load_2d(smem_u32(raw), &tmW, kbeg * (kBlockBytes / 4), n0, rfull0);
+            tma_load_2d(smem_u32(raw), &tmW, kbeg * (kBlockBytes / 4), wrow0, rfull0);
             for (int i = 0; i < total && !*abort_flag; ++i) {
                 const int kb = i >> 2, g = i & 3, s = i % NS;
                 if (g == 0 && kb + 1 < KBs) {  // raw tile of the next block, one block ahead
@@ -136,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
-                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kbeg + kb + 1) * (kBlockBytes / 4), n0,
+                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kbeg + kb + 1) * (kBlockBytes / 4), wrow0,
                                 rfull0 + 8 * r);
                 }
                 if (i >= NS && !mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status)) {
@@ -150,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16_f32(kTileRows, BN);
+            const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, mma_n);
             bool ok = true;
             for (int i = 0; i < total; ++i) {
                 const int s = i % NS;
@@ -235,11 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // buffers, column-major [BN][128], for the cluster reduction below
             float *part = reinterpret_cast<float *>(base);
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = 0; cc < (GATHER ? (M - m0 + 31) / 32 : BN / 32); ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
                 tmem_ld_wait();
-                if (S > 1) {
+                if constexpr (GATHER) {
+                    if (n < N) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = 32 * cc + j;
+                            if (col < M - m0) y[(int64_t)orow_s[col] * ldy + n] = __uint_as_float(v[j]);
+                        }
+                    }
+                } else if (S > 1) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) part[(32 * cc + j) * kTileRows + rl] = __uint_as_float(v[j]);
                 } else if (n < N) {
@@ -289,7 +318,7 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     if (e != cudaSuccess) return e;
     const int smem = Cfg<BN>::bytes;
     static_assert(Cfg<BN>::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers");
-    e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const int64_t tiles = ((N + kTileRows - 1) / kTileRows) * ((M + BN - 1) / BN);
@@ -314,7 +343,8 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     attr[0].val.clusterDim.z = S;
     cfg.attrs = attr;
     cfg.numAttrs = S > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tmW, tmX, y, ldy, (int)M, (int)N, KB, di.status);
+    GatherArgs ga = {};
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, false>, tmW, tmX, y, ldy, (int)M, (int)N, KB, ga, di.status);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -325,6 +355,27 @@ cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
     if (M <= 128) return launch_bn<128>(di, w, N, K, x, M, ldx, y, ldy, s);
     return launch_bn<256>(di, w, N, K, x, M, ldx, y, ldy, s);
+}
+
+cudaError_t launch_moe_tc(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
+                          const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
+                          const int *n_tiles, float *out, cudaStream_t s) {
+    constexpr int BN = kMoeTileItems;
+    CUtensorMap tmW, tmX;
+    cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kTileRows, kBlockBytes / 4);
+    if (e != cudaSuccess) return e;
+    e = make_act_tmap_sw128(&tmX, x_sorted, n_items, K, K, BN);
+    if (e != cudaSuccess) return e;
+    const int smem = Cfg<BN>::bytes;
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    GatherArgs ga;
+    ga.perm = perm;
+    ga.tiles = tiles;
+    ga.n_tiles = n_tiles;
+    const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)moe_max_tiles(E, n_items), 1);
+    gemm_tc_kernel<BN, true><<<grid, kThreads, smem, s>>>(tmW, tmX, out, N, 0, (int)N, (int)(K / kQK), ga, di.status);
+    return cudaGetLastError();
 }
 
 }  // namespace q4k

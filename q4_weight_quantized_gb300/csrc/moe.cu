@@ -25,7 +25,8 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__restrict__ ids, int n_items, int E,
                                                               int32_t *__restrict__ offsets,
                                                               int32_t *__restrict__ perm, float *__restrict__ zero_rows,
-                                                              int64_t row_len) {
+                                                              int64_t row_len, int4 *__restrict__ tiles,
+                                                              int *__restrict__ n_tiles) {
     extern __shared__ int route_smem[];
     int *base = route_smem;         // [E + 1]: running fill position per expert
     int *wc = route_smem + E + 1;   // [32][E]: per-warp counts, then per-warp bases
@@ -71,6 +72,36 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
     }
     __syncthreads();
     const int n_valid = base[E];
+    if (tiles) {
+        // token tiles of up to kMoeTileItems items per expert, listed in expert order
+        const int cnt = tid < E ? base[tid + 1] - base[tid] : 0;  // base[] holds the exclusive scan here
+        const int nt = (cnt + kMoeTileItems - 1) / kMoeTileItems;
+        int ti = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, ti, o);
+            if (lane >= o) ti += t;
+        }
+        __shared__ int tile_tot[kRouteWarps];
+        if (lane == 31) tile_tot[warp] = ti;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = tile_tot[lane];
+            int wi = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+                if (lane >= o) wi += t;
+            }
+            tile_tot[lane] = wi - w;
+            if (lane == 31) *n_tiles = wi;
+        }
+        __syncthreads();
+        const int first = ti - nt + tile_tot[warp];
+        for (int k = 0; k < nt; ++k)
+            tiles[first + k] = make_int4(tid, base[tid] + k * kMoeTileItems, min(kMoeTileItems, cnt - k * kMoeTileItems), 0);
+        __syncthreads();
+    }
 
     for (int c0 = 0; c0 < n_items; c0 += kRouteThreads) {
         for (int k = tid; k < kRouteWarps * E; k += kRouteThreads) wc[k] = 0;
@@ -133,16 +164,46 @@ __global__ void combine_kernel(const float *__restrict__ out, const float *__res
     }
 }
 
+// x_sorted[p] = activation row of item perm[p], one warp per row, 16-byte
+// accesses.  Rows past the valid item count (offsets[E]) are left alone.
+__global__ void gather_kernel(const uint16_t *__restrict__ x, int x_per_slot, int topk,
+                              const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets, int E,
+                              int64_t K, uint16_t *__restrict__ x_sorted) {
+    const int n_valid = __ldg(offsets + E);
+    const int lane = threadIdx.x & 31;
+    const int64_t chunks = K / 8;  // 16-byte chunks per row
+    for (int64_t p = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); p < n_valid;
+         p += (int64_t)gridDim.x * (blockDim.x / 32)) {
+        const int item = __ldg(perm + p);
+        const int64_t src = x_per_slot ? item : item / topk;
+        const uint4 *s = reinterpret_cast<const uint4 *>(x + src * K);
+        uint4 *d = reinterpret_cast<uint4 *>(x_sorted + p * K);
+        for (int64_t c = lane; c < chunks; c += 32) d[c] = __ldg(s + c);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per_slot, int topk, const int32_t *perm,
+                              const int32_t *offsets, int E, int64_t n_items, int64_t K, uint16_t *x_sorted,
+                              cudaStream_t s) {
+    int64_t blocks = (n_items + 7) / 8;
+    const int64_t cap = (int64_t)di.sm_count * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    gather_kernel<<<(int)blocks, 256, 0, s>>>(x, x_per_slot, topk, perm, offsets, E, K, x_sorted);
+    return cudaGetLastError();
+}
 
 size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kRouteWarps * E * 4; }
 
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
-                             float *zero_rows, int64_t row_len, cudaStream_t s) {
+                             float *zero_rows, int64_t row_len, int4 *tiles, int *n_tiles, cudaStream_t s) {
     const size_t smem = route_smem_bytes(E);
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    route_kernel<<<1, kRouteThreads, smem, s>>>(ids, (int)n_items, E, offsets, perm, zero_rows, row_len);
+    route_kernel<<<1, kRouteThreads, smem, s>>>(ids, (int)n_items, E, offsets, perm, zero_rows, row_len, tiles,
+                                                n_tiles);
     return cudaGetLastError();
 }
 

@@ -42,10 +42,28 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
                               int64_t T, int topk, float *out, cudaStream_t s);
 
 // Stable counting sort of items by expert (E <= 1024); when zero_rows is given,
-// rows of row_len floats belonging to items with invalid ids are zeroed.
+// rows of row_len floats belonging to items with invalid ids are zeroed.  When
+// tiles is given, it also lists every (expert, first item, item count) token
+// tile of at most kMoeTileItems items, and *n_tiles receives their number.
+constexpr int kMoeTileItems = 256;
 size_t route_smem_bytes(int E);
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
-                             float *zero_rows, int64_t row_len, cudaStream_t s);
+                             float *zero_rows, int64_t row_len, int4 *tiles, int *n_tiles, cudaStream_t s);
+
+// Upper bound on the number of token tiles the routing can produce.
+inline int64_t moe_max_tiles(int E, int64_t n_items) { return E + (n_items + kMoeTileItems - 1) / kMoeTileItems; }
+
+// MoE on the tensor cores: one CTA per (128-row weight tile, token tile of the
+// routing's tile list), reading the expert-sorted activation rows x_sorted.
+cudaError_t launch_moe_tc(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
+                          const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
+                          const int *n_tiles, float *out, cudaStream_t s);
+
+// x_sorted[p] = activation row of item perm[p] (p < offsets[E]): per-token rows
+// (x[item / topk]) or per-slot rows (x[item]), K bf16 each.
+cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per_slot, int topk, const int32_t *perm,
+                              const int32_t *offsets, int E, int64_t n_items, int64_t K, uint16_t *x_sorted,
+                              cudaStream_t s);
 
 // y[t] = sum_j gates[t][j] * out[t*topk+j] in slot order (N % 4 == 0)
 cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,

@@ -353,3 +353,23 @@ def test_moe_determinism(syn, moe_up):
     a = run_moe(moe_up, G.MOE_E, N, K, x, 0, ids, gates, 0, w_dev=w)
     b = run_moe(moe_up, G.MOE_E, N, K, x, 0, ids, gates, 0, w_dev=w)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,T,topk,N,K", [(4, 64, 2, 256, 512), (3, 300, 2, 200, 768)])
+def test_moe_tensor_core_path(ref, syn, E, T, topk, N, K):
+    # >= 32 items per expert on average: the tcgen05 path with expert-sorted rows;
+    # the second case has experts with more than 256 items (several token tiles)
+    w = np.concatenate([G.weights(4, 60 + e, N, K, outliers=True) for e in range(E)])
+    ids, gates = syn.routing(700 + T, 701 + T, T, E, topk)
+    ids[3, 1] = -5                                   # an invalid id: zero row, no contribution
+    x = G.activations(4, 11, T, K)
+    y = run_moe(w, E, N, K, x, q4k.Q4K_MOE_X_PER_TOKEN, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT)
+    want = ref.moe_slots(w, E, N, K, x, False, ids, threads=16)
+    assert np.all(y[3, 1] == 0.0)
+    assert G.rel_err(y, want) <= TOL_TC
+    xs = G.activations(4, 12, T * topk, K)
+    yc = run_moe(w, E, N, K, xs, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_COMBINE)
+    yc2 = run_moe(w, E, N, K, xs, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_COMBINE)
+    assert np.array_equal(yc.view(np.uint32), yc2.view(np.uint32))
+    want_c = ref.moe(w, E, N, K, xs, True, ids, gates, threads=16)
+    assert G.rel_err(yc, want_c) <= TOL_TC
