@@ -208,10 +208,11 @@ q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_
  *     zero, because each call writes every scratch byte it later reads.
  *   - A request whose scratch need, q4k_moe_workspace_size(n_experts, N, K, T,
  *     topk, y_mode), exceeds Q4K_MOE_NOALLOC_SCRATCH_BYTES fails with
- *     Q4K_ERR_WORKSPACE before anything is launched.  With Q4K_MOE_Y_PER_SLOT the
- *     need is only the routing (about 4*(E + T*topk) bytes); with
- *     Q4K_MOE_Y_COMBINE it adds 4*T*topk*N bytes (for example T = 64, topk = 8,
- *     N = 2048 needs 4 MiB).
+ *     Q4K_ERR_WORKSPACE before anything is launched.  With Q4K_MOE_Y_PER_SLOT and
+ *     fewer than 32*E items the need is only the routing (about 4*(E + T*topk)
+ *     bytes); Q4K_MOE_Y_COMBINE adds 4*T*topk*N bytes (for example T = 64,
+ *     topk = 8, N = 2048 needs 4 MiB), and from 32*E items on, where the experts
+ *     run on the tensor cores, the gathered activation rows add 2*T*topk*K bytes.
  * Other errors are those of q4k_moe_grouped_gemm. */
 #define Q4K_MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 q4k_status q4k_moe_grouped_gemm_noalloc(const void *w_experts, int32_t n_experts, int64_t N, int64_t K,

@@ -232,8 +232,11 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
     q4k_status st = check_device(&di);
     if (st != Q4K_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = M <= 16 ? launch_smallm(di, w, N, K, x, M, ldx, y, ldy, s)
-                                  : launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, s);
+    // M <= 16: small-M kernel; otherwise the tensor-core kernel, one CTA per
+    // output tile (with a cluster K split when the tiles leave the GPU half idle)
+    cudaError_t e;
+    if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, s);
+    else e = launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 
@@ -319,7 +322,7 @@ q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_
     if (e == cudaSuccess && tc)
         e = launch_moe_gather(di, x, x_mode, topk, perm, offsets, n_experts, T * topk, K, x_sorted, s);
     if (e == cudaSuccess)
-        e = tc ? launch_moe_tc(di, w_experts, n_experts, N, K, x_sorted, T * topk, perm, tiles, n_tiles, slot_out, s)
+        e = tc ? launch_moe_tcp(di, w_experts, n_experts, N, K, x_sorted, T * topk, perm, tiles, n_tiles, slot_out, s)
                : launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, T, topk, slot_out, s);
     if (e == cudaSuccess && y_mode == Q4K_MOE_Y_COMBINE)
         e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);

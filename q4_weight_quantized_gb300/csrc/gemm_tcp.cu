@@ -1,0 +1,382 @@
+// Persistent prefill / MoE Q4_K GEMM on the tcgen05 tensor cores.
+//
+// Same arithmetic as gemm_tc.cu (per-tile dequantization of Q4_K into a bf16
+// operand in shared memory, tcgen05.mma into an fp32 tensor-memory accumulator;
+// sparkinfer-server README, "Serve a GGUF instead of NVFP4"), organized so that
+// one CTA per SM streams tile after tile without draining its pipeline:
+//
+//   * warp 0    TMA: per 256-wide K block the raw Q4_K tile of 128 weight rows
+//               (two slots, issued one block ahead, across tile boundaries), per
+//               64-wide stage the 256-token activation tile (128-byte swizzle);
+//   * warp 1    MMA: one thread issues 4 x tcgen05.mma (128 x N x 16) per stage
+//               into one of two 256-column accumulators in tensor memory;
+//   * warps 2-9 dequant: two threads per weight row, each taking 16 of the 32
+//               code bytes of stage g (both its sub-blocks, 2g and 2g+1), writing
+//               the K-major 128-byte-swizzled bf16 operand;
+//   * warps 10-13 epilogue: tcgen05.ld of the finished accumulator and fp32
+//               stores, while the MMA warp already fills the other accumulator.
+// Tiles are taken round-robin (tile = CTA + k * grid).  In MoE mode the token
+// tiles come from the routing's tile list (expert, first item, count), the MMA
+// width is the count rounded up to 16, and output column j goes to the row of
+// item perm[first + j].  Every wait is bounded; the sum per output element runs
+// in a fixed order, so results are run-to-run deterministic.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "q4k_internal.h"
+#include "q4k_ptx.cuh"
+
+namespace q4k {
+namespace {
+
+constexpr int kTileRows = 128;                      // weight rows per tile (MMA M)
+constexpr int kBN = 256;                            // tokens per tile (MMA N at most)
+constexpr int kStageK = 64;                         // K per stage: one 128-byte swizzle row of bf16
+constexpr int kNS = 3;                              // stages
+constexpr int kXB = kBN * kStageK * 2;              // 32 KiB activations per stage
+constexpr int kAB = kTileRows * kStageK * 2;        // 16 KiB dequantized weights per stage
+constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K per block
+constexpr int kDqWarps = 8, kEpWarps = 4;
+constexpr int kThreads = (2 + kDqWarps + kEpWarps) * 32;
+constexpr int kX = 0, kA = kNS * kXB, kRaw = kA + kNS * kAB, kBar = kRaw + 2 * kRawBytes;
+constexpr int kNBars = 2 * kNS + 2 + 2 + 2 + 2;
+constexpr int kMisc = kBar + kNBars * 8;
+constexpr int kOrow = kMisc + 16;                   // [2][kBN] output rows (MoE)
+constexpr int kSmem = kOrow + 2 * kBN * 4 + 1024;   // + slack to align the base to 1024
+constexpr uint32_t kTmemCols = 2 * kBN;
+
+struct Tile {
+    int n0, m0, cnt, wrow0;
+};
+
+struct Params {
+    float *y;
+    int64_t ldy;
+    int M, N, KB;
+    int tiles_n, tiles_m;  // dense: output tiles along N and M
+    const int32_t *perm;   // MoE
+    const int4 *tiles;     // MoE: (expert, first item, count, -)
+    const int *n_tiles;    // MoE: number of token tiles
+    unsigned int *status;
+};
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<__nv_bfloat162 *>(&u); }
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
+
+// 128+q pairs (natural element order) of one 32-bit word of codes: low nibbles
+// of bytes (0,1), (2,3) and high nibbles of the same bytes
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t &lo23, uint32_t &hi01,
+                                            uint32_t &hi23) {
+    const uint32_t t01 = prmt(w, 0u, 0x4140u);
+    const uint32_t t23 = prmt(w, 0u, 0x4342u);
+    lo01 = lop3_and_or(t01, 0x000F000Fu, 0x43004300u);
+    lo23 = lop3_and_or(t23, 0x000F000Fu, 0x43004300u);
+    hi01 = lop3_and_or(t01 >> 4, 0x000F000Fu, 0x43004300u);
+    hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
+}
+
+template <bool GATHER>
+__device__ __forceinline__ Tile tile_of(const Params &p, int k) {
+    const int tile = blockIdx.x + k * gridDim.x;
+    const int nt = tile % p.tiles_n, mt = tile / p.tiles_n;
+    Tile t;
+    t.n0 = nt * kTileRows;
+    if constexpr (GATHER) {
+        const int4 tl = __ldg(p.tiles + mt);
+        t.m0 = tl.y;
+        t.cnt = tl.z;
+        t.wrow0 = tl.x * p.N + t.n0;
+    } else {
+        t.m0 = mt * kBN;
+        t.cnt = min(kBN, p.M - t.m0);
+        t.wrow0 = t.n0;
+    }
+    return t;
+}
+
+template <bool GATHER>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                               const __grid_constant__ CUtensorMap tmX, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *xs = base + kX;
+    uint8_t *as = base + kA;
+    uint8_t *raw = base + kRaw;
+    const uint32_t bar = smem_u32(base + kBar);
+    const uint32_t full0 = bar, empty0 = bar + 8 * kNS, rfull0 = bar + 16 * kNS, rempty0 = rfull0 + 16,
+                   accfull0 = rempty0 + 16, accempty0 = accfull0 + 16;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kMisc + 4);
+    int *orow = reinterpret_cast<int *>(base + kOrow);
+    unsigned int *status = p.status;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = GATHER ? __ldg(p.n_tiles) : p.tiles_m;
+    const int total_tiles = p.tiles_n * tiles_m;
+    const int my_tiles =
+        (int)blockIdx.x < total_tiles ? (total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    if (my_tiles == 0) return;  // no work: leave before any barrier or allocation
+    const int KB = p.KB;
+    const int nblocks = my_tiles * KB;  // raw blocks this CTA streams, in order
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(full0 + 8 * s, 1 + kDqWarps);  // producer (+ tx bytes) and the dequant warps
+            mbar_init(empty0 + 8 * s, 1);            // tcgen05.commit
+        }
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(rfull0 + 8 * r, 1);
+            mbar_init(rempty0 + 8 * r, kDqWarps);
+            mbar_init(accfull0 + 8 * r, 1);          // tcgen05.commit
+            mbar_init(accempty0 + 8 * r, kEpWarps);  // epilogue warps
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------- TMA
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
+            // raw block b = k * KB + kb (tile k of this CTA, block kb)
+            auto issue_raw = [&](int b) -> bool {
+                const Tile t = tile_of<GATHER>(p, b / KB);
+                const int r = b & 1;
+                if (b >= 2 && !mbar_wait(rempty0 + 8 * r, ((b >> 1) - 1) & 1, status)) return false;
+                mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
+                tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (b % KB) * (kBlockBytes / 4), t.wrow0,
+                            rfull0 + 8 * r);
+                return true;
+            };
+            bool ok = issue_raw(0);
+            Tile t = tile_of<GATHER>(p, 0);
+            for (int b = 0; b < nblocks && ok; ++b) {
+                const int kb = b % KB;
+                if (kb == 0 && b > 0) t = tile_of<GATHER>(p, b / KB);
+                if (b + 1 < nblocks && !issue_raw(b + 1)) {
+                    ok = false;
+                    break;
+                }
+                for (int g = 0; g < 4; ++g) {
+                    const int i = b * 4 + g, s = i % kNS;
+                    if (i >= kNS && !mbar_wait(empty0 + 8 * s, ((i / kNS) - 1) & 1, status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full0 + 8 * s, kXB);
+                    tma_load_2d(smem_u32(xs + s * kXB), &tmX, kb * kQK + kStageK * g, t.m0, full0 + 8 * s);
+                }
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA
+        if (lane == 0) {
+            bool ok = true;
+            for (int k = 0; k < my_tiles && ok; ++k) {
+                const Tile t = tile_of<GATHER>(p, k);
+                const int mma_n = GATHER ? (t.cnt + 15) & ~15 : kBN;
+                const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, mma_n);
+                const int buf = k & 1;
+                if (k >= 2 && !mbar_wait(accempty0 + 8 * buf, ((k >> 1) - 1) & 1, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * kBN);
+                for (int j = 0; j < KB * 4; ++j) {
+                    const int i = k * KB * 4 + j, s = i % kNS;
+                    if (!mbar_wait(full0 + 8 * s, (i / kNS) & 1, status) || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kAB));
+                    const uint64_t bd = umma_desc_sw128(smem_u32(xs + s * kXB));
+#pragma unroll
+                    for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
+                        umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (j | kk) != 0);
+                    umma_commit(empty0 + 8 * s);
+                }
+                if (ok) umma_commit(accfull0 + 8 * buf);
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (warp < 2 + kDqWarps) {
+        // ---------------------------------------------------- dequant warps
+        const int t = threadIdx.x - 64;
+        const int row = t & (kTileRows - 1);  // weight row within the tile
+        const int h = t >> 7;                 // which 16 code bytes of each group: elements 16h..16h+15
+        const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
+        bool ok = true;
+        for (int b = 0; b < nblocks && ok; ++b) {
+            const int r = b & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(rfull0 + 8 * r, (b >> 1) & 1, status))) {
+                ok = false;
+                break;
+            }
+            const uint8_t *rowp = raw + r * kRawBytes + row * kBlockBytes;
+            const uint4 hd = *reinterpret_cast<const uint4 *>(rowp);
+            const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+            const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+            const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
+            const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+            const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+            for (int g = 0; g < 4; ++g) {
+                const int i = b * 4 + g, s = i % kNS;
+                if (i >= kNS &&
+                    !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / kNS) - 1) & 1, status))) {
+                    ok = false;
+                    break;
+                }
+                // scales of sub-blocks 2g (low nibbles) and 2g+1 (high nibbles)
+                const uint32_t scw = g < 2 ? sc_lo : sc_hi, mw = g < 2 ? m_lo : m_hi;
+                const int b0 = (2 * g) & 3, b1 = (2 * g + 1) & 3;
+                const float dsc0 = d * (float)((scw >> (8 * b0)) & 0xFFu), dm0 = dmin * (float)((mw >> (8 * b0)) & 0xFFu);
+                const float dsc1 = d * (float)((scw >> (8 * b1)) & 0xFFu), dm1 = dmin * (float)((mw >> (8 * b1)) & 0xFFu);
+                const __nv_bfloat162 s0 = __floats2bfloat162_rn(dsc0, dsc0), n0v = __floats2bfloat162_rn(-dm0, -dm0);
+                const __nv_bfloat162 s1 = __floats2bfloat162_rn(dsc1, dsc1), n1v = __floats2bfloat162_rn(-dm1, -dm1);
+                const uint4 qw = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g + 16 * h);
+                const uint32_t wds[4] = {qw.x, qw.y, qw.z, qw.w};
+                uint8_t *arow = as + s * kAB + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {  // chunk 2h+j: elements 16h+8j .. +7 of each sub-block
+                    uint32_t lo[4], hi[4];
+                    unpack_word(wds[2 * j], lo[0], lo[1], hi[0], hi[1]);
+                    unpack_word(wds[2 * j + 1], lo[2], lo[3], hi[2], hi[3]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        lo[q] = as_u32(__hfma2(__hsub2(as_bf2(lo[q]), k128), s0, n0v));
+                        hi[q] = as_u32(__hfma2(__hsub2(as_bf2(hi[q]), k128), s1, n1v));
+                    }
+                    const int cl = 2 * h + j;
+                    *reinterpret_cast<uint4 *>(arow + ((cl ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4 *>(arow + (((cl + 4) ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+                fence_proxy_async_smem();  // make the stores visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full0 + 8 * s);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rempty0 + 8 * r);
+            if (*abort_flag) ok = false;
+        }
+        if (!ok && lane == 0) *abort_flag = 1;
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+        const int et = threadIdx.x - (2 + kDqWarps) * 32;
+        for (int k = 0; k < my_tiles; ++k) {
+            const Tile t = tile_of<GATHER>(p, k);
+            const int buf = k & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(accfull0 + 8 * buf, (k >> 1) & 1, status))) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            int *orw = orow + buf * kBN;
+            if constexpr (GATHER) {
+                for (int j = et; j < t.cnt; j += kEpWarps * 32) orw[j] = __ldg(p.perm + t.m0 + j);
+                asm volatile("bar.sync 2, %0;" ::"n"(kEpWarps * 32) : "memory");
+            }
+            const int n = t.n0 + 32 * q + lane;
+#pragma unroll 1
+            for (int cc = 0; cc < (t.cnt + 31) / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tmem + (uint32_t)(buf * kBN) + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
+                tmem_ld_wait();
+                if (n < p.N) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = 32 * cc + j;
+                        if (col < t.cnt) {
+                            const int64_t yrow = GATHER ? (int64_t)orw[col] : (int64_t)(t.m0 + col);
+                            p.y[yrow * p.ldy + n] = __uint_as_float(v[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty0 + 8 * buf);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool GATHER>
+cudaError_t launch(const DeviceInfo &di, const CUtensorMap &tmW, const CUtensorMap &tmX, const Params &p,
+                   int grid, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tcp_kernel<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    gemm_tcp_kernel<GATHER><<<grid, kThreads, kSmem, s>>>(tmW, tmX, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tcp_tiles(int64_t M, int64_t N) {
+    return (int)(((N + kTileRows - 1) / kTileRows) * ((M + kBN - 1) / kBN));
+}
+
+cudaError_t launch_gemm_tcp(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
+                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
+    CUtensorMap tmW, tmX;
+    cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
+    if (e != cudaSuccess) return e;
+    e = make_act_tmap_sw128(&tmX, x, M, K, ldx, kBN);
+    if (e != cudaSuccess) return e;
+    Params p = {};
+    p.y = y;
+    p.ldy = ldy;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.KB = (int)(K / kQK);
+    p.tiles_n = (int)((N + kTileRows - 1) / kTileRows);
+    p.tiles_m = (int)((M + kBN - 1) / kBN);
+    p.status = di.status;
+    const int tiles = p.tiles_n * p.tiles_m;
+    return launch<false>(di, tmW, tmX, p, tiles < di.sm_count ? tiles : di.sm_count, s);
+}
+
+cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
+                           const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
+                           const int *n_tiles, float *out, cudaStream_t s) {
+    CUtensorMap tmW, tmX;
+    cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kTileRows, kBlockBytes / 4);
+    if (e != cudaSuccess) return e;
+    e = make_act_tmap_sw128(&tmX, x_sorted, n_items, K, K, kBN);
+    if (e != cudaSuccess) return e;
+    Params p = {};
+    p.y = out;
+    p.ldy = N;
+    p.N = (int)N;
+    p.KB = (int)(K / kQK);
+    p.tiles_n = (int)((N + kTileRows - 1) / kTileRows);
+    p.perm = perm;
+    p.tiles = tiles;
+    p.n_tiles = n_tiles;
+    p.status = di.status;
+    return launch<true>(di, tmW, tmX, p, di.sm_count, s);
+}
+
+}  // namespace q4k

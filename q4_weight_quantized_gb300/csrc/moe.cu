@@ -17,30 +17,70 @@ namespace {
 
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kHistStride = kRouteWarps + 1;  // [E][33]: the warps' columns of one expert, padded
+constexpr int kRouteUnroll = 8;               // id loads in flight per lane
 
-// One CTA.  Histogram (integer atomics in shared memory: order-independent),
-// exclusive scan, then a stable scatter in chunks of 1024 items: within a chunk,
-// an item's position is its expert's running base + the count of same-expert
-// items in earlier warps + its rank among same-expert lanes of its own warp.
+// Expert of item i, or -1 for an id outside [0, E) and for i past `hi`.
+__device__ __forceinline__ int route_expert(const int32_t *ids, int i, int hi, int E) {
+    if (i >= hi) return -1;
+    const int e = __ldg(ids + i);
+    return e >= 0 && e < E ? e : -1;
+}
+
+// One CTA.  Warp w owns the contiguous item range [n*w/32, n*(w+1)/32), so a
+// stable order is: expert, then warp, then item within the warp.
+//   1. each warp counts its items per expert (lanes with equal ids are grouped
+//      with a match, and the group's first lane adds the group size to the
+//      warp's private column: no atomics);
+//   2. per expert, an exclusive scan over the 32 warp columns, then an
+//      exclusive scan of the expert totals gives offsets[];
+//   3. each warp walks its range again in item order: an item's position is
+//      its expert's offset + its warp's base + the running count of that
+//      expert in the warp + its rank among equal lanes of the same round.
+// Two reads of the ids and four block barriers, independent of the item count.
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__restrict__ ids, int n_items, int E,
                                                               int32_t *__restrict__ offsets,
                                                               int32_t *__restrict__ perm, float *__restrict__ zero_rows,
                                                               int64_t row_len, int4 *__restrict__ tiles,
                                                               int *__restrict__ n_tiles) {
     extern __shared__ int route_smem[];
-    int *base = route_smem;         // [E + 1]: running fill position per expert
-    int *wc = route_smem + E + 1;   // [32][E]: per-warp counts, then per-warp bases
+    int *base = route_smem;                    // [E + 1]: expert offsets
+    int *hist = route_smem + E + 1;            // [E][kHistStride]: per-warp counts, then per-warp running positions
     __shared__ int warp_tot[kRouteWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lo = (int)((int64_t)n_items * warp / kRouteWarps);
+    const int hi = (int)((int64_t)n_items * (warp + 1) / kRouteWarps);
+    const unsigned lt_mask = (1u << lane) - 1u;
 
-    for (int e = tid; e <= E; e += kRouteThreads) base[e] = 0;
+    for (int k = tid; k < E * kHistStride; k += kRouteThreads) hist[k] = 0;
     __syncthreads();
-    for (int i = tid; i < n_items; i += kRouteThreads) {
-        const int e = ids[i];
-        if (e >= 0 && e < E) atomicAdd(&base[e], 1);
+    // 1. per-warp counts
+    for (int i0 = lo; i0 < hi; i0 += 32 * kRouteUnroll) {
+        int ev[kRouteUnroll];
+#pragma unroll
+        for (int u = 0; u < kRouteUnroll; ++u) ev[u] = route_expert(ids, i0 + 32 * u + lane, hi, E);
+#pragma unroll
+        for (int u = 0; u < kRouteUnroll; ++u) {
+            const unsigned same = __match_any_sync(0xFFFFFFFFu, ev[u]);
+            if (ev[u] >= 0 && (same & lt_mask) == 0) hist[ev[u] * kHistStride + warp] += __popc(same);
+            __syncwarp();
+        }
     }
     __syncthreads();
-    // exclusive scan of base[0..E) (E <= 1024 = one value per thread)
+    // 2a. per expert: exclusive scan over the warp columns (one warp per expert, lane = column)
+    for (int ex = warp; ex < E; ex += kRouteWarps) {
+        const int c = hist[ex * kHistStride + lane];
+        int inc = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        hist[ex * kHistStride + lane] = inc - c;
+        if (lane == 31) base[ex] = inc;  // the expert's total, for now
+    }
+    __syncthreads();
+    // 2b. exclusive scan of the expert totals (E <= 1024: one per thread)
     const int v = tid < E ? base[tid] : 0;
     int incl = v;
 #pragma unroll
@@ -51,7 +91,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int w = warp_tot[lane];
+        const int w = warp_tot[lane];
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -72,9 +112,25 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
     }
     __syncthreads();
     const int n_valid = base[E];
+    // 3. stable scatter: each warp walks its own range in item order
+    for (int i0 = lo; i0 < hi; i0 += 32 * kRouteUnroll) {
+        int ev[kRouteUnroll];
+#pragma unroll
+        for (int u = 0; u < kRouteUnroll; ++u) ev[u] = route_expert(ids, i0 + 32 * u + lane, hi, E);
+#pragma unroll
+        for (int u = 0; u < kRouteUnroll; ++u) {
+            const int e = ev[u];
+            const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+            int *run = hist + (e >= 0 ? e : 0) * kHistStride + warp;
+            if (e >= 0) perm[base[e] + *run + __popc(same & lt_mask)] = i0 + 32 * u + lane;
+            __syncwarp();
+            if (e >= 0 && (same & lt_mask) == 0) *run += __popc(same);
+            __syncwarp();
+        }
+    }
     if (tiles) {
         // token tiles of up to kMoeTileItems items per expert, listed in expert order
-        const int cnt = tid < E ? base[tid + 1] - base[tid] : 0;  // base[] holds the exclusive scan here
+        const int cnt = tid < E ? base[tid + 1] - base[tid] : 0;
         const int nt = (cnt + kMoeTileItems - 1) / kMoeTileItems;
         int ti = nt;
 #pragma unroll
@@ -100,34 +156,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
         const int first = ti - nt + tile_tot[warp];
         for (int k = 0; k < nt; ++k)
             tiles[first + k] = make_int4(tid, base[tid] + k * kMoeTileItems, min(kMoeTileItems, cnt - k * kMoeTileItems), 0);
-        __syncthreads();
-    }
-
-    for (int c0 = 0; c0 < n_items; c0 += kRouteThreads) {
-        for (int k = tid; k < kRouteWarps * E; k += kRouteThreads) wc[k] = 0;
-        __syncthreads();
-        const int i = c0 + tid;
-        int e = -1;
-        if (i < n_items) {
-            e = ids[i];
-            if (e < 0 || e >= E) e = -1;
-        }
-        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) wc[warp * E + e] = __popc(peers);
-        __syncthreads();
-        for (int ex = tid; ex < E; ex += kRouteThreads) {
-            int run = base[ex];
-            for (int w = 0; w < kRouteWarps; ++w) {
-                const int t = wc[w * E + ex];
-                wc[w * E + ex] = run;
-                run += t;
-            }
-            base[ex] = run;
-        }
-        __syncthreads();
-        if (e >= 0) perm[wc[warp * E + e] + rank] = i;
-        __syncthreads();
     }
     for (int k = n_valid + tid; k < n_items; k += kRouteThreads) perm[k] = -1;
     if (zero_rows && n_valid < n_items) {
@@ -195,7 +223,7 @@ cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per
     return cudaGetLastError();
 }
 
-size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kRouteWarps * E * 4; }
+size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kHistStride * E * 4; }
 
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
                              float *zero_rows, int64_t row_len, int4 *tiles, int *n_tiles, cudaStream_t s) {

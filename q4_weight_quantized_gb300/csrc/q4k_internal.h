@@ -35,6 +35,15 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
 
+// Persistent variant for many output tiles (one CTA per SM, double-buffered
+// tensor-memory accumulators, 256-token tiles; gemm_tcp.cu).
+int gemm_tcp_tiles(int64_t M, int64_t N);
+cudaError_t launch_gemm_tcp(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
+                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
+cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
+                           const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
+                           const int *n_tiles, float *out, cudaStream_t s);
+
 // MoE: all experts stacked as E*N rows; rows of x and of out are chosen through
 // the routing permutation (perm/offsets from launch_moe_route).
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,

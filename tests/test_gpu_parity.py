@@ -211,6 +211,18 @@ def test_prefill_split_k_ragged(ref, M, N, K):
     assert G.rel_err(gpu_gemm(b, N, K, x), ref.gemm(b, N, K, x, threads=16)) <= TOL_TC
 
 
+def test_prefill_persistent_ragged(ref):
+    # enough 128 x 256 tiles for the persistent kernel, ragged in M (600 = 2*256 + 88)
+    # and N (6600 = 51*128 + 72); several tiles per CTA
+    M, N, K = 600, 6600, 1024
+    b = G.weights(3, 5, N, K, outliers=True)
+    x = G.activations(3, 6, M, K)
+    y = gpu_gemm(b, N, K, x)
+    rows = np.unique(np.concatenate([G.sample_rows(N, 40, seed=5), np.arange(N - 72, N)]))
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=16)
+    assert G.rel_err(y[:, rows], want) <= TOL_TC
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (128, 5120, 17408), (1024, 5120, 17408),
                                    (4096, 17408, 5120)])
 def test_prefill_full_size(ref, M, N, K):
