@@ -14,9 +14,9 @@ tokens, default 2048).
 
 Timing: W warm-up steps, then exactly K steps between a barrier plus
 cudaDeviceSynchronize on both sides, timed with CUDA events on the launching
-stream.  Each step's kernels are replayed from a CUDA graph; consecutive steps
-cycle through R weight sets whose total exceeds the 129 MB L2, so the weights
-always come from HBM.  SM clocks and throttle reasons are sampled through NVML
+stream.  The steps are replayed from CUDA graphs of R consecutive steps (as a
+decode loop captures its layers); consecutive steps cycle through R weight sets
+whose total exceeds the 129 MB L2, so the weights always come from HBM.  SM clocks and throttle reasons are sampled through NVML
 during the timed region.  `e2e` repeats the metric through the public API with
 the activations copied from pinned host memory and the outputs copied back every
 step.  `--impl reference` times the plain-C oracle on the host cores instead.
@@ -258,8 +258,12 @@ class GpuRunner:
 
     def launches_per_step(self) -> int:
         if self.wl.moe:
-            return 3 * 2 + 1  # route + grouped GEMM for gate, up, down; + combine
-        return sum(1 if M <= 16 else -(-M // 16) for (_, _, _, M, _, _) in self.wl.mats)
+            mo = self.wl.moe
+            # per grouped GEMM: routing + expert GEMM (+ the activation gather on
+            # the tensor-core path, from 32 items per expert); + the combine
+            tc = mo["T"] * mo["topk"] >= 32 * mo["E"]
+            return 3 * (3 if tc else 2) + 1
+        return len(self.wl.mats)  # one kernel per matrix
 
     def step_one(self, r: int, i: int):
         """Enqueue only matrix i of the step, with weight set r."""
@@ -326,18 +330,32 @@ def run_gpu(args, rank, local_rank, world):
     torch.cuda.synchronize()
     q4k.q4k_check_device(stream)
 
-    # one graph per weight set for the timed steps (nothing else in them)
-    graphs = []
-    for r in range(gr.R):
+    # Steps are captured R at a time (step r uses weight set r), as a decode loop
+    # captures its layers: one graph of R consecutive steps, replayed, plus one
+    # graph of the first K mod R (and W mod R) steps, so that exactly K timed
+    # and W warm-up steps run.  Nothing else is in the graphs.
+    def capture(n):
+        if n == 0:
+            return None
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            gr.step(r)
-        graphs.append(g)
+            for r in range(n):
+                gr.step(r)
+        return g
+
+    g_full = capture(gr.R)
+    g_rem = capture(args.steps % gr.R)
+    g_wrem = capture(args.warmup % gr.R)
+
+    def run_steps(n, rem):
+        for _ in range(n // gr.R):
+            g_full.replay()
+        if rem is not None:
+            rem.replay()
 
     # warm-up steps
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % gr.R].replay()
+        run_steps(args.warmup, g_wrem)
     torch.cuda.synchronize()
 
     # timed region
@@ -349,8 +367,7 @@ def run_gpu(args, rank, local_rank, world):
     with clocks:
         with torch.cuda.stream(stream):
             t0.record(stream)
-            for i in range(args.steps):
-                graphs[i % gr.R].replay()
+            run_steps(args.steps, g_rem)
             t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -432,7 +449,7 @@ def run_gpu(args, rank, local_rank, world):
                        (gr.R, gr.R * (wl.weight_bytes() if not wl.moe else sum(
                            wl.moe[k].nbytes for k in ("gate", "up", "down"))) / 1e6),
                        parallelism="replicas x%d" % world,
-                       timing="CUDA graph per step, CUDA events; kernel times from per-kernel graphs"),
+                       timing="CUDA graphs of %d steps, CUDA events; kernel times from per-kernel graphs" % gr.R),
         "gpu_launches": gr.launches_per_step() * args.steps,
     }
     # roofline of the dominant kernel

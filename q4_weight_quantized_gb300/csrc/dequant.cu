@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 
 #include "q4k_internal.h"
+#include "q4k_ptx.cuh"
 
 namespace q4k {
 namespace {
@@ -41,6 +42,8 @@ __device__ __forceinline__ void decode_pair(const uint8_t *sc12, int j, int &sc,
 template <typename Store>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w, int64_t n_blocks,
                                                       Store store) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -105,8 +108,8 @@ cudaError_t launch(const void *w, int64_t N, int64_t K, Store st, cudaStream_t s
     int64_t cap = (int64_t)sms * 16;
     int grid = (int)(want < cap ? want : cap);
     if (grid < 1) grid = 1;
-    dequant_kernel<Store><<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(w), n_blocks, st);
-    return cudaGetLastError();
+    return launch_pdl(dequant_kernel<Store>, dim3(grid), dim3(threads), 0, s, dim3(1), static_cast<const uint8_t *>(w),
+                      n_blocks, st);
 }
 
 }  // namespace

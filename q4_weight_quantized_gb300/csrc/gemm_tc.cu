@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
                                                               int64_t ldy, int M, int N, int KB, GatherArgs ga,
                                                               unsigned int *status) {
+    pdl_wait();  // the tile list (routing) and the activations may come from the previous kernel
+    pdl_trigger();
     using C = Cfg<BN>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -331,22 +333,10 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
         if (want > KB / 4) want = KB / 4;
         if (want > 1) S = (int)want;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = S;
-    cfg.attrs = attr;
-    cfg.numAttrs = S > 1 ? 1 : 0;
     GatherArgs ga = {};
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, false>, tmW, tmX, y, ldy, (int)M, (int)N, KB, ga, di.status);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
+    return launch_pdl(gemm_tc_kernel<BN, false>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
+                      tmX, y, ldy, (int)M, (int)N, KB, ga, di.status);
 }
 
 }  // namespace
@@ -374,8 +364,8 @@ cudaError_t launch_moe_tc(const DeviceInfo &di, const void *w_experts, int E, in
     ga.tiles = tiles;
     ga.n_tiles = n_tiles;
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)moe_max_tiles(E, n_items), 1);
-    gemm_tc_kernel<BN, true><<<grid, kThreads, smem, s>>>(tmW, tmX, out, N, 0, (int)N, (int)(K / kQK), ga, di.status);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tc_kernel<BN, true>, grid, dim3(kThreads), (size_t)smem, s, dim3(1), tmW, tmX, out, N, 0,
+                      (int)N, (int)(K / kQK), ga, di.status);
 }
 
 }  // namespace q4k

@@ -98,6 +98,8 @@ __device__ __forceinline__ Tile tile_of(const Params &p, int k) {
 template <bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                const __grid_constant__ CUtensorMap tmX, Params p) {
+    pdl_wait();  // the tile list and the sorted activations come from the routing kernels
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *xs = base + kX;
@@ -328,8 +330,7 @@ cudaError_t launch(const DeviceInfo &di, const CUtensorMap &tmW, const CUtensorM
                    int grid, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tcp_kernel<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    gemm_tcp_kernel<GATHER><<<grid, kThreads, kSmem, s>>>(tmW, tmX, p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tcp_kernel<GATHER>, dim3(grid), dim3(kThreads), kSmem, s, dim3(1), tmW, tmX, p);
 }
 
 }  // namespace

@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
                                                               int32_t *__restrict__ perm, float *__restrict__ zero_rows,
                                                               int64_t row_len, int4 *__restrict__ tiles,
                                                               int *__restrict__ n_tiles) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int route_smem[];
     int *base = route_smem;                    // [E + 1]: expert offsets
     int *hist = route_smem + E + 1;            // [E][kHistStride]: per-warp counts, then per-warp running positions
@@ -173,6 +175,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
 __global__ void combine_kernel(const float *__restrict__ out, const float *__restrict__ gates,
                                const int32_t *__restrict__ ids, int E, int64_t T, int topk, int64_t N,
                                float *__restrict__ y) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t n4 = N / 4;
     const int64_t total = T * n4;
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
@@ -197,6 +201,8 @@ __global__ void combine_kernel(const float *__restrict__ out, const float *__res
 __global__ void gather_kernel(const uint16_t *__restrict__ x, int x_per_slot, int topk,
                               const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets, int E,
                               int64_t K, uint16_t *__restrict__ x_sorted) {
+    pdl_wait();
+    pdl_trigger();
     const int n_valid = __ldg(offsets + E);
     const int lane = threadIdx.x & 31;
     const int64_t chunks = K / 8;  // 16-byte chunks per row
@@ -219,8 +225,8 @@ cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per
     const int64_t cap = (int64_t)di.sm_count * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    gather_kernel<<<(int)blocks, 256, 0, s>>>(x, x_per_slot, topk, perm, offsets, E, K, x_sorted);
-    return cudaGetLastError();
+    return launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, dim3(1), x, x_per_slot, topk, perm, offsets,
+                      E, K, x_sorted);
 }
 
 size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kHistStride * E * 4; }
@@ -230,9 +236,8 @@ cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t
     const size_t smem = route_smem_bytes(E);
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    route_kernel<<<1, kRouteThreads, smem, s>>>(ids, (int)n_items, E, offsets, perm, zero_rows, row_len, tiles,
-                                                n_tiles);
-    return cudaGetLastError();
+    return launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), smem, s, dim3(1), ids, (int)n_items, E, offsets, perm,
+                      zero_rows, row_len, tiles, n_tiles);
 }
 
 cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,
@@ -242,8 +247,7 @@ cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const flo
     const int64_t cap = (int64_t)di.sm_count * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    combine_kernel<<<(int)blocks, 256, 0, s>>>(out, gates, ids, E, T, topk, N, y);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, s, dim3(1), out, gates, ids, E, T, topk, N, y);
 }
 
 }  // namespace q4k

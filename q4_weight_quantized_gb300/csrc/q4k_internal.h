@@ -78,6 +78,37 @@ cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per
 cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,
                                int64_t T, int topk, int64_t N, float *y, cudaStream_t s);
 
+// Launches kern<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialization (the kernel may begin while the previous kernel in the stream
+// drains; it waits for it with griddepcontrol.wait before touching global
+// memory) and, when `cluster` holds more than one CTA, thread-block clusters of
+// that shape.
+template <typename... Exp, typename... Act>
+cudaError_t launch_pdl(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, dim3 cluster,
+                       Act &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster.x * cluster.y * cluster.z > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster.x;
+        attr[n].val.clusterDim.y = cluster.y;
+        attr[n].val.clusterDim.z = cluster.z;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Act &&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // TMA descriptor of a Q4_K matrix viewed as uint32 words: dims {K/256*36, N},
 // row pitch K/256*144 bytes, box {box_words, box_rows}, zero fill outside.
 cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K, int box_rows, int box_words);

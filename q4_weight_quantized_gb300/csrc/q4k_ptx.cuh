@@ -215,6 +215,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------ programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialization, so it may start while the previous kernel in the stream is
+// still draining.  pdl_wait blocks until that kernel has completed and its
+// memory is visible; each kernel calls it before its first global-memory
+// access.  pdl_trigger lets the next kernel in the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t elect_one() {
     uint32_t pred = 0;
     asm volatile(

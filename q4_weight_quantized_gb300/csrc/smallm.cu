@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const int kb0 = (int)((int64_t)KB * split / S), kb1 = (int)((int64_t)KB * (split + 1) / S);
     const int nblk = kb1 - kb0 > warp ? (kb1 - kb0 - warp + kWarps - 1) / kWarps : 0;  // this warp's blocks
 
+    if constexpr (MOE) pdl_wait();  // the routing comes from the previous kernel
     int off0 = 0, cnt = ra.M, tma_row = row0;
     if constexpr (MOE) {
         const int e = blockIdx.z;
@@ -180,6 +181,8 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
     }
+    if constexpr (!MOE) pdl_wait();  // x may come from the previous kernel
+    pdl_trigger();
     __syncthreads();
 
     // issue the copies of iteration `it` (chunk it / nblk, block it % nblk) into its slot
@@ -376,24 +379,11 @@ template <int NT, bool MOE, bool ONE, int SLOTS>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
     const int smem = smem_total(nx, SLOTS, MOE);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S, tiles, E);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = S;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = S > 1 ? 1 : 0;
     auto kern = smallm_kernel<NT, MOE, ONE, SLOTS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, ra, N, KB, nx, status);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmX, ra, N, KB, nx,
+                      status);
 }
 
 // Split K across a cluster only when the row tiles cannot fill the GPU at the
