@@ -314,6 +314,10 @@ def run_gpu(args, rank, local_rank, world):
 
     build_library()
     q4k.load()
+    # weights are uploaded once and only read afterwards, as in serving: the
+    # small-M kernels may copy their first weight blocks while the previous
+    # kernel drains (include/q4k.h, q4k_set_static_weights)
+    q4k.q4k_set_static_weights(True)
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     if world > 1:
@@ -448,7 +452,7 @@ def run_gpu(args, rank, local_rank, world):
         "config": dict(wl.config, l2="rotating %d weight sets, %.0f MB total > 129 MB L2" %
                        (gr.R, gr.R * (wl.weight_bytes() if not wl.moe else sum(
                            wl.moe[k].nbytes for k in ("gate", "up", "down"))) / 1e6),
-                       parallelism="replicas x%d" % world,
+                       parallelism="replicas x%d" % world, static_weights=True,
                        timing="CUDA graphs of %d steps, CUDA events; kernel times from per-kernel graphs" % gr.R),
         "gpu_launches": gr.launches_per_step() * args.steps,
     }

@@ -89,6 +89,22 @@ int q4k_version(void);
  * Q4K_ERR_CUDA if the synchronization itself failed. */
 q4k_status q4k_check_device(void *stream);
 
+/* Declares whether the weight matrices read by the small-M calls (q4k_gemv, and
+ * q4k_gemm with M <= 16) are static: never written by the kernel enqueued on the
+ * same stream immediately before the call.  Every kernel of the library is
+ * launched so that it may start while the previous kernel on its stream drains,
+ * and it waits for that kernel to finish before it touches memory.  With static
+ * weights on, the small-M kernels already copy their first weight blocks into
+ * shared memory during that wait, which hides part of each call's start-up
+ * (about 1.5 us on a 50 MB GEMV).  That is the usual inference setting: weights
+ * are uploaded once, by copies, and only read afterwards.  Keep it off (the
+ * default) when a kernel may write a weight buffer right before a q4k call reads
+ * it, for example a fill or an on-device quantization kernel: the early copies
+ * could then see the old contents.  Activations and outputs are never touched
+ * early.  Process-wide; applies to calls enqueued after it returns.  Returns the
+ * previous setting (0 or 1). */
+int q4k_set_static_weights(int enable);
+
 /* ----------------------------------------------------------------- dequant --
  * Standalone dequantization of an N x K Q4_K matrix:
  *     out[n][k] = d*sc_s*q - dmin*m_s   (fp32, computed as fp32 multiplies and one

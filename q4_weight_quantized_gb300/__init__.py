@@ -25,7 +25,7 @@ QK = 256
 # every symbol include/q4k.h declares
 EXPORTS = (
     "q4k_status_string", "q4k_last_cuda_error", "q4k_row_bytes", "q4k_version", "q4k_check_device",
-    "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
+    "q4k_set_static_weights", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
     "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_noalloc",
 )
 
@@ -59,6 +59,7 @@ def load(path: str | None = None):
         "q4k_row_bytes": ([i64], sz),
         "q4k_version": ([], st),
         "q4k_check_device": ([P], st),
+        "q4k_set_static_weights": ([ctypes.c_int], ctypes.c_int),
         "q4k_dequant": ([P, i64, i64, P, P], st),
         "q4k_dequant_bf16": ([P, i64, i64, P, P], st),
         "q4k_gemv": ([P, i64, i64, P, P, P], st),
@@ -122,6 +123,13 @@ def q4k_version() -> int:
 
 def q4k_check_device(stream=None) -> None:
     _check(load().q4k_check_device(_stream(stream)), "q4k_check_device")
+
+
+def q4k_set_static_weights(enable: bool) -> bool:
+    """Declare the weights read by the small-M calls static (never written by the
+    kernel enqueued just before a call on the same stream); returns the previous
+    setting.  See include/q4k.h."""
+    return bool(load().q4k_set_static_weights(1 if enable else 0))
 
 
 def q4k_dequant(w, N: int, K: int, out, stream=None) -> None:

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "q4k.h"
@@ -13,6 +14,9 @@
 namespace q4k {
 
 __device__ unsigned int g_status_word;  // kernels OR Q4K_DEV_* bits here
+
+// q4k_set_static_weights (process-wide, default off)
+static std::atomic<int> g_static_weights{0};
 
 namespace {
 
@@ -175,6 +179,8 @@ size_t q4k_row_bytes(int64_t K) { return k_ok(K) ? (size_t)(K / kQK) * kBlockByt
 
 int q4k_version(void) { return 100; }
 
+int q4k_set_static_weights(int enable) { return g_static_weights.exchange(enable ? 1 : 0); }
+
 q4k_status q4k_check_device(void *stream) {
     DeviceInfo di;
     q4k_status st = check_device(&di);
@@ -235,7 +241,7 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
     // M <= 16: small-M kernel; otherwise the tensor-core kernel, one CTA per
     // output tile (with a cluster K split when the tiles leave the GPU half idle)
     cudaError_t e;
-    if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, s);
+    if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, g_static_weights.load(std::memory_order_relaxed) != 0, s);
     else e = launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }

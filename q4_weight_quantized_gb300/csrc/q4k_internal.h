@@ -27,9 +27,10 @@ cudaError_t device_info(DeviceInfo *out);
 cudaError_t launch_dequant_f32(const void *w, int64_t N, int64_t K, float *out, cudaStream_t s);
 cudaError_t launch_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *out, cudaStream_t s);
 
-// M in [1, 16]
+// M in [1, 16].  early_weights: the first weight blocks may be copied before
+// the kernel has waited on the previous kernel in the stream (static weights).
 cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                          int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
+                          int64_t ldx, float *y, int64_t ldy, bool early_weights, cudaStream_t s);
 
 // M > 16: per-tile dequantization into shared memory + tcgen05 MMA (gemm_tc.cu)
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,

@@ -120,6 +120,7 @@ struct RowArgs {
     int topk;             // MoE
     const int32_t *perm;  // MoE routing permutation
     const int32_t *offsets;
+    int early_w;          // dense: copy the first weight blocks before waiting on the previous kernel
 };
 
 // Activation row and output offset of token slot n (-1 if the slot is empty).
@@ -180,13 +181,25 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         fence_mbar_init();
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
+        if constexpr (!MOE) {
+            // static weights: the weight halves of the first slots go out before the
+            // wait (the transaction count covers the activations copied after it)
+            if (ra.early_w)
+                for (int it = 0; it < SLOTS && it < total; ++it) {
+                    const uint32_t bar = bar0 + 8 * (it % SLOTS);
+                    mbar_arrive_expect_tx(bar, kBlkWBytes + min(kPerChunk, cnt) * kXBlkBytes);
+                    tma_load_2d(smem_u32(region + (it % SLOTS) * sbytes), &tmW, (kb0 + warp + kWarps * it) * kBlkWords,
+                                tma_row, bar);
+                }
+        }
     }
     if constexpr (!MOE) pdl_wait();  // x may come from the previous kernel
     pdl_trigger();
     __syncthreads();
 
-    // issue the copies of iteration `it` (chunk it / nblk, block it % nblk) into its slot
-    auto issue = [&](int it) {
+    // issue the copies of iteration `it` (chunk it / nblk, block it % nblk) into
+    // its slot; `weights` false: the weight copy (and the transaction count) went out already
+    auto issue = [&](int it, bool weights) {
         const int ch = it / nblk, kb = kb0 + warp + kWarps * (it % nblk);
         const int slot = it % SLOTS;
         const int nvalid = min(kPerChunk, cnt - ch * kPerChunk);
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         long long unused;
         slot_rows<MOE>(ra, off0, cnt, ch * kPerChunk + lane, xrow, unused);
         const uint32_t dst = smem_u32(region + slot * sbytes);
-        if (lane == 0) {
+        if (lane == 0 && weights) {
             mbar_arrive_expect_tx(bar0 + 8 * slot, kBlkWBytes + nvalid * kXBlkBytes);
             tma_load_2d(dst, &tmW, kb * kBlkWords, tma_row, bar0 + 8 * slot);
         }
@@ -202,7 +215,8 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         if (lane < nvalid) tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes, &tmX, kb * (kQK / 4), xrow, bar0 + 8 * slot);
     };
 
-    for (int it = 0; it < SLOTS && it < total; ++it) issue(it);
+    const bool early = !MOE && ra.early_w;
+    for (int it = 0; it < SLOTS && it < total; ++it) issue(it, !early);
 
     const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -291,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             // the slot is consumed: order the reads before the copy that refills it
             __syncwarp();
             fence_proxy_async_smem();
-            if (it + SLOTS < total) issue(it + SLOTS);
+            if (it + SLOTS < total) issue(it + SLOTS, true);
         }
         if constexpr (MOE) {
             // reduce this chunk across the warps (warp order) and store it
@@ -399,7 +413,7 @@ int split_for(const DeviceInfo &di, int64_t tiles, int KB) {
 }  // namespace
 
 cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                          int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
+                          int64_t ldx, float *y, int64_t ldy, bool early_weights, cudaStream_t s) {
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w, N, K, kRows, kBlkWords);
     if (e != cudaSuccess) return e;
@@ -410,6 +424,7 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
     const int S = split_for(di, tiles, KB);
     RowArgs ra = {};
     ra.y = y; ra.ldy = ldy; ra.M = (int)M;
+    ra.early_w = early_weights ? 1 : 0;
     const int nx = (int)M;
     if (M == 1) return launch_cfg<1, false, true, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
     if (M <= 4) return launch_cfg<1, false, false, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);

@@ -193,6 +193,54 @@ def test_verify_gemm_full_size(ref, M):
     assert G.rel_err(y[:, rows], want) <= TOL_SMALL
 
 
+
+@pytest.mark.parametrize("N,K", [(2000, 5120), (5120, 17408)], ids=["ragged", "split_k"])
+def test_static_weights_same_bits(ref, N, K):
+    # the early weight copies change when the weights arrive, not what is computed
+    b = G.weights(2, 3, N, K)
+    w = G.dev(b)
+    x = G.activations(2, 4, 16, K)
+    off = {m: gpu_gemm(b, N, K, x[:m], w_dev=w) for m in (1, 4, 16)}
+    prev = q4k.q4k_set_static_weights(True)
+    try:
+        assert q4k.q4k_set_static_weights(True) is True
+        on = {m: gpu_gemm(b, N, K, x[:m], w_dev=w) for m in (1, 4, 16)}
+    finally:
+        q4k.q4k_set_static_weights(prev)
+    for m in off:
+        assert np.array_equal(off[m].view(np.uint32), on[m].view(np.uint32)), m
+    rows = np.unique(np.concatenate([G.sample_rows(N, 48, seed=3), np.arange(N - 16, N)]))
+    assert G.rel_err(on[16][:, rows], ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=8)) <= TOL_SMALL
+
+
+def test_weights_written_by_the_previous_kernel(ref):
+    # static weights off (the default): a kernel that writes the weight buffer
+    # right before the call finishes before the GEMV reads it, every time
+    assert q4k.q4k_set_static_weights(False) is False
+    N, K = 4096, 5120
+    b = G.weights(2, 5, N, K)
+    src = G.dev(b)
+    x = G.activations(2, 6, 1, K)
+    xd = G.dev(x)
+    key = torch.full_like(src, 0x5A)
+    scrambled = torch.bitwise_xor(src, key)
+    w = torch.empty_like(src)
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    outs = []
+    for i in range(6):
+        # alternate the buffer between garbage and the real weights with kernels
+        torch.bitwise_xor(scrambled, key if i % 2 == 0 else torch.zeros_like(key), out=w)
+        if i % 2 == 1:
+            torch.bitwise_xor(w, key, out=w)
+        q4k.q4k_gemv(w, N, K, xd, y)
+        outs.append(G.host(y).copy())
+    torch.cuda.synchronize()
+    rows = G.sample_rows(N, 64, seed=9)
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x)
+    for o in outs:
+        assert G.rel_err(o[:, rows], want) <= TOL_SMALL
+
+
 # ------------------------------------------------------------------ prefill
 
 @pytest.mark.parametrize("M", [17, 40, 128])

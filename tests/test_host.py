@@ -96,6 +96,16 @@ def test_no_device_status(lib):
     assert lib.q4k_gemv(A16, 4, 256, A16, A16, None) == q4k.Q4K_ERR_DEVICE
 
 
+def test_static_weights_switch(lib):
+    prev = q4k.q4k_set_static_weights(True)
+    try:
+        assert q4k.q4k_set_static_weights(False) is True
+        assert q4k.q4k_set_static_weights(False) is False
+        assert lib.q4k_set_static_weights(7) == 0 and lib.q4k_set_static_weights(0) == 1
+    finally:
+        q4k.q4k_set_static_weights(prev)
+
+
 def test_binding_raises(lib):
     with pytest.raises(q4k.Q4KError) as ei:
         q4k.q4k_dequant(A16, 4, 300, A16, stream=0)
