@@ -46,28 +46,35 @@
 namespace q4k {
 namespace {
 
-constexpr int kRows = 32;                  // weight rows per CTA
-constexpr int kRowTiles = kRows / 16;      // 16-row MMA tiles per CTA
 constexpr int kWarps = 4;                  // split the CTA's K blocks
 constexpr int kThreads = kWarps * 32;
-constexpr int kBlkWBytes = kRows * kBlockBytes;  // 4608: one block column of the CTA's rows
 constexpr int kBlkWords = kBlockBytes / 4;       // 36 (TMA box inner dim, uint32)
 constexpr int kXBlkBytes = kQK * 2;              // 512: one token's activations for one block
 constexpr int kTableRowBytes = 80;  // 8 x (dsc, bias) + 16 pad: conflict-free 16-byte reads
-constexpr int kTableBytes = kRows * kTableRowBytes;
-constexpr int kRedBytes = kWarps * 16 * kRows * 4 + 16 * kRows * 4;  // per-warp + final partials
 
-__host__ __device__ constexpr int slot_bytes(int nx) { return (kBlkWBytes + nx * kXBlkBytes + 127) / 128 * 128; }
-// per warp: [ring of `slots` slots][scale table]
-__host__ __device__ constexpr int warp_bytes(int nx, int slots) { return slots * slot_bytes(nx) + kTableBytes; }
-// CTA: [warp regions][barriers][reduction buffer (MoE only; dense reuses the rings)]
-__host__ __device__ constexpr int bars_off(int nx, int slots) { return kWarps * warp_bytes(nx, slots); }
-__host__ __device__ constexpr int red_off(int nx, int slots) { return bars_off(nx, slots) + kWarps * slots * 8 + 64; }
-__host__ __device__ constexpr int smem_total(int nx, int slots, bool moe) {
-    return red_off(nx, slots) + (moe ? kRedBytes : 0);
-}
-
-static_assert(kRedBytes <= kWarps * 2 * slot_bytes(1), "dense reduction buffers alias the rings");
+// Shared-memory geometry of a CTA that owns ROWS weight rows (32 or 48).
+template <int ROWS>
+struct Geo {
+    static constexpr int kRowTiles = ROWS / 16;            // 16-row MMA tiles per CTA
+    static constexpr int kBlkWBytes = ROWS * kBlockBytes;   // one block column of the CTA's rows
+    static constexpr int kTableBytes = ROWS * kTableRowBytes;
+    static constexpr int kRedBytes = kWarps * 16 * ROWS * 4 + 16 * ROWS * 4;  // per-warp + final partials
+    __host__ __device__ static constexpr int slot_bytes(int nx) {
+        return (kBlkWBytes + nx * kXBlkBytes + 127) / 128 * 128;
+    }
+    // per warp: [ring of `slots` slots][scale table]
+    __host__ __device__ static constexpr int warp_bytes(int nx, int slots) { return slots * slot_bytes(nx) + kTableBytes; }
+    // CTA: [warp regions][barriers][reduction buffer (MoE only; dense reuses the rings)]
+    __host__ __device__ static constexpr int bars_off(int nx, int slots) { return kWarps * warp_bytes(nx, slots); }
+    __host__ __device__ static constexpr int red_off(int nx, int slots) {
+        return bars_off(nx, slots) + kWarps * slots * 8 + 64;
+    }
+    __host__ __device__ static constexpr int smem_total(int nx, int slots, bool moe) {
+        return red_off(nx, slots) + (moe ? kRedBytes : 0);
+    }
+    static_assert(ROWS % 16 == 0 && ROWS <= 64, "rows per CTA");
+    static_assert(kRedBytes <= kWarps * 2 * slot_bytes(1), "dense reduction buffers alias the rings");
+};
 
 __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t &lo23, uint32_t &hi01,
                                             uint32_t &hi23) {
@@ -141,8 +148,9 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 }
 
 // NT: 8-token MMA tiles (1 or 2).  ONE: exactly one token (the epilogue keeps
-// only the accumulators that hold it).  SLOTS: ring depth per warp.
-template <int NT, bool MOE, bool ONE, int SLOTS>
+// only the accumulators that hold it).  SLOTS: ring depth per warp.  ROWS:
+// weight rows per CTA (32 or 48).
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
                                                           int KB, int nx, unsigned int *status) {
@@ -150,6 +158,8 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     __shared__ int abort_flag;
     __shared__ long long yoff_s[16];
 
+    using G = Geo<ROWS>;
+    constexpr int kRows = ROWS, kRowTiles = G::kRowTiles, kBlkWBytes = G::kBlkWBytes;
     constexpr int kPerChunk = 8 * NT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = lane & 3, r = lane >> 2;
@@ -171,10 +181,10 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const int chunks = (cnt + kPerChunk - 1) / kPerChunk;
     const int total = chunks * nblk;  // this warp's (chunk, block) iterations
 
-    const int sbytes = slot_bytes(nx);
-    uint8_t *region = smem + warp * warp_bytes(nx, SLOTS);
+    const int sbytes = G::slot_bytes(nx);
+    uint8_t *region = smem + warp * G::warp_bytes(nx, SLOTS);
     float *table = reinterpret_cast<float *>(region + SLOTS * sbytes);
-    const uint32_t bar0 = smem_u32(smem + bars_off(nx, SLOTS)) + warp * SLOTS * 8;
+    const uint32_t bar0 = smem_u32(smem + G::bars_off(nx, SLOTS)) + warp * SLOTS * 8;
     if (threadIdx.x == 0) abort_flag = 0;
     if (lane == 0) {
         for (int i = 0; i < SLOTS; ++i) mbar_init(bar0 + 8 * i, 1);
@@ -246,6 +256,10 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             const uint8_t *wst = region + slot * sbytes;
             const uint8_t *xs = wst + kBlkWBytes;
             decode_scales(wst + lane * kBlockBytes, table + lane * (kTableRowBytes / 4));
+            if constexpr (kRows > 32) {
+                if (lane < kRows - 32)
+                    decode_scales(wst + (lane + 32) * kBlockBytes, table + (lane + 32) * (kTableRowBytes / 4));
+            }
             __syncwarp();
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         }
         if constexpr (MOE) {
             // reduce this chunk across the warps (warp order) and store it
-            float *red_w = reinterpret_cast<float *>(smem + red_off(nx, SLOTS));  // [4][16][kRows]
+            float *red_w = reinterpret_cast<float *>(smem + G::red_off(nx, SLOTS));  // [4][16][kRows]
             float *mine = red_w + warp * 16 * kRows;
 #pragma unroll
             for (int rt = 0; rt < kRowTiles; ++rt)
@@ -389,47 +403,88 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     }
 }
 
-template <int NT, bool MOE, bool ONE, int SLOTS>
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
-    const int smem = smem_total(nx, SLOTS, MOE);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS>;
+    const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE);
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmX, ra, N, KB, nx,
                       status);
 }
 
-// Split K across a cluster only when the row tiles cannot fill the GPU at the
-// four CTAs per SM that fit for M <= 4.  Depends on (N, K, device), never on M.
-int split_for(const DeviceInfo &di, int64_t tiles, int KB) {
-    int64_t S = (4 * (int64_t)di.sm_count) / (tiles > 0 ? tiles : 1);
-    if (S > 8) S = 8;
-    if (S > KB / kWarps) S = KB / kWarps;  // keep at least one block per warp
-    if (S < 1) S = 1;
-    return (int)S;
+// CTAs of the one-token kernel with ROWS rows that fit on one SM (per device).
+template <int ROWS>
+int resident_ctas(const DeviceInfo &di) {
+    static int cache[64];
+    int &slot = cache[di.device < 64 ? di.device : 63];
+    if (slot == 0) {
+        const int smem = Geo<ROWS>::smem_total(1, 2, false);
+        auto kern = smallm_kernel<1, false, true, 2, ROWS>;
+        int n = 0;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
+        slot = e == cudaSuccess && n > 0 ? n : 1;
+    }
+    return slot;
+}
+
+// How a dense call splits its work: CTAs of `rows` weight rows (32 or 48), and a
+// cluster of S CTAs splitting K when the row tiles alone cannot fill the GPU in
+// one wave.  Of the candidates, the one whose busiest SM streams the fewest
+// weights wins (ties go to 32 rows).  Depends on (N, K, device) only, never on
+// M, so the summation order of a row does not depend on how many tokens share
+// the call.
+struct Split {
+    int rows, S;
+};
+
+Split split_for(const DeviceInfo &di, int64_t N, int KB) {
+    Split best = {32, 1};
+    int64_t best_load = -1;
+    const int cand[2] = {32, 48};
+    for (int rows : cand) {
+        const int64_t tiles = (N + rows - 1) / rows;
+        const int64_t fit = (int64_t)(rows == 32 ? resident_ctas<32>(di) : resident_ctas<48>(di)) * di.sm_count;
+        int64_t S = fit / tiles;
+        if (S > 8) S = 8;
+        if (S > KB / kWarps) S = KB / kWarps;  // keep at least one block per warp
+        if (S < 1) S = 1;
+        const int64_t per_sm = (tiles * S + di.sm_count - 1) / di.sm_count;
+        const int64_t load = per_sm * rows * ((KB + S - 1) / S);  // rows x blocks on the busiest SM
+        if (best_load < 0 || load < best_load) {
+            best = {rows, (int)S};
+            best_load = load;
+        }
+    }
+    return best;
 }
 
 }  // namespace
 
 cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                           int64_t ldx, float *y, int64_t ldy, bool early_weights, cudaStream_t s) {
+    const int KB = (int)(K / kQK);
+    const Split sp = split_for(di, N, KB);
+    const int S = sp.S, tiles = (int)((N + sp.rows - 1) / sp.rows);
     CUtensorMap tmW, tmX;
-    cudaError_t e = make_weight_tmap(&tmW, w, N, K, kRows, kBlkWords);
+    cudaError_t e = make_weight_tmap(&tmW, w, N, K, sp.rows, kBlkWords);
     if (e != cudaSuccess) return e;
     e = make_act_tmap(&tmX, x, M, K, ldx, kQK / 4);
     if (e != cudaSuccess) return e;
-    const int KB = (int)(K / kQK);
-    const int tiles = (int)((N + kRows - 1) / kRows);
-    const int S = split_for(di, tiles, KB);
     RowArgs ra = {};
     ra.y = y; ra.ldy = ldy; ra.M = (int)M;
     ra.early_w = early_weights ? 1 : 0;
-    const int nx = (int)M;
-    if (M == 1) return launch_cfg<1, false, true, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
-    if (M <= 4) return launch_cfg<1, false, false, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
-    if (M <= 8) return launch_cfg<1, false, false, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
-    return launch_cfg<2, false, false, 2>(S, tiles, 1, nx, s, tmW, tmX, ra, (int)N, KB, di.status);
+    const int nx = (int)M, n = (int)N;
+    if (sp.rows == 48) {
+        if (M == 1) return launch_cfg<1, false, true, 2, 48>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+        if (M <= 8) return launch_cfg<1, false, false, 2, 48>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+        return launch_cfg<2, false, false, 2, 48>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+    }
+    if (M == 1) return launch_cfg<1, false, true, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+    if (M <= 8) return launch_cfg<1, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+    return launch_cfg<2, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
 }
 
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
@@ -437,6 +492,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
                               int64_t T, int topk, float *out, cudaStream_t s) {
     CUtensorMap tmW, tmX;
     // all experts stacked: E*N rows of the same pitch
+    constexpr int kRows = 32;
     cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kRows, kBlkWords);
     if (e != cudaSuccess) return e;
     e = make_act_tmap(&tmX, x, x_per_slot ? T * topk : T, K, K, kQK / 4);
@@ -448,8 +504,8 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     ra.x_per_slot = x_per_slot; ra.topk = topk; ra.perm = perm; ra.offsets = offsets;
     const int64_t items = T * topk;
     if (items <= 64 * (int64_t)E)
-        return launch_cfg<1, true, false, 3>(1, tiles, E, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
-    return launch_cfg<2, true, false, 2>(1, tiles, E, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
+        return launch_cfg<1, true, false, 3, 32>(1, tiles, E, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
+    return launch_cfg<2, true, false, 2, 32>(1, tiles, E, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
 }
 
 }  // namespace q4k

@@ -177,18 +177,20 @@ def test_decode_gemv_full_size(ref, shape):
     b = G.weights(cfg, 0, N, K)
     x = G.activations(cfg, 1, 1, K)
     y = gpu_gemm(b, N, K, x)
-    rows = G.sample_rows(N, 256)
+    # sampled rows plus the last 64, which lie in the ragged last row tile
+    rows = np.unique(np.concatenate([G.sample_rows(N, 256), np.arange(N - 64, N)]))
     want = ref.gemm(G.rows_of(b, rows), len(rows), K, x)
     assert G.rel_err(y[:, rows], want) <= TOL_SMALL
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
-def test_verify_gemm_full_size(ref, M):
-    cfg, N, K = 2, 17408, 5120
+@pytest.mark.parametrize("M,N,K", [(1, 17408, 5120), (2, 17408, 5120), (4, 17408, 5120), (8, 17408, 5120),
+                                   (16, 17408, 5120), (4, 5120, 17408), (16, 5120, 17408)])
+def test_verify_gemm_full_size(ref, M, N, K):
+    cfg = 2
     b = G.weights(cfg, 0, N, K)
     x = G.activations(cfg, 1, M, K)
     y = gpu_gemm(b, N, K, x)
-    rows = G.sample_rows(N, 128)
+    rows = np.unique(np.concatenate([G.sample_rows(N, 128), np.arange(N - 48, N)]))
     want = ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=8)
     assert G.rel_err(y[:, rows], want) <= TOL_SMALL
 
