@@ -259,10 +259,10 @@ class GpuRunner:
     def launches_per_step(self) -> int:
         if self.wl.moe:
             mo = self.wl.moe
-            # per grouped GEMM: routing + expert GEMM (+ the activation gather on
-            # the tensor-core path, from 32 items per expert); + the combine
+            # one routing; per grouped GEMM the expert GEMM (+ the activation gather
+            # on the tensor-core path, from 32 items per expert); + the combine
             tc = mo["T"] * mo["topk"] >= 32 * mo["E"]
-            return 3 * (3 if tc else 2) + 1
+            return 1 + 3 * (2 if tc else 1) + 1
         return len(self.wl.mats)  # one kernel per matrix
 
     def step_one(self, r: int, i: int):
@@ -284,12 +284,14 @@ class GpuRunner:
             E, T, topk = mo["E"], mo["T"], mo["topk"]
             if mark:
                 mark(0)
+            # the layer's three projections share one routing: the first call sorts
+            # the items, the other two reuse the sort left in the workspace
             q4k.q4k_moe_grouped_gemm(s["gate"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk, self.y_gate,
                                      0, self.moe_ws, self.moe_wsb)
-            q4k.q4k_moe_grouped_gemm(s["up"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk, self.y_up, 0,
-                                     self.moe_ws, self.moe_wsb)
-            q4k.q4k_moe_grouped_gemm(s["down"], E, 2048, 768, self.xd, 1, self.ids, self.gates, T, topk, self.y_down,
-                                     1, self.moe_ws, self.moe_wsb)
+            q4k.q4k_moe_grouped_gemm_reuse_routing(s["up"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk,
+                                                   self.y_up, 0, self.moe_ws, self.moe_wsb)
+            q4k.q4k_moe_grouped_gemm_reuse_routing(s["down"], E, 2048, 768, self.xd, 1, self.ids, self.gates, T, topk,
+                                                   self.y_down, 1, self.moe_ws, self.moe_wsb)
             if mark:
                 mark(1)
             return

@@ -203,6 +203,27 @@ q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_
                                 int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk,
                                 float *y, int y_mode, void *ws, size_t ws_bytes, void *stream);
 
+/* q4k_moe_grouped_gemm_reuse_routing: q4k_moe_grouped_gemm without the routing
+ * step.  The gate, up and down projections of one routed layer share the same
+ * top-k ids (sparkinfer-server README, "Determinism": discrete top-k expert
+ * routing), so after one q4k_moe_grouped_gemm call has sorted the items into
+ * `ws`, the layer's other projections can use that sort instead of repeating it.
+ * Same arguments, results and errors as q4k_moe_grouped_gemm (same bits), under
+ * these conditions, which cannot be checked:
+ *   - `ws` holds the routing written by the last q4k_moe_grouped_gemm call that
+ *     used it (calls to this function leave it unchanged, so any number of them
+ *     may follow one routing call), ordered before this call on the GPU;
+ *   - that call had the same n_experts, T and topk, and topk_ids has not changed
+ *     since.
+ * N, K, x, x_mode, gates, y and y_mode may differ from that call; ws_bytes must
+ * cover this call (q4k_moe_workspace_size), and the routing part of the
+ * workspace depends only on (n_experts, T, topk).  A stale routing gives wrong
+ * results, not an error. */
+q4k_status q4k_moe_grouped_gemm_reuse_routing(const void *w_experts, int32_t n_experts, int64_t N, int64_t K,
+                                              const uint16_t *x, int x_mode, const int32_t *topk_ids,
+                                              const float *gates, int64_t T, int32_t topk, float *y, int y_mode,
+                                              void *ws, size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------- allocation-free MoE --
  * No counterpart on the pages: an addition for callers that cannot provide a
  * workspace - code that must not call cudaMalloc/cudaFree (they synchronize the

@@ -26,7 +26,8 @@ QK = 256
 EXPORTS = (
     "q4k_status_string", "q4k_last_cuda_error", "q4k_row_bytes", "q4k_version", "q4k_check_device",
     "q4k_set_static_weights", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
-    "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_noalloc",
+    "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_reuse_routing",
+    "q4k_moe_grouped_gemm_noalloc",
 )
 
 # fixed scratch capacity of q4k_moe_grouped_gemm_noalloc (Q4K_MOE_NOALLOC_SCRATCH_BYTES)
@@ -68,6 +69,7 @@ def load(path: str | None = None):
         "q4k_moe_route": ([P, i64, i32, i32, P, P, P], st),
         "q4k_moe_workspace_size": ([i32, i64, i64, i64, i32, st], sz),
         "q4k_moe_grouped_gemm": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P, sz, P], st),
+        "q4k_moe_grouped_gemm_reuse_routing": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P, sz, P], st),
         "q4k_moe_grouped_gemm_noalloc": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P], st),
     }
     for name, (args, res) in sig.items():
@@ -167,6 +169,16 @@ def q4k_moe_grouped_gemm(w_experts, n_experts: int, N: int, K: int, x, x_mode: i
     _check(load().q4k_moe_grouped_gemm(_ptr(w_experts), n_experts, N, K, _ptr(x), x_mode, _ptr(topk_ids),
                                        _ptr(gates), T, topk, _ptr(y), y_mode, _ptr(ws), ws_bytes, _stream(stream)),
            "q4k_moe_grouped_gemm")
+
+
+def q4k_moe_grouped_gemm_reuse_routing(w_experts, n_experts: int, N: int, K: int, x, x_mode: int, topk_ids, gates,
+                                       T: int, topk: int, y, y_mode: int, ws, ws_bytes: int, stream=None) -> None:
+    """q4k_moe_grouped_gemm reusing the routing that the last q4k_moe_grouped_gemm
+    call left in `ws` (same n_experts, T, topk and unchanged topk_ids)."""
+    _check(load().q4k_moe_grouped_gemm_reuse_routing(_ptr(w_experts), n_experts, N, K, _ptr(x), x_mode,
+                                                     _ptr(topk_ids), _ptr(gates), T, topk, _ptr(y), y_mode, _ptr(ws),
+                                                     ws_bytes, _stream(stream)),
+           "q4k_moe_grouped_gemm_reuse_routing")
 
 
 def q4k_moe_grouped_gemm_noalloc(w_experts, n_experts: int, N: int, K: int, x, x_mode: int, topk_ids, gates,

@@ -268,7 +268,7 @@ q4k_status q4k_moe_route(const int32_t *topk_ids, int64_t T, int32_t topk, int32
     DeviceInfo di;
     q4k_status st = check_device(&di);
     if (st != Q4K_OK) return st;
-    cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, nullptr, 0, nullptr, nullptr,
+    cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, false, nullptr, nullptr,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
@@ -288,9 +288,10 @@ size_t q4k_moe_workspace_size(int32_t n_experts, int64_t N, int64_t K, int64_t T
     return b;
 }
 
-q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_t N, int64_t K, const uint16_t *x,
-                                int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk,
-                                float *y, int y_mode, void *ws, size_t ws_bytes, void *stream) {
+// route: compute the routing into ws; otherwise use the one a previous call left there
+static q4k_status moe_common(const void *w_experts, int32_t n_experts, int64_t N, int64_t K, const uint16_t *x,
+                             int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk, float *y,
+                             int y_mode, void *ws, size_t ws_bytes, void *stream, bool route) {
     if (!w_experts || !x || !topk_ids || !y || !ws) return Q4K_ERR_NULL;
     if (y_mode == Q4K_MOE_Y_COMBINE && !gates) return Q4K_ERR_NULL;
     if (!moe_shape_ok(n_experts, N, K, T, topk)) return Q4K_ERR_SHAPE;
@@ -321,18 +322,34 @@ q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_
         x_sorted = reinterpret_cast<uint16_t *>(p);
         p += align256((size_t)(T * topk) * (size_t)K * 2);
     }
-    float *slot_out = y_mode == Q4K_MOE_Y_COMBINE ? reinterpret_cast<float *>(p) : y;
-    cudaError_t e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm,
-                                     y_mode == Q4K_MOE_Y_PER_SLOT ? y : nullptr, N, tc ? tiles : nullptr,
-                                     tc ? n_tiles : nullptr, s);
+    const bool per_slot = y_mode == Q4K_MOE_Y_PER_SLOT;
+    float *slot_out = per_slot ? y : reinterpret_cast<float *>(p);
+    cudaError_t e = cudaSuccess;
+    if (route) e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, true, tiles, n_tiles, s);
     if (e == cudaSuccess && tc)
-        e = launch_moe_gather(di, x, x_mode, topk, perm, offsets, n_experts, T * topk, K, x_sorted, s);
+        e = launch_moe_gather(di, x, x_mode, topk, perm, offsets, n_experts, T * topk, K, x_sorted,
+                              per_slot ? y : nullptr, N, s);
     if (e == cudaSuccess)
         e = tc ? launch_moe_tcp(di, w_experts, n_experts, N, K, x_sorted, T * topk, perm, tiles, n_tiles, slot_out, s)
-               : launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, T, topk, slot_out, s);
-    if (e == cudaSuccess && y_mode == Q4K_MOE_Y_COMBINE)
-        e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);
+               : launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, tiles, n_tiles, T, topk,
+                                   slot_out, per_slot, s);
+    if (e == cudaSuccess && !per_slot) e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_t N, int64_t K, const uint16_t *x,
+                                int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk,
+                                float *y, int y_mode, void *ws, size_t ws_bytes, void *stream) {
+    return moe_common(w_experts, n_experts, N, K, x, x_mode, topk_ids, gates, T, topk, y, y_mode, ws, ws_bytes, stream,
+                      true);
+}
+
+q4k_status q4k_moe_grouped_gemm_reuse_routing(const void *w_experts, int32_t n_experts, int64_t N, int64_t K,
+                                              const uint16_t *x, int x_mode, const int32_t *topk_ids,
+                                              const float *gates, int64_t T, int32_t topk, float *y, int y_mode,
+                                              void *ws, size_t ws_bytes, void *stream) {
+    return moe_common(w_experts, n_experts, N, K, x, x_mode, topk_ids, gates, T, topk, y, y_mode, ws, ws_bytes, stream,
+                      false);
 }
 
 }  // extern "C"

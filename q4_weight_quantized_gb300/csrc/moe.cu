@@ -20,11 +20,12 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kHistStride = kRouteWarps + 1;  // [E][33]: the warps' columns of one expert, padded
 constexpr int kRouteUnroll = 8;               // id loads in flight per lane
 
-// Expert of item i, or -1 for an id outside [0, E) and for i past `hi`.
+// Expert of item i; E (a pseudo-expert after the last) for an id outside
+// [0, E); -1 for i past `hi`.
 __device__ __forceinline__ int route_expert(const int32_t *ids, int i, int hi, int E) {
     if (i >= hi) return -1;
     const int e = __ldg(ids + i);
-    return e >= 0 && e < E ? e : -1;
+    return e >= 0 && e < E ? e : E;
 }
 
 // One CTA.  Warp w owns the contiguous item range [n*w/32, n*(w+1)/32), so a
@@ -37,24 +38,26 @@ __device__ __forceinline__ int route_expert(const int32_t *ids, int i, int hi, i
 //   3. each warp walks its range again in item order: an item's position is
 //      its expert's offset + its warp's base + the running count of that
 //      expert in the warp + its rank among equal lanes of the same round.
+// Items with an invalid id form a pseudo-expert E placed after the valid ones:
+// with invalid_tail they fill perm[offsets[E] ..) in item order (the expert
+// kernels zero their per-slot rows); otherwise that tail is -1.
 // Two reads of the ids and four block barriers, independent of the item count.
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__restrict__ ids, int n_items, int E,
                                                               int32_t *__restrict__ offsets,
-                                                              int32_t *__restrict__ perm, float *__restrict__ zero_rows,
-                                                              int64_t row_len, int4 *__restrict__ tiles,
-                                                              int *__restrict__ n_tiles) {
+                                                              int32_t *__restrict__ perm, int invalid_tail,
+                                                              int4 *__restrict__ tiles, int *__restrict__ n_tiles) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ int route_smem[];
-    int *base = route_smem;                    // [E + 1]: expert offsets
-    int *hist = route_smem + E + 1;            // [E][kHistStride]: per-warp counts, then per-warp running positions
+    int *base = route_smem;                    // [E + 1]: expert offsets (base[E]: the invalid items)
+    int *hist = route_smem + E + 1;            // [E + 1][kHistStride]: per-warp counts, then running positions
     __shared__ int warp_tot[kRouteWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lo = (int)((int64_t)n_items * warp / kRouteWarps);
     const int hi = (int)((int64_t)n_items * (warp + 1) / kRouteWarps);
     const unsigned lt_mask = (1u << lane) - 1u;
 
-    for (int k = tid; k < E * kHistStride; k += kRouteThreads) hist[k] = 0;
+    for (int k = tid; k < (E + 1) * kHistStride; k += kRouteThreads) hist[k] = 0;
     __syncthreads();
     // 1. per-warp counts
     for (int i0 = lo; i0 < hi; i0 += 32 * kRouteUnroll) {
@@ -70,7 +73,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
     }
     __syncthreads();
     // 2a. per expert: exclusive scan over the warp columns (one warp per expert, lane = column)
-    for (int ex = warp; ex < E; ex += kRouteWarps) {
+    for (int ex = warp; ex <= E; ex += kRouteWarps) {
         const int c = hist[ex * kHistStride + lane];
         int inc = c;
 #pragma unroll
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
             if (lane >= o) inc += t;
         }
         hist[ex * kHistStride + lane] = inc - c;
-        if (lane == 31) base[ex] = inc;  // the expert's total, for now
+        if (lane == 31 && ex < E) base[ex] = inc;  // the expert's total, for now
     }
     __syncthreads();
     // 2b. exclusive scan of the expert totals (E <= 1024: one per thread)
@@ -123,10 +126,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
         for (int u = 0; u < kRouteUnroll; ++u) {
             const int e = ev[u];
             const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+            const bool place = e >= 0 && (e < E || invalid_tail);
             int *run = hist + (e >= 0 ? e : 0) * kHistStride + warp;
-            if (e >= 0) perm[base[e] + *run + __popc(same & lt_mask)] = i0 + 32 * u + lane;
+            if (place) perm[base[e] + *run + __popc(same & lt_mask)] = i0 + 32 * u + lane;
             __syncwarp();
-            if (e >= 0 && (same & lt_mask) == 0) *run += __popc(same);
+            if (place && (same & lt_mask) == 0) *run += __popc(same);
             __syncwarp();
         }
     }
@@ -159,15 +163,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
         for (int k = 0; k < nt; ++k)
             tiles[first + k] = make_int4(tid, base[tid] + k * kMoeTileItems, min(kMoeTileItems, cnt - k * kMoeTileItems), 0);
     }
-    for (int k = n_valid + tid; k < n_items; k += kRouteThreads) perm[k] = -1;
-    if (zero_rows && n_valid < n_items) {
-        // items with an id outside [0, E) get zero output rows (one warp per item)
-        for (int it = warp; it < n_items; it += kRouteWarps) {
-            const int e = ids[it];
-            if (e < 0 || e >= E)
-                for (int64_t k = lane; k < row_len; k += 32) zero_rows[(int64_t)it * row_len + k] = 0.0f;
-        }
-    }
+    if (!invalid_tail)
+        for (int k = n_valid + tid; k < n_items; k += kRouteThreads) perm[k] = -1;
 }
 
 // y[t][n] = sum_{j < topk} g[t][j] * out[(t*topk + j)][n], j in increasing order;
@@ -197,47 +194,55 @@ __global__ void combine_kernel(const float *__restrict__ out, const float *__res
 }
 
 // x_sorted[p] = activation row of item perm[p], one warp per row, 16-byte
-// accesses.  Rows past the valid item count (offsets[E]) are left alone.
+// accesses.  Rows past the valid item count (offsets[E]) are left alone.  With
+// zero_y, the per-slot output rows (N floats) of the items with an invalid id,
+// listed in perm[offsets[E] .. n_items), are zeroed.
 __global__ void gather_kernel(const uint16_t *__restrict__ x, int x_per_slot, int topk,
                               const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets, int E,
-                              int64_t K, uint16_t *__restrict__ x_sorted) {
+                              int64_t K, uint16_t *__restrict__ x_sorted, float *__restrict__ zero_y, int64_t N,
+                              int n_items) {
     pdl_wait();
     pdl_trigger();
     const int n_valid = __ldg(offsets + E);
     const int lane = threadIdx.x & 31;
     const int64_t chunks = K / 8;  // 16-byte chunks per row
-    for (int64_t p = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); p < n_valid;
-         p += (int64_t)gridDim.x * (blockDim.x / 32)) {
+    const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), nw = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t p = w0; p < n_valid; p += nw) {
         const int item = __ldg(perm + p);
         const int64_t src = x_per_slot ? item : item / topk;
         const uint4 *s = reinterpret_cast<const uint4 *>(x + src * K);
         uint4 *d = reinterpret_cast<uint4 *>(x_sorted + p * K);
         for (int64_t c = lane; c < chunks; c += 32) d[c] = __ldg(s + c);
     }
+    if (zero_y)
+        for (int64_t p = n_valid + w0; p < n_items; p += nw) {
+            float *row = zero_y + (int64_t)__ldg(perm + p) * N;
+            for (int64_t c = lane; c < N; c += 32) row[c] = 0.0f;
+        }
 }
 
 }  // namespace
 
 cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per_slot, int topk, const int32_t *perm,
                               const int32_t *offsets, int E, int64_t n_items, int64_t K, uint16_t *x_sorted,
-                              cudaStream_t s) {
+                              float *zero_y, int64_t N, cudaStream_t s) {
     int64_t blocks = (n_items + 7) / 8;
     const int64_t cap = (int64_t)di.sm_count * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, dim3(1), x, x_per_slot, topk, perm, offsets,
-                      E, K, x_sorted);
+                      E, K, x_sorted, zero_y, N, (int)n_items);
 }
 
-size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kHistStride * E * 4; }
+size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kHistStride * (E + 1) * 4; }
 
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
-                             float *zero_rows, int64_t row_len, int4 *tiles, int *n_tiles, cudaStream_t s) {
+                             bool invalid_tail, int4 *tiles, int *n_tiles, cudaStream_t s) {
     const size_t smem = route_smem_bytes(E);
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), smem, s, dim3(1), ids, (int)n_items, E, offsets, perm,
-                      zero_rows, row_len, tiles, n_tiles);
+                      invalid_tail ? 1 : 0, tiles, n_tiles);
 }
 
 cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,

@@ -47,21 +47,29 @@ cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, i
 
 // MoE: all experts stacked as E*N rows; rows of x and of out are chosen through
 // the routing permutation (perm/offsets from launch_moe_route).
+// With zero_invalid, the per-slot rows of the items with an invalid id
+// (perm[offsets[E] .. T*topk)) are zeroed.
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
-                              int64_t T, int topk, float *out, cudaStream_t s);
+                              const int4 *tok_tiles, const int *n_tiles, int64_t T, int topk, float *out,
+                              bool zero_invalid, cudaStream_t s);
 
-// Stable counting sort of items by expert (E <= 1024); when zero_rows is given,
-// rows of row_len floats belonging to items with invalid ids are zeroed.  When
+// Stable counting sort of items by expert (E <= 1024).  Items with an id
+// outside [0, E) are left out of offsets; with invalid_tail they follow the
+// valid items in perm (item order), otherwise that tail of perm is -1.  When
 // tiles is given, it also lists every (expert, first item, item count) token
 // tile of at most kMoeTileItems items, and *n_tiles receives their number.
 constexpr int kMoeTileItems = 256;
 size_t route_smem_bytes(int E);
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
-                             float *zero_rows, int64_t row_len, int4 *tiles, int *n_tiles, cudaStream_t s);
+                             bool invalid_tail, int4 *tiles, int *n_tiles, cudaStream_t s);
 
-// Upper bound on the number of token tiles the routing can produce.
-inline int64_t moe_max_tiles(int E, int64_t n_items) { return E + (n_items + kMoeTileItems - 1) / kMoeTileItems; }
+// Upper bound on the number of token tiles the routing can produce: an expert
+// with c > 0 items gives ceil(c / 256) <= 1 + (c - 1) / 256 tiles, and at most
+// min(E, n_items) experts have items.
+inline int64_t moe_max_tiles(int E, int64_t n_items) {
+    return (n_items < E ? n_items : (int64_t)E) + (n_items + kMoeTileItems - 1) / kMoeTileItems;
+}
 
 // MoE on the tensor cores: one CTA per (128-row weight tile, token tile of the
 // routing's tile list), reading the expert-sorted activation rows x_sorted.
@@ -70,10 +78,12 @@ cudaError_t launch_moe_tc(const DeviceInfo &di, const void *w_experts, int E, in
                           const int *n_tiles, float *out, cudaStream_t s);
 
 // x_sorted[p] = activation row of item perm[p] (p < offsets[E]): per-token rows
-// (x[item / topk]) or per-slot rows (x[item]), K bf16 each.
+// (x[item / topk]) or per-slot rows (x[item]), K bf16 each.  With zero_y, the N
+// floats of zero_y's row of every invalid item (perm[offsets[E] .. n_items)) are
+// zeroed.
 cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per_slot, int topk, const int32_t *perm,
                               const int32_t *offsets, int E, int64_t n_items, int64_t K, uint16_t *x_sorted,
-                              cudaStream_t s);
+                              float *zero_y, int64_t N, cudaStream_t s);
 
 // y[t] = sum_j gates[t][j] * out[t*topk+j] in slot order (N % 4 == 0)
 cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,

@@ -117,8 +117,9 @@ __device__ __forceinline__ void decode_scales(const uint8_t *blk, float *table_r
 }
 
 // Where each token slot of a chunk reads its activation row and writes its
-// output row.  Dense: slot n is token n.  MoE: slot n of expert e's list is the
-// (token, k-slot) item perm[offsets[e] + n].
+// output row.  Dense: slot n is token n.  MoE: slot n of a token tile is the
+// (token, k-slot) item perm[first + n], first being the tile's first position
+// in the expert-sorted order.
 struct RowArgs {
     float *y;
     int64_t ldy;          // dense: output row stride; MoE: N
@@ -126,7 +127,11 @@ struct RowArgs {
     int x_per_slot;       // MoE: activation row is the item (1) or its token (0)
     int topk;             // MoE
     const int32_t *perm;  // MoE routing permutation
-    const int32_t *offsets;
+    const int4 *tiles;    // MoE: the routing's token tiles (expert, first item, count)
+    const int *n_tiles;
+    const int32_t *n_valid;  // MoE: offsets[E]; perm[*n_valid .. n_items) are the invalid items
+    int n_items;             // MoE: T * topk
+    int zero_invalid;        // MoE: zero the per-slot rows of the invalid items
     int early_w;          // dense: copy the first weight blocks before waiting on the previous kernel
 };
 
@@ -172,9 +177,19 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     if constexpr (MOE) pdl_wait();  // the routing comes from the previous kernel
     int off0 = 0, cnt = ra.M, tma_row = row0;
     if constexpr (MOE) {
-        const int e = blockIdx.z;
-        off0 = __ldg(ra.offsets + e);
-        cnt = __ldg(ra.offsets + e + 1) - off0;
+        // grid layer z = token tile z of the routing (only tiles of experts that have items);
+        // the layer right after the last tile zeroes the invalid items' rows of this row tile
+        const int n_tl = __ldg(ra.n_tiles);
+        if ((int)blockIdx.z >= n_tl) {  // leave before any barrier
+            if ((int)blockIdx.z == n_tl && ra.zero_invalid)
+                for (int p = __ldg(ra.n_valid) + warp; p < ra.n_items; p += kWarps)
+                    if (row0 + lane < N && lane < kRows) ra.y[(long long)__ldg(ra.perm + p) * ra.ldy + row0 + lane] = 0.0f;
+            return;
+        }
+        const int4 tl = __ldg(ra.tiles + blockIdx.z);
+        const int e = tl.x;
+        off0 = tl.y;
+        cnt = tl.z;
         if (cnt <= 0) return;  // expert without tokens: the whole CTA leaves before any barrier
         tma_row = e * N + row0;
     }
@@ -489,7 +504,8 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
 
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
-                              int64_t T, int topk, float *out, cudaStream_t s) {
+                              const int4 *tok_tiles, const int *n_tiles, int64_t T, int topk, float *out,
+                              bool zero_invalid, cudaStream_t s) {
     CUtensorMap tmW, tmX;
     // all experts stacked: E*N rows of the same pitch
     constexpr int kRows = 32;
@@ -501,11 +517,15 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     const int tiles = (int)((N + kRows - 1) / kRows);
     RowArgs ra = {};
     ra.y = out; ra.ldy = N; ra.M = 0;
-    ra.x_per_slot = x_per_slot; ra.topk = topk; ra.perm = perm; ra.offsets = offsets;
+    ra.x_per_slot = x_per_slot; ra.topk = topk; ra.perm = perm; ra.tiles = tok_tiles; ra.n_tiles = n_tiles;
     const int64_t items = T * topk;
+    ra.n_valid = offsets + E; ra.n_items = (int)items; ra.zero_invalid = zero_invalid ? 1 : 0;
+    // one grid layer per possible token tile (+1 to zero the invalid items' rows);
+    // layers past the routing's tile count leave at once
+    const int layers = (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
     if (items <= 64 * (int64_t)E)
-        return launch_cfg<1, true, false, 3, 32>(1, tiles, E, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
-    return launch_cfg<2, true, false, 2, 32>(1, tiles, E, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
+        return launch_cfg<1, true, false, 3, 32>(1, tiles, layers, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
+    return launch_cfg<2, true, false, 2, 32>(1, tiles, layers, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
 }
 
 }  // namespace q4k

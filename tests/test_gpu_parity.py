@@ -406,6 +406,51 @@ def test_moe_special_cases(ref, syn):
     assert G.rel_err(yc3, want) <= TOL_SMALL
 
 
+
+@pytest.mark.parametrize("T", [1, 16, 256, 600])
+def test_moe_reuse_routing_same_bits(syn, moe_up, moe_down, T):
+    # one routing call, then the layer's other projections reuse its sort: the
+    # same bits as routing every call, invalid ids included (T = 600: tensor cores)
+    E, topk = G.MOE_E, G.MOE_TOPK
+    (Nu, Ku), (Nd, Kd) = G.MOE_UP, G.MOE_DOWN
+    ids, gates = syn.routing(90 + T, 91 + T, T, E, topk)
+    ids[0, 3] = -1
+    ids[T - 1, 0] = E + 7
+    x = G.dev(G.activations(4, 20, T, Ku))
+    xd = G.dev(G.activations(4, 21, T * topk, Kd))
+    wu, wd = G.dev(moe_up), G.dev(moe_down)
+    wu2 = G.dev(np.ascontiguousarray(moe_up[::-1]))   # another "up" matrix: the experts in reverse order
+    idd, gd = G.dev(ids), G.dev(gates)
+    P, C = q4k.Q4K_MOE_Y_PER_SLOT, q4k.Q4K_MOE_Y_COMBINE
+    calls = [(wu, Nu, Ku, x, q4k.Q4K_MOE_X_PER_TOKEN, P), (wu2, Nu, Ku, x, q4k.Q4K_MOE_X_PER_TOKEN, P),
+             (wd, Nd, Kd, xd, q4k.Q4K_MOE_X_PER_SLOT, C)]
+    size = max(q4k.q4k_moe_workspace_size(E, N, K, T, topk, ym) for (_, N, K, _, _, ym) in calls)
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+
+    def out(N, ym):
+        return torch.full((T, N) if ym == C else (T, topk, N), float("nan"), dtype=torch.float32, device="cuda")
+
+    shared, fresh = [], []
+    for i, (w, N, K, xx, xm, ym) in enumerate(calls):
+        y = out(N, ym)
+        fn = q4k.q4k_moe_grouped_gemm if i == 0 else q4k.q4k_moe_grouped_gemm_reuse_routing
+        fn(w, E, N, K, xx, xm, idd, gd, T, topk, y, ym, ws, size)
+        shared.append(y)
+    for (w, N, K, xx, xm, ym) in calls:
+        y = out(N, ym)
+        wsf = torch.empty(q4k.q4k_moe_workspace_size(E, N, K, T, topk, ym), dtype=torch.uint8, device="cuda")
+        q4k.q4k_moe_grouped_gemm(w, E, N, K, xx, xm, idd, gd, T, topk, y, ym, wsf, wsf.numel())
+        fresh.append(y)
+    torch.cuda.synchronize()
+    for a, b in zip(shared, fresh):
+        a, b = G.host(a), G.host(b)
+        assert not np.isnan(a).any()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    for y in shared[:2]:
+        h = G.host(y)
+        assert np.all(h[0, 3] == 0) and np.all(h[T - 1, 0] == 0)
+
+
 def test_moe_determinism(syn, moe_up):
     N, K = G.MOE_UP
     T = 16
