@@ -154,8 +154,10 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 
 // NT: 8-token MMA tiles (1 or 2).  ONE: exactly one token (the epilogue keeps
 // only the accumulators that hold it).  SLOTS: ring depth per warp.  ROWS:
-// weight rows per CTA (32 or 48).
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS>
+// weight rows per warp tile (32 or 48).  RS (MoE with few K blocks): the warps
+// split rows instead of K - warp w owns rows w*ROWS.. of a 4*ROWS-row CTA over
+// all K blocks and stores its own outputs, with no cross-warp reduction.
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
                                                           int KB, int nx, unsigned int *status) {
@@ -170,20 +172,24 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const int c = lane & 3, r = lane >> 2;
     const int S = gridDim.x;       // K split = cluster size (always 1 for MoE)
     const int split = blockIdx.x;  // == cluster rank
-    const int row0 = blockIdx.y * kRows;
+    static_assert(!RS || (MOE && ROWS == 32), "row split is a MoE mode");
+    const int row0 = blockIdx.y * kRows * (RS ? kWarps : 1);
+    const int wrow0 = row0 + (RS ? warp * kRows : 0);  // this warp's first row
     const int kb0 = (int)((int64_t)KB * split / S), kb1 = (int)((int64_t)KB * (split + 1) / S);
-    const int nblk = kb1 - kb0 > warp ? (kb1 - kb0 - warp + kWarps - 1) / kWarps : 0;  // this warp's blocks
+    // this warp's blocks: all of them (row split), or blocks warp, warp+4, ... of the split
+    const int nblk = RS ? kb1 - kb0 : (kb1 - kb0 > warp ? (kb1 - kb0 - warp + kWarps - 1) / kWarps : 0);
+    const int kb_first = RS ? kb0 : kb0 + warp, kb_step = RS ? 1 : kWarps;
 
     if constexpr (MOE) pdl_wait();  // the routing comes from the previous kernel
-    int off0 = 0, cnt = ra.M, tma_row = row0;
+    int off0 = 0, cnt = ra.M, tma_row = wrow0;
     if constexpr (MOE) {
         // grid layer z = token tile z of the routing (only tiles of experts that have items);
         // the layer right after the last tile zeroes the invalid items' rows of this row tile
         const int n_tl = __ldg(ra.n_tiles);
         if ((int)blockIdx.z >= n_tl) {  // leave before any barrier
             if ((int)blockIdx.z == n_tl && ra.zero_invalid)
-                for (int p = __ldg(ra.n_valid) + warp; p < ra.n_items; p += kWarps)
-                    if (row0 + lane < N && lane < kRows) ra.y[(long long)__ldg(ra.perm + p) * ra.ldy + row0 + lane] = 0.0f;
+                for (int p = __ldg(ra.n_valid) + (RS ? 0 : warp); p < ra.n_items; p += (RS ? 1 : kWarps))
+                    if (wrow0 + lane < N) ra.y[(long long)__ldg(ra.perm + p) * ra.ldy + wrow0 + lane] = 0.0f;
             return;
         }
         const int4 tl = __ldg(ra.tiles + blockIdx.z);
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         off0 = tl.y;
         cnt = tl.z;
         if (cnt <= 0) return;  // expert without tokens: the whole CTA leaves before any barrier
-        tma_row = e * N + row0;
+        tma_row = e * N + wrow0;
     }
     const int chunks = (cnt + kPerChunk - 1) / kPerChunk;
     const int total = chunks * nblk;  // this warp's (chunk, block) iterations
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
                 for (int it = 0; it < SLOTS && it < total; ++it) {
                     const uint32_t bar = bar0 + 8 * (it % SLOTS);
                     mbar_arrive_expect_tx(bar, kBlkWBytes + min(kPerChunk, cnt) * kXBlkBytes);
-                    tma_load_2d(smem_u32(region + (it % SLOTS) * sbytes), &tmW, (kb0 + warp + kWarps * it) * kBlkWords,
+                    tma_load_2d(smem_u32(region + (it % SLOTS) * sbytes), &tmW, (kb_first + kb_step * it) * kBlkWords,
                                 tma_row, bar);
                 }
         }
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     // issue the copies of iteration `it` (chunk it / nblk, block it % nblk) into
     // its slot; `weights` false: the weight copy (and the transaction count) went out already
     auto issue = [&](int it, bool weights) {
-        const int ch = it / nblk, kb = kb0 + warp + kWarps * (it % nblk);
+        const int ch = it / nblk, kb = kb_first + kb_step * (it % nblk);
         const int slot = it % SLOTS;
         const int nvalid = min(kPerChunk, cnt - ch * kPerChunk);
         int xrow;
@@ -336,7 +342,27 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             fence_proxy_async_smem();
             if (it + SLOTS < total) issue(it + SLOTS, true);
         }
-        if constexpr (MOE) {
+        if constexpr (MOE && RS) {
+            // row split: this warp stores its own rows of the chunk, staged through
+            // its [16][kRows] slice so that the stores coalesce
+            float *mine = reinterpret_cast<float *>(smem + G::red_off(nx, SLOTS)) + warp * 16 * kRows;
+#pragma unroll
+            for (int rt = 0; rt < kRowTiles; ++rt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int rA = rt * 16 + r, tk = nt * 8 + 2 * c;
+                    mine[tk * kRows + rA] = acc[rt][nt][0];
+                    mine[(tk + 1) * kRows + rA] = acc[rt][nt][1];
+                    mine[tk * kRows + rA + 8] = acc[rt][nt][2];
+                    mine[(tk + 1) * kRows + rA + 8] = acc[rt][nt][3];
+                }
+            __syncwarp();
+            if (!aborted && wrow0 + lane < N)
+                for (int tk = 0; tk < nvalid; ++tk)
+                    ra.y[(long long)__ldg(ra.perm + off0 + ch * kPerChunk + tk) * ra.ldy + wrow0 + lane] =
+                        mine[tk * kRows + lane];
+            __syncwarp();  // the slice is reused by the next chunk
+        } else if constexpr (MOE) {
             // reduce this chunk across the warps (warp order) and store it
             float *red_w = reinterpret_cast<float *>(smem + G::red_off(nx, SLOTS));  // [4][16][kRows]
             float *mine = red_w + warp * 16 * kRows;
@@ -418,11 +444,11 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     }
 }
 
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS>
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
     const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS>;
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmX, ra, N, KB, nx,
@@ -514,7 +540,13 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     e = make_act_tmap(&tmX, x, x_per_slot ? T * topk : T, K, K, kQK / 4);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
-    const int tiles = (int)((N + kRows - 1) / kRows);
+    // The warps split rows instead of K when K gives them fewer than two blocks
+    // each, and with fewer than four when the 128-row CTAs of the experts that can
+    // have items still give every SM two CTAs (items spread over many experts).
+    const int64_t items_all = T * topk;
+    const int64_t rs_ctas = (N + kRows * kWarps - 1) / (kRows * kWarps) * (items_all < E ? items_all : E);
+    const bool rs = KB < 2 * kWarps || (KB < 4 * kWarps && rs_ctas >= 2 * (int64_t)di.sm_count);
+    const int tiles = (int)((N + kRows * (rs ? kWarps : 1) - 1) / (kRows * (rs ? kWarps : 1)));
     RowArgs ra = {};
     ra.y = out; ra.ldy = N; ra.M = 0;
     ra.x_per_slot = x_per_slot; ra.topk = topk; ra.perm = perm; ra.tiles = tok_tiles; ra.n_tiles = n_tiles;
@@ -523,6 +555,11 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     // one grid layer per possible token tile (+1 to zero the invalid items' rows);
     // layers past the routing's tile count leave at once
     const int layers = (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
+    if (rs) {
+        if (items <= 64 * (int64_t)E)
+            return launch_cfg<1, true, false, 3, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
+        return launch_cfg<2, true, false, 2, 32, true>(1, tiles, layers, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
+    }
     if (items <= 64 * (int64_t)E)
         return launch_cfg<1, true, false, 3, 32>(1, tiles, layers, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
     return launch_cfg<2, true, false, 2, 32>(1, tiles, layers, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
