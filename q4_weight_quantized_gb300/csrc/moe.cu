@@ -15,10 +15,10 @@
 namespace q4k {
 namespace {
 
-constexpr int kRouteThreads = 1024;
+constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kHistStride = kRouteWarps + 1;  // [E][33]: the warps' columns of one expert, padded
-constexpr int kRouteUnroll = 8;               // id loads in flight per lane
+constexpr int kWhStride = kRouteWarps + 1;  // [E+1][17]: the warps' columns of one expert, padded
+constexpr int kRouteMaxCtas = 128;
 
 // Expert of item i; E (a pseudo-expert after the last) for an id outside
 // [0, E); -1 for i past `hi`.
@@ -28,142 +28,136 @@ __device__ __forceinline__ int route_expert(const int32_t *ids, int i, int hi, i
     return e >= 0 && e < E ? e : E;
 }
 
-// One CTA.  Warp w owns the contiguous item range [n*w/32, n*(w+1)/32), so a
-// stable order is: expert, then warp, then item within the warp.
-//   1. each warp counts its items per expert (lanes with equal ids are grouped
-//      with a match, and the group's first lane adds the group size to the
-//      warp's private column: no atomics);
-//   2. per expert, an exclusive scan over the 32 warp columns, then an
-//      exclusive scan of the expert totals gives offsets[];
-//   3. each warp walks its range again in item order: an item's position is
-//      its expert's offset + its warp's base + the running count of that
-//      expert in the warp + its rank among equal lanes of the same round.
-// Items with an invalid id form a pseudo-expert E placed after the valid ones:
-// with invalid_tail they fill perm[offsets[E] ..) in item order (the expert
-// kernels zero their per-slot rows); otherwise that tail is -1.
-// Two reads of the ids and four block barriers, independent of the item count.
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__restrict__ ids, int n_items, int E,
-                                                              int32_t *__restrict__ offsets,
-                                                              int32_t *__restrict__ perm, int invalid_tail,
-                                                              int4 *__restrict__ tiles, int *__restrict__ n_tiles) {
-    pdl_wait();
-    pdl_trigger();
-    extern __shared__ int route_smem[];
-    int *base = route_smem;                    // [E + 1]: expert offsets (base[E]: the invalid items)
-    int *hist = route_smem + E + 1;            // [E + 1][kHistStride]: per-warp counts, then running positions
-    __shared__ int warp_tot[kRouteWarps];
+// Exclusive prefix sums of a0, a1 (two consecutive values per thread, in thread
+// order) over the CTA; *total receives the sum of all.  Every thread calls it.
+__device__ __forceinline__ void block_scan2(int a0, int a1, int &x0, int &x1, int &total, int *scratch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int lo = (int)((int64_t)n_items * warp / kRouteWarps);
-    const int hi = (int)((int64_t)n_items * (warp + 1) / kRouteWarps);
-    const unsigned lt_mask = (1u << lane) - 1u;
-
-    for (int k = tid; k < (E + 1) * kHistStride; k += kRouteThreads) hist[k] = 0;
-    __syncthreads();
-    // 1. per-warp counts
-    for (int i0 = lo; i0 < hi; i0 += 32 * kRouteUnroll) {
-        int ev[kRouteUnroll];
-#pragma unroll
-        for (int u = 0; u < kRouteUnroll; ++u) ev[u] = route_expert(ids, i0 + 32 * u + lane, hi, E);
-#pragma unroll
-        for (int u = 0; u < kRouteUnroll; ++u) {
-            const unsigned same = __match_any_sync(0xFFFFFFFFu, ev[u]);
-            if (ev[u] >= 0 && (same & lt_mask) == 0) hist[ev[u] * kHistStride + warp] += __popc(same);
-            __syncwarp();
-        }
-    }
-    __syncthreads();
-    // 2a. per expert: exclusive scan over the warp columns (one warp per expert, lane = column)
-    for (int ex = warp; ex <= E; ex += kRouteWarps) {
-        const int c = hist[ex * kHistStride + lane];
-        int inc = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if (lane >= o) inc += t;
-        }
-        hist[ex * kHistStride + lane] = inc - c;
-        if (lane == 31 && ex < E) base[ex] = inc;  // the expert's total, for now
-    }
-    __syncthreads();
-    // 2b. exclusive scan of the expert totals (E <= 1024: one per thread)
-    const int v = tid < E ? base[tid] : 0;
-    int incl = v;
+    const int v = a0 + a1;
+    int inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
+        const int t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += t;
     }
-    if (lane == 31) warp_tot[warp] = incl;
+    if (lane == 31) scratch[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        const int w = warp_tot[lane];
+        const int w = lane < kRouteWarps ? scratch[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
             if (lane >= o) wi += t;
         }
-        warp_tot[lane] = wi - w;  // exclusive over warps
+        if (lane < kRouteWarps) scratch[lane] = wi - w;
+        if (lane == kRouteWarps - 1) scratch[kRouteWarps] = wi;
     }
     __syncthreads();
-    const int excl = incl - v + warp_tot[warp];
-    if (tid < E) {
-        base[tid] = excl;
-        offsets[tid] = excl;
+    x0 = inc - v + scratch[warp];
+    x1 = x0 + a0;
+    total = scratch[kRouteWarps];
+    __syncthreads();  // scratch is reused by the next call
+}
+
+// Stable counting sort of the items by expert over many CTAs, with no
+// cross-CTA communication.  CTA c owns the contiguous item range [c*R, (c+1)*R):
+//   1. it counts every item per expert, and separately those before its range
+//      (integer shared-memory atomics: the counts do not depend on order), which
+//      gives the expert offsets and where its own items of each expert start;
+//   2. its warps split the range into contiguous runs; each warp counts its run
+//      per expert (lanes with equal ids grouped by a match, the group's first
+//      lane adds the group size to the warp's private column: no atomics), an
+//      exclusive scan over the warp columns gives each warp's start;
+//   3. each warp walks its run again in item order: an item's position is its
+//      expert's start in this CTA + its warp's start + the warp's running count
+//      of that expert + its rank among equal lanes of the round.
+// Items with an invalid id form a pseudo-expert E placed after the valid ones:
+// with invalid_tail they fill perm[offsets[E] ..) in item order (the expert
+// kernels zero their per-slot rows); otherwise that tail is -1.  CTA 0 writes
+// offsets[] and the token-tile list.
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__restrict__ ids, int n_items, int E,
+                                                              int range, int32_t *__restrict__ offsets,
+                                                              int32_t *__restrict__ perm, int invalid_tail,
+                                                              int4 *__restrict__ tiles, int *__restrict__ n_tiles) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ int route_smem[];
+    const int E1 = E + 1;
+    int *total = route_smem;                     // [E+1] items per expert (E: invalid ids)
+    int *start_e = route_smem + E1;              // [E+1] items before this range, then this range's first position
+    int *wh = route_smem + 2 * E1;               // [E+1][kWhStride] per-warp counts, then running positions
+    __shared__ int scratch[kRouteWarps + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c0 = blockIdx.x * range, c1 = min(c0 + range, n_items);
+    const int lo = c0 + (int)((int64_t)(c1 - c0) * warp / kRouteWarps);
+    const int hi = c0 + (int)((int64_t)(c1 - c0) * (warp + 1) / kRouteWarps);
+    const unsigned lt_mask = (1u << lane) - 1u;
+
+    for (int k = tid; k < E1; k += kRouteThreads) total[k] = 0, start_e[k] = 0;
+    for (int k = tid; k < E1 * kWhStride; k += kRouteThreads) wh[k] = 0;
+    __syncthreads();
+    // 1. counts of all items, and of the items before this range
+    for (int i = tid; i < n_items; i += kRouteThreads) {
+        const int e = route_expert(ids, i, n_items, E);
+        atomicAdd(&total[e], 1);
+        if (i < c0) atomicAdd(&start_e[e], 1);
     }
-    if (tid == E - 1) {
-        base[E] = excl + v;
-        offsets[E] = excl + v;
+    // 2. per-warp counts of this range
+    for (int i0 = lo; i0 < hi; i0 += 32) {
+        const int e = route_expert(ids, i0 + lane, hi, E);
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+        if (e >= 0 && (same & lt_mask) == 0) wh[e * kWhStride + warp] += __popc(same);
+        __syncwarp();
     }
     __syncthreads();
-    const int n_valid = base[E];
-    // 3. stable scatter: each warp walks its own range in item order
-    for (int i0 = lo; i0 < hi; i0 += 32 * kRouteUnroll) {
-        int ev[kRouteUnroll];
+    // expert offsets: exclusive scan of total[0..E) (two experts per thread)
+    const int e0 = 2 * tid, e1 = 2 * tid + 1;
+    int x0, x1, n_valid;
+    block_scan2(e0 < E ? total[e0] : 0, e1 < E ? total[e1] : 0, x0, x1, n_valid, scratch);
+    // this range's first position per expert (the pseudo-expert E follows the valid items)
+    if (e0 < E) start_e[e0] += x0;
+    if (e1 < E) start_e[e1] += x1;
+    if (tid == 0) start_e[E] += n_valid;
+    if (blockIdx.x == 0) {
+        if (e0 < E) offsets[e0] = x0;
+        if (e1 < E) offsets[e1] = x1;
+        if (tid == 0) offsets[E] = n_valid;
+    }
+    // per expert: exclusive scan over the warp columns
+    for (int ex = tid; ex < E1; ex += kRouteThreads) {
+        int run = 0;
 #pragma unroll
-        for (int u = 0; u < kRouteUnroll; ++u) ev[u] = route_expert(ids, i0 + 32 * u + lane, hi, E);
-#pragma unroll
-        for (int u = 0; u < kRouteUnroll; ++u) {
-            const int e = ev[u];
-            const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
-            const bool place = e >= 0 && (e < E || invalid_tail);
-            int *run = hist + (e >= 0 ? e : 0) * kHistStride + warp;
-            if (place) perm[base[e] + *run + __popc(same & lt_mask)] = i0 + 32 * u + lane;
-            __syncwarp();
-            if (place && (same & lt_mask) == 0) *run += __popc(same);
-            __syncwarp();
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int t = wh[ex * kWhStride + w];
+            wh[ex * kWhStride + w] = run;
+            run += t;
         }
     }
-    if (tiles) {
+    if (blockIdx.x == 0 && tiles) {
         // token tiles of up to kMoeTileItems items per expert, listed in expert order
-        const int cnt = tid < E ? base[tid + 1] - base[tid] : 0;
-        const int nt = (cnt + kMoeTileItems - 1) / kMoeTileItems;
-        int ti = nt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xFFFFFFFFu, ti, o);
-            if (lane >= o) ti += t;
-        }
-        __shared__ int tile_tot[kRouteWarps];
-        if (lane == 31) tile_tot[warp] = ti;
-        __syncthreads();
-        if (warp == 0) {
-            const int w = tile_tot[lane];
-            int wi = w;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-                if (lane >= o) wi += t;
-            }
-            tile_tot[lane] = wi - w;
-            if (lane == 31) *n_tiles = wi;
-        }
-        __syncthreads();
-        const int first = ti - nt + tile_tot[warp];
-        for (int k = 0; k < nt; ++k)
-            tiles[first + k] = make_int4(tid, base[tid] + k * kMoeTileItems, min(kMoeTileItems, cnt - k * kMoeTileItems), 0);
+        const int nt0 = e0 < E ? (total[e0] + kMoeTileItems - 1) / kMoeTileItems : 0;
+        const int nt1 = e1 < E ? (total[e1] + kMoeTileItems - 1) / kMoeTileItems : 0;
+        int f0, f1, nt;
+        block_scan2(nt0, nt1, f0, f1, nt, scratch);
+        for (int k = 0; k < nt0; ++k)
+            tiles[f0 + k] = make_int4(e0, x0 + k * kMoeTileItems, min(kMoeTileItems, total[e0] - k * kMoeTileItems), 0);
+        for (int k = 0; k < nt1; ++k)
+            tiles[f1 + k] = make_int4(e1, x1 + k * kMoeTileItems, min(kMoeTileItems, total[e1] - k * kMoeTileItems), 0);
+        if (tid == 0) *n_tiles = nt;
     }
-    if (!invalid_tail)
+    __syncthreads();
+    // 3. stable scatter: each warp walks its run in item order
+    for (int i0 = lo; i0 < hi; i0 += 32) {
+        const int e = route_expert(ids, i0 + lane, hi, E);
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+        const bool place = e >= 0 && (e < E || invalid_tail);
+        int *run = wh + (e >= 0 ? e : 0) * kWhStride + warp;
+        if (place) perm[start_e[e] + *run + __popc(same & lt_mask)] = i0 + lane;
+        __syncwarp();
+        if (place && (same & lt_mask) == 0) *run += __popc(same);
+        __syncwarp();
+    }
+    if (!invalid_tail && blockIdx.x == 0)
         for (int k = n_valid + tid; k < n_items; k += kRouteThreads) perm[k] = -1;
 }
 
@@ -234,15 +228,20 @@ cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per
                       E, K, x_sorted, zero_y, N, (int)n_items);
 }
 
-size_t route_smem_bytes(int E) { return (size_t)(E + 1) * 4 + (size_t)kHistStride * (E + 1) * 4; }
+size_t route_smem_bytes(int E) { return (size_t)(E + 1) * (2 + kWhStride) * 4; }
 
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
                              bool invalid_tail, int4 *tiles, int *n_tiles, cudaStream_t s) {
     const size_t smem = route_smem_bytes(E);
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), smem, s, dim3(1), ids, (int)n_items, E, offsets, perm,
-                      invalid_tail ? 1 : 0, tiles, n_tiles);
+    // ranges of a multiple of 512 items, at most kRouteMaxCtas of them
+    int64_t range = (n_items + kRouteMaxCtas - 1) / kRouteMaxCtas;
+    range = (range + kRouteThreads - 1) / kRouteThreads * kRouteThreads;
+    if (range < kRouteThreads) range = kRouteThreads;
+    const int ctas = (int)((n_items + range - 1) / range);
+    return launch_pdl(route_kernel, dim3(ctas > 0 ? ctas : 1), dim3(kRouteThreads), smem, s, dim3(1), ids, (int)n_items,
+                      E, (int)range, offsets, perm, invalid_tail ? 1 : 0, tiles, n_tiles);
 }
 
 cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,

@@ -311,6 +311,25 @@ def test_moe_route_invalid_ids(ref):
     assert np.array_equal(G.host(off), want_off) and np.array_equal(G.host(perm), want_perm)
 
 
+
+@pytest.mark.parametrize("T,topk,E,skew", [(5000, 3, 1024, False), (4000, 2, 8, True), (70000, 8, 128, False)],
+                         ids=["E1024", "skewed", "560k_items"])
+def test_moe_route_many_ctas(ref, T, topk, E, skew):
+    # the routing spreads its items over up to 128 CTAs (ranges of a multiple of 512):
+    # positions must still be the stable order across range boundaries, invalid ids included
+    rng = np.random.default_rng(T)
+    if skew:
+        ids = np.where(rng.random((T, topk)) < 0.9, 3, rng.integers(-1, E + 1, (T, topk))).astype(np.int32)
+    else:
+        ids = rng.integers(-2, E + 2, (T, topk)).astype(np.int32)
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * topk, dtype=torch.int32, device="cuda")
+    q4k.q4k_moe_route(G.dev(ids), T, topk, E, off, perm)
+    torch.cuda.synchronize()
+    want_off, want_perm, _ = ref.moe_route(ids, E)
+    assert np.array_equal(G.host(off), want_off) and np.array_equal(G.host(perm), want_perm)
+
+
 def run_moe(w_blocks, E, N, K, x, x_mode, ids, gates, y_mode, w_dev=None):
     T, topk = ids.shape
     w = w_dev if w_dev is not None else G.dev(w_blocks)
