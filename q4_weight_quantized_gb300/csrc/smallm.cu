@@ -116,6 +116,82 @@ __device__ __forceinline__ void decode_scales(const uint8_t *blk, float *table_r
     for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
+// After a wait gave up: wait (each wait bounded too) for the copies this warp
+// still has in flight, ring iterations [from, to), so that none lands after the
+// CTA has left.
+template <int SLOTS>
+__device__ __forceinline__ void drain_ring(uint32_t bar0, int from, int to, unsigned int *status) {
+    for (int k = from; k < to; ++k) (void)mbar_wait(bar0 + 8 * (k % SLOTS), (k / SLOTS) & 1, status);
+}
+
+// acc += one staged block: the ROWS = 16*RT weight rows of `wst` (144 bytes each),
+// the activations of 8*NT token slots in `xs` (512 bytes each; only `live`
+// 8-token tiles are read) and the rows' (d*sc, bias) table.  Lane (r, c) of the
+// MMA fragment layout.  Per 32-weight sub-block s of a row:
+//     acc += (d sc_s) C_s - bias_s S_s,  C_s = sum (128 + q) x,  S_s = sum x.
+template <int NT, bool ONE, int RT>
+__device__ __forceinline__ void block_mma(const uint8_t *wst, const uint8_t *xs, const float *table,
+                                          const bool (&live)[NT], float (&acc)[RT][NT][4], int r, int c) {
+    constexpr int kRowTiles = RT;
+    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        // activations for sub-blocks 2g (xl) and 2g+1 (xh), per 8-token tile
+        uint32_t xl[NT][4], xh[NT][4];
+        float sl[NT][4], sh[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+            if (live[nt]) {
+                const uint8_t *xp = xs + (nt * 8 + r) * kXBlkBytes + 128 * g + 16 * c;
+                a = *reinterpret_cast<const uint4 *>(xp);
+                b = *reinterpret_cast<const uint4 *>(xp + 64);
+            }
+            xl[nt][0] = a.x; xl[nt][1] = a.y; xl[nt][2] = a.z; xl[nt][3] = a.w;
+            xh[nt][0] = b.x; xh[nt][1] = b.y; xh[nt][2] = b.z; xh[nt][3] = b.w;
+            mma_bf16_16816(sl[nt], ones, xl[nt][0], xl[nt][1], zero4);
+            mma_bf16_16816(sl[nt], ones, xl[nt][2], xl[nt][3], sl[nt]);
+            mma_bf16_16816(sh[nt], ones, xh[nt][0], xh[nt][1], zero4);
+            mma_bf16_16816(sh[nt], ones, xh[nt][2], xh[nt][3], sh[nt]);
+        }
+#pragma unroll
+        for (int rt = 0; rt < kRowTiles; ++rt) {
+            const int rA = rt * 16 + r, rB = rA + 8;
+            const uint2 wa = *reinterpret_cast<const uint2 *>(wst + rA * kBlockBytes + 16 + 32 * g + 8 * c);
+            const uint2 wb = *reinterpret_cast<const uint2 *>(wst + rB * kBlockBytes + 16 + 32 * g + 8 * c);
+            uint32_t alo0[4], alo1[4], ahi0[4], ahi1[4];
+            // word 0 (elements 8c..8c+3) feeds MMA 0, word 1 (8c+4..8c+7) MMA 1
+            unpack_word(wa.x, alo0[0], alo0[2], ahi0[0], ahi0[2]);
+            unpack_word(wb.x, alo0[1], alo0[3], ahi0[1], ahi0[3]);
+            unpack_word(wa.y, alo1[0], alo1[2], ahi1[0], ahi1[2]);
+            unpack_word(wb.y, alo1[1], alo1[3], ahi1[1], ahi1[3]);
+            const float4 sa = *reinterpret_cast<const float4 *>(table + rA * (kTableRowBytes / 4) + 4 * g);
+            const float4 sb = *reinterpret_cast<const float4 *>(table + rB * (kTableRowBytes / 4) + 4 * g);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float cl[4], chh[4];
+                mma_bf16_16816(cl, alo0, xl[nt][0], xl[nt][1], zero4);
+                mma_bf16_16816(cl, alo1, xl[nt][2], xl[nt][3], cl);
+                mma_bf16_16816(chh, ahi0, xh[nt][0], xh[nt][1], zero4);
+                mma_bf16_16816(chh, ahi1, xh[nt][2], xh[nt][3], chh);
+                float *a4 = acc[rt][nt];
+                // sub-block 2g, then 2g+1; accumulators 1 and 3 hold odd tokens
+                a4[0] = fmaf(sa.x, cl[0], a4[0]); a4[0] = fmaf(-sa.y, sl[nt][0], a4[0]);
+                a4[2] = fmaf(sb.x, cl[2], a4[2]); a4[2] = fmaf(-sb.y, sl[nt][2], a4[2]);
+                a4[0] = fmaf(sa.z, chh[0], a4[0]); a4[0] = fmaf(-sa.w, sh[nt][0], a4[0]);
+                a4[2] = fmaf(sb.z, chh[2], a4[2]); a4[2] = fmaf(-sb.w, sh[nt][2], a4[2]);
+                if constexpr (!ONE) {
+                    a4[1] = fmaf(sa.x, cl[1], a4[1]); a4[1] = fmaf(-sa.y, sl[nt][1], a4[1]);
+                    a4[3] = fmaf(sb.x, cl[3], a4[3]); a4[3] = fmaf(-sb.y, sl[nt][3], a4[3]);
+                    a4[1] = fmaf(sa.z, chh[1], a4[1]); a4[1] = fmaf(-sa.w, sh[nt][1], a4[1]);
+                    a4[3] = fmaf(sb.z, chh[3], a4[3]); a4[3] = fmaf(-sb.w, sh[nt][3], a4[3]);
+                }
+            }
+        }
+    }
+}
+
 // Where each token slot of a chunk reads its activation row and writes its
 // output row.  Dense: slot n is token n.  MoE: slot n of a token tile is the
 // (token, k-slot) item perm[first + n], first being the tile's first position
@@ -249,8 +325,6 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const bool early = !MOE && ra.early_w;
     for (int it = 0; it < SLOTS && it < total; ++it) issue(it, !early);
 
-    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
-    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     float acc[kRowTiles][NT][4];
     bool aborted = false;
     int it = 0;
@@ -282,61 +356,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
                     decode_scales(wst + (lane + 32) * kBlockBytes, table + (lane + 32) * (kTableRowBytes / 4));
             }
             __syncwarp();
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                // activations for sub-blocks 2g (xl) and 2g+1 (xh), per 8-token tile
-                uint32_t xl[NT][4], xh[NT][4];
-                float sl[NT][4], sh[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-                    if (live[nt]) {
-                        const uint8_t *xp = xs + (nt * 8 + r) * kXBlkBytes + 128 * g + 16 * c;
-                        a = *reinterpret_cast<const uint4 *>(xp);
-                        b = *reinterpret_cast<const uint4 *>(xp + 64);
-                    }
-                    xl[nt][0] = a.x; xl[nt][1] = a.y; xl[nt][2] = a.z; xl[nt][3] = a.w;
-                    xh[nt][0] = b.x; xh[nt][1] = b.y; xh[nt][2] = b.z; xh[nt][3] = b.w;
-                    mma_bf16_16816(sl[nt], ones, xl[nt][0], xl[nt][1], zero4);
-                    mma_bf16_16816(sl[nt], ones, xl[nt][2], xl[nt][3], sl[nt]);
-                    mma_bf16_16816(sh[nt], ones, xh[nt][0], xh[nt][1], zero4);
-                    mma_bf16_16816(sh[nt], ones, xh[nt][2], xh[nt][3], sh[nt]);
-                }
-#pragma unroll
-                for (int rt = 0; rt < kRowTiles; ++rt) {
-                    const int rA = rt * 16 + r, rB = rA + 8;
-                    const uint2 wa = *reinterpret_cast<const uint2 *>(wst + rA * kBlockBytes + 16 + 32 * g + 8 * c);
-                    const uint2 wb = *reinterpret_cast<const uint2 *>(wst + rB * kBlockBytes + 16 + 32 * g + 8 * c);
-                    uint32_t alo0[4], alo1[4], ahi0[4], ahi1[4];
-                    // word 0 (elements 8c..8c+3) feeds MMA 0, word 1 (8c+4..8c+7) MMA 1
-                    unpack_word(wa.x, alo0[0], alo0[2], ahi0[0], ahi0[2]);
-                    unpack_word(wb.x, alo0[1], alo0[3], ahi0[1], ahi0[3]);
-                    unpack_word(wa.y, alo1[0], alo1[2], ahi1[0], ahi1[2]);
-                    unpack_word(wb.y, alo1[1], alo1[3], ahi1[1], ahi1[3]);
-                    const float4 sa = *reinterpret_cast<const float4 *>(table + rA * (kTableRowBytes / 4) + 4 * g);
-                    const float4 sb = *reinterpret_cast<const float4 *>(table + rB * (kTableRowBytes / 4) + 4 * g);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        float cl[4], chh[4];
-                        mma_bf16_16816(cl, alo0, xl[nt][0], xl[nt][1], zero4);
-                        mma_bf16_16816(cl, alo1, xl[nt][2], xl[nt][3], cl);
-                        mma_bf16_16816(chh, ahi0, xh[nt][0], xh[nt][1], zero4);
-                        mma_bf16_16816(chh, ahi1, xh[nt][2], xh[nt][3], chh);
-                        float *a4 = acc[rt][nt];
-                        // sub-block 2g, then 2g+1; accumulators 1 and 3 hold odd tokens
-                        a4[0] = fmaf(sa.x, cl[0], a4[0]); a4[0] = fmaf(-sa.y, sl[nt][0], a4[0]);
-                        a4[2] = fmaf(sb.x, cl[2], a4[2]); a4[2] = fmaf(-sb.y, sl[nt][2], a4[2]);
-                        a4[0] = fmaf(sa.z, chh[0], a4[0]); a4[0] = fmaf(-sa.w, sh[nt][0], a4[0]);
-                        a4[2] = fmaf(sb.z, chh[2], a4[2]); a4[2] = fmaf(-sb.w, sh[nt][2], a4[2]);
-                        if constexpr (!ONE) {
-                            a4[1] = fmaf(sa.x, cl[1], a4[1]); a4[1] = fmaf(-sa.y, sl[nt][1], a4[1]);
-                            a4[3] = fmaf(sb.x, cl[3], a4[3]); a4[3] = fmaf(-sb.y, sl[nt][3], a4[3]);
-                            a4[1] = fmaf(sa.z, chh[1], a4[1]); a4[1] = fmaf(-sa.w, sh[nt][1], a4[1]);
-                            a4[3] = fmaf(sb.z, chh[3], a4[3]); a4[3] = fmaf(-sb.w, sh[nt][3], a4[3]);
-                        }
-                    }
-                }
-            }
+            block_mma<NT, ONE, kRowTiles>(wst, xs, table, live, acc, r, c);
             // the slot is consumed: order the reads before the copy that refills it
             __syncwarp();
             fence_proxy_async_smem();
@@ -395,6 +415,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             __syncthreads();  // red_w and the token table are reused by the next chunk
         }
     }
+    if (aborted) drain_ring<SLOTS>(bar0, it, min(total, it + SLOTS), status);
     if constexpr (MOE) return;
 
     __syncthreads();  // all slots consumed: the rings become reduction space
