@@ -26,8 +26,10 @@
 //     its partial tile in its idle stage buffers and every rank sums one slice of
 //     columns over the cluster's distributed shared memory, in rank order - no
 //     workspace, no atomics.
-// Every wait is bounded; the accumulator is a plain sum per output element in a
-// fixed order, so the result is run-to-run deterministic.
+// Every wait is bounded.  After one gives up, the producer waits (bounded) for
+// the copies it still has in flight and tensor memory is freed only after the
+// MMAs issued so far have completed.  The accumulator is a plain sum per output
+// element in a fixed order, so the result is run-to-run deterministic.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,7 +54,7 @@ struct Cfg {
     static constexpr int a_off = NS * XB;
     static constexpr int raw_off = a_off + NS * kABytes;
     static constexpr int bar_off = raw_off + 2 * kRawBytes;
-    static constexpr int n_bars = 2 * NS + 5;
+    static constexpr int n_bars = 3 * NS + 5;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;  // + slack to align the base to 1024
 };
@@ -71,21 +73,11 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t
     hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
 }
 
-// MoE mode: the CTA's token tile comes from the routing's tile list; its
-// activation rows are rows [first, first + count) of the expert-sorted
-// activation copy, and output column j goes to the row of item perm[first + j].
-struct GatherArgs {
-    const int32_t *perm;
-    const int4 *tiles;  // (expert, first item, item count, -)
-    const int *n_tiles;
-};
-
-template <int BN, bool GATHER>
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
-                                                              int64_t ldy, int M, int N, int KB, GatherArgs ga,
-                                                              unsigned int *status) {
-    pdl_wait();  // the tile list (routing) and the activations may come from the previous kernel
+                                                              int64_t ldy, int M, int N, int KB, unsigned int *status) {
+    pdl_wait();  // the activations may come from the previous kernel
     pdl_trigger();
     using C = Cfg<BN>;
     constexpr int NS = C::NS;
@@ -95,26 +87,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint8_t *as = base + C::a_off;
     uint8_t *raw = base + C::raw_off;
     const uint32_t bar = smem_u32(base + C::bar_off);
-    const uint32_t full0 = bar, empty0 = bar + 8 * NS, rfull0 = bar + 16 * NS, rempty0 = rfull0 + 16,
-                   accfull = rempty0 + 16;
+    // full: the four dequant warps wrote the stage's operand; xfull: its activation
+    // copy landed (tx bytes); empty: the MMAs reading the stage are done; rfull /
+    // rempty: the raw Q4_K tile ring; accfull: all MMAs of the tile are done
+    const uint32_t full0 = bar, empty0 = bar + 8 * NS, xfull0 = bar + 16 * NS, rfull0 = bar + 24 * NS,
+                   rempty0 = rfull0 + 16, accfull = rempty0 + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + C::misc_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::misc_off + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileRows;
-    int m0 = blockIdx.y * BN;
-    int wrow0 = n0;  // first weight row of the tile in the tensor map
-    int mma_n = BN;  // MMA N (tokens): BN, or the tile's item count rounded up to 16
-    __shared__ int orow_s[GATHER ? BN : 1];
-    if constexpr (GATHER) {
-        if ((int)blockIdx.y >= __ldg(ga.n_tiles)) return;  // beyond the routing's tiles: leave before any barrier
-        const int4 tl = __ldg(ga.tiles + blockIdx.y);
-        m0 = tl.y;  // rows of the expert-sorted activations
-        M = tl.y + tl.z;
-        wrow0 = tl.x * N + n0;
-        mma_n = (tl.z + 15) & ~15;
-        for (int j = threadIdx.x; j < tl.z; j += kThreads) orow_s[j] = __ldg(ga.perm + tl.y + j);
-    }
+    const int m0 = blockIdx.y * BN;
     // split K over a cluster of gridDim.z CTAs: this CTA takes blocks [kbeg, kbeg + KBs)
     const int S = gridDim.z, split = blockIdx.z;
     const int kbeg = (int)((int64_t)KB * split / S);
@@ -123,8 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8 * s, 1 + 4);  // producer (+ tx bytes) and the four dequant warps
-            mbar_init(empty0 + 8 * s, 1);     // tcgen05.commit
+            mbar_init(full0 + 8 * s, 4);   // the four dequant warps
+            mbar_init(xfull0 + 8 * s, 1);  // producer (+ tx bytes)
+            mbar_init(empty0 + 8 * s, 1);  // tcgen05.commit
         }
         for (int r = 0; r < 2; ++r) {
             mbar_init(rfull0 + 8 * r, 1);
@@ -149,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
             mbar_arrive_expect_tx(rfull0, kRawBytes);
-            tma_load_2d(smem_u32(raw), &tmW, kbeg * (kBlockBytes / 4), wrow0, rfull0);
+            tma_load_2d(smem_u32(raw), &tmW, kbeg * (kBlockBytes / 4), n0, rfull0);
+            int raw_issued = 1, x_issued = 0;
             for (int i = 0; i < total && !*abort_flag; ++i) {
                 const int kb = i >> 2, g = i & 3, s = i % NS;
                 if (g == 0 && kb + 1 < KBs) {  // raw tile of the next block, one block ahead
@@ -159,27 +144,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
-                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kbeg + kb + 1) * (kBlockBytes / 4), wrow0,
+                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kbeg + kb + 1) * (kBlockBytes / 4), n0,
                                 rfull0 + 8 * r);
+                    ++raw_issued;
                 }
                 if (i >= NS && !mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(full0 + 8 * s, C::XB);
-                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, full0 + 8 * s);
+                mbar_arrive_expect_tx(xfull0 + 8 * s, C::XB);
+                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, xfull0 + 8 * s);
+                ++x_issued;
+            }
+            if (*abort_flag) {
+                // a wait gave up somewhere: wait (bounded) for this CTA's copies still in flight
+                for (int j = raw_issued > 2 ? raw_issued - 2 : 0; j < raw_issued; ++j)
+                    (void)mbar_wait(rfull0 + 8 * (j & 1), (j >> 1) & 1, status);
+                for (int j = x_issued > NS ? x_issued - NS : 0; j < x_issued; ++j)
+                    (void)mbar_wait(xfull0 + 8 * (j % NS), (j / NS) & 1, status);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, mma_n);
-            bool ok = true;
+            const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, BN);
             for (int i = 0; i < total; ++i) {
                 const int s = i % NS;
-                if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status)) {
+                if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status) || !mbar_wait(xfull0 + 8 * s, (i / NS) & 1, status)) {
                     *abort_flag = 1;
-                    ok = false;
                     break;
                 }
                 tc_fence_after();
@@ -190,7 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
                 umma_commit(empty0 + 8 * s);
             }
-            if (ok) umma_commit(accfull);
+            // completes once every MMA issued above has (also after an abort, so
+            // that tensor memory is freed only after the MMAs that write it)
+            umma_commit(accfull);
         }
     } else {
         // ---------------------------------------------------- dequant warps
@@ -250,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         if (!ok && lane == 0) *abort_flag = 1;
         // ------------------------------------------------------- epilogue
-        if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(accfull, 0, status))) {
+        if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(accfull, 0, status)) && !*abort_flag) {
             tc_fence_after();
             const int q = warp & 3;  // tensor-memory lane quarter this warp may read
             const int rl = 32 * q + lane, n = n0 + rl;
@@ -258,19 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // buffers, column-major [BN][128], for the cluster reduction below
             float *part = reinterpret_cast<float *>(base);
 #pragma unroll 1
-            for (int cc = 0; cc < (GATHER ? (M - m0 + 31) / 32 : BN / 32); ++cc) {
+            for (int cc = 0; cc < BN / 32; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
                 tmem_ld_wait();
-                if constexpr (GATHER) {
-                    if (n < N) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int col = 32 * cc + j;
-                            if (col < M - m0) y[(int64_t)orow_s[col] * ldy + n] = __uint_as_float(v[j]);
-                        }
-                    }
-                } else if (S > 1) {
+                if (S > 1) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) part[(32 * cc + j) * kTileRows + rl] = __uint_as_float(v[j]);
                 } else if (n < N) {
@@ -305,6 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        // every MMA has completed (immediate on the normal path; after an abort,
+        // a bounded wait for the MMAs still running) before the columns are freed
+        (void)mbar_wait(accfull, 0, status);
         tc_fence_after();
         tmem_dealloc(tmem, BN);
     }
@@ -320,7 +309,7 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     if (e != cudaSuccess) return e;
     const int smem = Cfg<BN>::bytes;
     static_assert(Cfg<BN>::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers");
-    e = cudaFuncSetAttribute(gemm_tc_kernel<BN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const int64_t tiles = ((N + kTileRows - 1) / kTileRows) * ((M + BN - 1) / BN);
@@ -333,10 +322,9 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
         if (want > KB / 4) want = KB / 4;
         if (want > 1) S = (int)want;
     }
-    GatherArgs ga = {};
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
-    return launch_pdl(gemm_tc_kernel<BN, false>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
-                      tmX, y, ldy, (int)M, (int)N, KB, ga, di.status);
+    return launch_pdl(gemm_tc_kernel<BN>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW, tmX, y,
+                      ldy, (int)M, (int)N, KB, di.status);
 }
 
 }  // namespace
@@ -345,27 +333,6 @@ cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
     if (M <= 128) return launch_bn<128>(di, w, N, K, x, M, ldx, y, ldy, s);
     return launch_bn<256>(di, w, N, K, x, M, ldx, y, ldy, s);
-}
-
-cudaError_t launch_moe_tc(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
-                          const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
-                          const int *n_tiles, float *out, cudaStream_t s) {
-    constexpr int BN = kMoeTileItems;
-    CUtensorMap tmW, tmX;
-    cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kTileRows, kBlockBytes / 4);
-    if (e != cudaSuccess) return e;
-    e = make_act_tmap_sw128(&tmX, x_sorted, n_items, K, K, BN);
-    if (e != cudaSuccess) return e;
-    const int smem = Cfg<BN>::bytes;
-    e = cudaFuncSetAttribute(gemm_tc_kernel<BN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    GatherArgs ga;
-    ga.perm = perm;
-    ga.tiles = tiles;
-    ga.n_tiles = n_tiles;
-    const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)moe_max_tiles(E, n_items), 1);
-    return launch_pdl(gemm_tc_kernel<BN, true>, grid, dim3(kThreads), (size_t)smem, s, dim3(1), tmW, tmX, out, N, 0,
-                      (int)N, (int)(K / kQK), ga, di.status);
 }
 
 }  // namespace q4k

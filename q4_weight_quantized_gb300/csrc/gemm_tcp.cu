@@ -40,7 +40,7 @@ constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K per block
 constexpr int kDqWarps = 8, kEpWarps = 4;
 constexpr int kThreads = (2 + kDqWarps + kEpWarps) * 32;
 constexpr int kX = 0, kA = kNS * kXB, kRaw = kA + kNS * kAB, kBar = kRaw + 2 * kRawBytes;
-constexpr int kNBars = 2 * kNS + 2 + 2 + 2 + 2;
+constexpr int kNBars = 3 * kNS + 2 + 2 + 2 + 2 + 1;
 constexpr int kMisc = kBar + kNBars * 8;
 constexpr int kOrow = kMisc + 16;                   // [2][kBN] output rows (MoE)
 constexpr int kSmem = kOrow + 2 * kBN * 4 + 1024;   // + slack to align the base to 1024
@@ -106,8 +106,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
     uint8_t *as = base + kA;
     uint8_t *raw = base + kRaw;
     const uint32_t bar = smem_u32(base + kBar);
-    const uint32_t full0 = bar, empty0 = bar + 8 * kNS, rfull0 = bar + 16 * kNS, rempty0 = rfull0 + 16,
-                   accfull0 = rempty0 + 16, accempty0 = accfull0 + 16;
+    // full: the dequant warps wrote the stage's operand; xfull: its activation copy
+    // landed; empty: its MMAs are done; rfull / rempty: raw Q4_K ring; accfull /
+    // accempty: the two tensor-memory accumulators; mmadone: every MMA issued
+    const uint32_t full0 = bar, empty0 = bar + 8 * kNS, xfull0 = bar + 16 * kNS, rfull0 = bar + 24 * kNS,
+                   rempty0 = rfull0 + 16, accfull0 = rempty0 + 16, accempty0 = accfull0 + 16,
+                   mmadone = accempty0 + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kMisc + 4);
     int *orow = reinterpret_cast<int *>(base + kOrow);
@@ -124,8 +128,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(full0 + 8 * s, 1 + kDqWarps);  // producer (+ tx bytes) and the dequant warps
-            mbar_init(empty0 + 8 * s, 1);            // tcgen05.commit
+            mbar_init(full0 + 8 * s, kDqWarps);  // the dequant warps
+            mbar_init(xfull0 + 8 * s, 1);        // producer (+ tx bytes)
+            mbar_init(empty0 + 8 * s, 1);        // tcgen05.commit
         }
         for (int r = 0; r < 2; ++r) {
             mbar_init(rfull0 + 8 * r, 1);
@@ -133,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
             mbar_init(accfull0 + 8 * r, 1);          // tcgen05.commit
             mbar_init(accempty0 + 8 * r, kEpWarps);  // epilogue warps
         }
+        mbar_init(mmadone, 1);  // tcgen05.commit after the last MMA
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -151,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
             // raw block b = k * KB + kb (tile k of this CTA, block kb)
+            int raw_issued = 0, x_issued = 0;
             auto issue_raw = [&](int b) -> bool {
                 const Tile t = tile_of<GATHER>(p, b / KB);
                 const int r = b & 1;
@@ -158,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
                 tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (b % KB) * (kBlockBytes / 4), t.wrow0,
                             rfull0 + 8 * r);
+                ++raw_issued;
                 return true;
             };
             bool ok = issue_raw(0);
@@ -179,11 +187,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full0 + 8 * s, kXB);
-                    tma_load_2d(smem_u32(xs + s * kXB), &tmX, kb * kQK + kStageK * g, t.m0, full0 + 8 * s);
+                    mbar_arrive_expect_tx(xfull0 + 8 * s, kXB);
+                    tma_load_2d(smem_u32(xs + s * kXB), &tmX, kb * kQK + kStageK * g, t.m0, xfull0 + 8 * s);
+                    ++x_issued;
                 }
             }
             if (!ok) *abort_flag = 1;
+            if (*abort_flag) {
+                // a wait gave up somewhere: wait (bounded) for this CTA's copies still in flight
+                for (int j = raw_issued > 2 ? raw_issued - 2 : 0; j < raw_issued; ++j)
+                    (void)mbar_wait(rfull0 + 8 * (j & 1), (j >> 1) & 1, status);
+                for (int j = x_issued > kNS ? x_issued - kNS : 0; j < x_issued; ++j)
+                    (void)mbar_wait(xfull0 + 8 * (j % kNS), (j / kNS) & 1, status);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
@@ -202,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 const uint32_t d = tmem + (uint32_t)(buf * kBN);
                 for (int j = 0; j < KB * 4; ++j) {
                     const int i = k * KB * 4 + j, s = i % kNS;
-                    if (!mbar_wait(full0 + 8 * s, (i / kNS) & 1, status) || *abort_flag) {
+                    if (!mbar_wait(full0 + 8 * s, (i / kNS) & 1, status) ||
+                        !mbar_wait(xfull0 + 8 * s, (i / kNS) & 1, status) || *abort_flag) {
                         ok = false;
                         break;
                     }
@@ -217,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 if (ok) umma_commit(accfull0 + 8 * buf);
             }
             if (!ok) *abort_flag = 1;
+            umma_commit(mmadone);  // completes once every MMA issued above has
         }
     } else if (warp < 2 + kDqWarps) {
         // ---------------------------------------------------- dequant warps
@@ -320,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        (void)mbar_wait(mmadone, 0, status);  // no MMA still writes the columns
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

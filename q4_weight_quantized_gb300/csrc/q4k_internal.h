@@ -71,12 +71,6 @@ inline int64_t moe_max_tiles(int E, int64_t n_items) {
     return (n_items < E ? n_items : (int64_t)E) + (n_items + kMoeTileItems - 1) / kMoeTileItems;
 }
 
-// MoE on the tensor cores: one CTA per (128-row weight tile, token tile of the
-// routing's tile list), reading the expert-sorted activation rows x_sorted.
-cudaError_t launch_moe_tc(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
-                          const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
-                          const int *n_tiles, float *out, cudaStream_t s);
-
 // x_sorted[p] = activation row of item perm[p] (p < offsets[E]): per-token rows
 // (x[item / topk]) or per-slot rows (x[item]), K bf16 each.  With zero_y, the N
 // floats of zero_y's row of every invalid item (perm[offsets[E] .. n_items)) are
