@@ -1,4 +1,4 @@
-// Persistent prefill / MoE Q4_K GEMM on the tcgen05 tensor cores.
+// Persistent MoE expert Q4_K GEMM on the tcgen05 tensor cores.
 //
 // Same arithmetic as gemm_tc.cu (per-tile dequantization of Q4_K into a bf16
 // operand in shared memory, tcgen05.mma into an fp32 tensor-memory accumulator;
@@ -15,11 +15,12 @@
 //               the K-major 128-byte-swizzled bf16 operand;
 //   * warps 10-13 epilogue: tcgen05.ld of the finished accumulator and fp32
 //               stores, while the MMA warp already fills the other accumulator.
-// Tiles are taken round-robin (tile = CTA + k * grid).  In MoE mode the token
-// tiles come from the routing's tile list (expert, first item, count), the MMA
-// width is the count rounded up to 16, and output column j goes to the row of
-// item perm[first + j].  Every wait is bounded; the sum per output element runs
-// in a fixed order, so results are run-to-run deterministic.
+// Tiles are (128-row weight tile, token tile of the routing's list) pairs taken
+// round-robin (tile = CTA + k * grid).  A token tile is (expert, first item,
+// count <= 256) of the expert-sorted activation rows; the MMA width is the count
+// rounded up to 16, and output column j goes to the row of item perm[first + j].
+// Every wait is bounded; the sum per output element runs in a fixed order, so
+// results are run-to-run deterministic.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,11 +54,11 @@ struct Tile {
 struct Params {
     float *y;
     int64_t ldy;
-    int M, N, KB;
-    int tiles_n, tiles_m;  // dense: output tiles along N and M
-    const int32_t *perm;   // MoE
+    int N, KB;
+    int tiles_n;           // 128-row weight tiles per expert
+    const int32_t *perm;   // routing permutation
     const int4 *tiles;     // MoE: (expert, first item, count, -)
-    const int *n_tiles;    // MoE: number of token tiles
+    const int *n_tiles;    // number of token tiles
     unsigned int *status;
 };
 
@@ -76,29 +77,21 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t
     hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
 }
 
-template <bool GATHER>
 __device__ __forceinline__ Tile tile_of(const Params &p, int k) {
     const int tile = blockIdx.x + k * gridDim.x;
     const int nt = tile % p.tiles_n, mt = tile / p.tiles_n;
+    const int4 tl = __ldg(p.tiles + mt);
     Tile t;
     t.n0 = nt * kTileRows;
-    if constexpr (GATHER) {
-        const int4 tl = __ldg(p.tiles + mt);
-        t.m0 = tl.y;
-        t.cnt = tl.z;
-        t.wrow0 = tl.x * p.N + t.n0;
-    } else {
-        t.m0 = mt * kBN;
-        t.cnt = min(kBN, p.M - t.m0);
-        t.wrow0 = t.n0;
-    }
+    t.m0 = tl.y;
+    t.cnt = tl.z;
+    t.wrow0 = tl.x * p.N + t.n0;
     return t;
 }
 
-template <bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                const __grid_constant__ CUtensorMap tmX, Params p) {
-    pdl_wait();  // the tile list and the sorted activations come from the routing kernels
+    pdl_wait();  // the tile list and the sorted activations come from the routing and gather kernels
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -118,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
     unsigned int *status = p.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = GATHER ? __ldg(p.n_tiles) : p.tiles_m;
+    const int tiles_m = __ldg(p.n_tiles);
     const int total_tiles = p.tiles_n * tiles_m;
     const int my_tiles =
         (int)blockIdx.x < total_tiles ? (total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
@@ -159,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
             // raw block b = k * KB + kb (tile k of this CTA, block kb)
             int raw_issued = 0, x_issued = 0;
             auto issue_raw = [&](int b) -> bool {
-                const Tile t = tile_of<GATHER>(p, b / KB);
+                const Tile t = tile_of(p, b / KB);
                 const int r = b & 1;
                 if (b >= 2 && !mbar_wait(rempty0 + 8 * r, ((b >> 1) - 1) & 1, status)) return false;
                 mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
@@ -169,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 return true;
             };
             bool ok = issue_raw(0);
-            Tile t = tile_of<GATHER>(p, 0);
+            Tile t = tile_of(p, 0);
             for (int b = 0; b < nblocks && ok; ++b) {
                 const int kb = b % KB;
-                if (kb == 0 && b > 0) t = tile_of<GATHER>(p, b / KB);
+                if (kb == 0 && b > 0) t = tile_of(p, b / KB);
                 if (b + 1 < nblocks && !issue_raw(b + 1)) {
                     ok = false;
                     break;
@@ -206,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
         if (lane == 0) {
             bool ok = true;
             for (int k = 0; k < my_tiles && ok; ++k) {
-                const Tile t = tile_of<GATHER>(p, k);
-                const int mma_n = GATHER ? (t.cnt + 15) & ~15 : kBN;
+                const Tile t = tile_of(p, k);
+                const int mma_n = (t.cnt + 15) & ~15;
                 const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, mma_n);
                 const int buf = k & 1;
                 if (k >= 2 && !mbar_wait(accempty0 + 8 * buf, ((k >> 1) - 1) & 1, status)) {
@@ -301,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         const int et = threadIdx.x - (2 + kDqWarps) * 32;
         for (int k = 0; k < my_tiles; ++k) {
-            const Tile t = tile_of<GATHER>(p, k);
+            const Tile t = tile_of(p, k);
             const int buf = k & 1;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(accfull0 + 8 * buf, (k >> 1) & 1, status))) {
                 if (lane == 0) *abort_flag = 1;
@@ -309,10 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
             }
             tc_fence_after();
             int *orw = orow + buf * kBN;
-            if constexpr (GATHER) {
-                for (int j = et; j < t.cnt; j += kEpWarps * 32) orw[j] = __ldg(p.perm + t.m0 + j);
-                asm volatile("bar.sync 2, %0;" ::"n"(kEpWarps * 32) : "memory");
-            }
+            for (int j = et; j < t.cnt; j += kEpWarps * 32) orw[j] = __ldg(p.perm + t.m0 + j);
+            asm volatile("bar.sync 2, %0;" ::"n"(kEpWarps * 32) : "memory");
             const int n = t.n0 + 32 * q + lane;
 #pragma unroll 1
             for (int cc = 0; cc < (t.cnt + 31) / 32; ++cc) {
@@ -324,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                     for (int j = 0; j < 32; ++j) {
                         const int col = 32 * cc + j;
                         if (col < t.cnt) {
-                            const int64_t yrow = GATHER ? (int64_t)orw[col] : (int64_t)(t.m0 + col);
+                            const int64_t yrow = orw[col];
                             p.y[yrow * p.ldy + n] = __uint_as_float(v[j]);
                         }
                     }
@@ -344,39 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
     }
 }
 
-template <bool GATHER>
-cudaError_t launch(const DeviceInfo &di, const CUtensorMap &tmW, const CUtensorMap &tmX, const Params &p,
-                   int grid, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tcp_kernel<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+cudaError_t launch(const CUtensorMap &tmW, const CUtensorMap &tmX, const Params &p, int grid, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tcp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(gemm_tcp_kernel<GATHER>, dim3(grid), dim3(kThreads), kSmem, s, dim3(1), tmW, tmX, p);
+    return launch_pdl(gemm_tcp_kernel, dim3(grid), dim3(kThreads), kSmem, s, dim3(1), tmW, tmX, p);
 }
 
 }  // namespace
-
-int gemm_tcp_tiles(int64_t M, int64_t N) {
-    return (int)(((N + kTileRows - 1) / kTileRows) * ((M + kBN - 1) / kBN));
-}
-
-cudaError_t launch_gemm_tcp(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
-    CUtensorMap tmW, tmX;
-    cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
-    if (e != cudaSuccess) return e;
-    e = make_act_tmap_sw128(&tmX, x, M, K, ldx, kBN);
-    if (e != cudaSuccess) return e;
-    Params p = {};
-    p.y = y;
-    p.ldy = ldy;
-    p.M = (int)M;
-    p.N = (int)N;
-    p.KB = (int)(K / kQK);
-    p.tiles_n = (int)((N + kTileRows - 1) / kTileRows);
-    p.tiles_m = (int)((M + kBN - 1) / kBN);
-    p.status = di.status;
-    const int tiles = p.tiles_n * p.tiles_m;
-    return launch<false>(di, tmW, tmX, p, tiles < di.sm_count ? tiles : di.sm_count, s);
-}
 
 cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                            const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
@@ -396,7 +361,7 @@ cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, i
     p.tiles = tiles;
     p.n_tiles = n_tiles;
     p.status = di.status;
-    return launch<true>(di, tmW, tmX, p, di.sm_count, s);
+    return launch(tmW, tmX, p, di.sm_count, s);
 }
 
 }  // namespace q4k

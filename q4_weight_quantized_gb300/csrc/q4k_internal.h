@@ -36,11 +36,9 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
 
-// Persistent variant for many output tiles (one CTA per SM, double-buffered
-// tensor-memory accumulators, 256-token tiles; gemm_tcp.cu).
-int gemm_tcp_tiles(int64_t M, int64_t N);
-cudaError_t launch_gemm_tcp(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
+// MoE expert GEMM on the tensor cores: a persistent kernel (one CTA per SM,
+// double-buffered tensor-memory accumulators) walking the routing's token tiles
+// over the expert-sorted activation rows x_sorted (gemm_tcp.cu).
 cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                            const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
                            const int *n_tiles, float *out, cudaStream_t s);

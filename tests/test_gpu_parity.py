@@ -261,9 +261,8 @@ def test_prefill_split_k_ragged(ref, M, N, K):
     assert G.rel_err(gpu_gemm(b, N, K, x), ref.gemm(b, N, K, x, threads=16)) <= TOL_TC
 
 
-def test_prefill_persistent_ragged(ref):
-    # enough 128 x 256 tiles for the persistent kernel, ragged in M (600 = 2*256 + 88)
-    # and N (6600 = 51*128 + 72); several tiles per CTA
+def test_prefill_many_tiles_ragged(ref):
+    # more 128 x 256 tiles than SMs, ragged in M (600 = 2*256 + 88) and N (6600 = 51*128 + 72)
     M, N, K = 600, 6600, 1024
     b = G.weights(3, 5, N, K, outliers=True)
     x = G.activations(3, 6, M, K)
