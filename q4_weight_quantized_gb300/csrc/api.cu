@@ -68,9 +68,54 @@ cudaError_t device_info(DeviceInfo *out) {
     return cudaSuccess;
 }
 
-// Weight matrix as a 2-D uint32 tensor: dims {K/256*36, N}, row pitch K/256*144
-// bytes; tiles of box_rows rows x box_words words, no swizzle, zero fill outside.
-cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K, int box_rows, int box_words) {
+cudaError_t ensure_smem(const void *kern, int bytes) {
+    struct Entry {
+        const void *kern;
+        int device, bytes;
+    };
+    static std::mutex mu;
+    static Entry table[256];
+    static int used = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    int i = 0;
+    while (i < used && !(table[i].kern == kern && table[i].device == dev)) ++i;
+    if (i < used && table[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (i < used) {
+        table[i].bytes = bytes;
+    } else if (used < 256) {
+        table[used++] = {kern, dev, bytes};
+    }
+    return cudaSuccess;
+}
+
+// Encoding a descriptor costs host time on every call; the last few per thread
+// are kept, keyed by everything that goes into them.
+struct TmapKey {
+    const void *ptr;
+    int64_t d0, d1, stride;
+    int box0, box1, kind;
+    bool operator==(const TmapKey &o) const {
+        return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && stride == o.stride && box0 == o.box0 && box1 == o.box1 &&
+               kind == o.kind;
+    }
+};
+
+static cudaError_t encode_cached(CUtensorMap *m, const TmapKey &k, CUtensorMapDataType dtype, CUtensorMapSwizzle sw) {
+    constexpr int kSlots = 16;
+    thread_local TmapKey keys[kSlots];
+    thread_local CUtensorMap maps[kSlots];
+    thread_local bool valid[kSlots] = {};
+    thread_local int next = 0;
+    for (int i = 0; i < kSlots; ++i)
+        if (valid[i] && keys[i] == k) {
+            *m = maps[i];
+            return cudaSuccess;
+        }
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -80,59 +125,41 @@ cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
     if (!g_encode) return cudaErrorNotSupported;
-    const int64_t KB = K / kQK;
-    cuuint64_t dims[2] = {(cuuint64_t)(KB * (kBlockBytes / 4)), (cuuint64_t)N};
-    cuuint64_t strides[1] = {(cuuint64_t)(KB * kBlockBytes)};
-    cuuint32_t box[2] = {(cuuint32_t)box_words, (cuuint32_t)box_rows};
+    cuuint64_t dims[2] = {(cuuint64_t)k.d0, (cuuint64_t)k.d1};
+    cuuint64_t strides[1] = {(cuuint64_t)k.stride};
+    cuuint32_t box[2] = {(cuuint32_t)k.box0, (cuuint32_t)k.box1};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(w), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    CUresult r = g_encode(m, dtype, 2, const_cast<void *>(k.ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    keys[next] = k;
+    maps[next] = *m;
+    valid[next] = true;
+    next = (next + 1) % kSlots;
+    return cudaSuccess;
+}
+
+// Weight matrix as a 2-D uint32 tensor: dims {K/256*36, N}, row pitch K/256*144
+// bytes; tiles of box_rows rows x box_words words, no swizzle, zero fill outside.
+cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K, int box_rows, int box_words) {
+    const int64_t KB = K / kQK;
+    const TmapKey k = {w, KB * (kBlockBytes / 4), N, KB * kBlockBytes, box_words, box_rows, 0};
+    return encode_cached(m, k, CU_TENSOR_MAP_DATA_TYPE_UINT32, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Activations [rows][ld] bf16 as a 2-D uint64 tensor (4 bf16 per element): dims
 // {K/4, rows}, row pitch ld*2 bytes, box {box_elems, 1 row}.
 cudaError_t make_act_tmap(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_elems) {
-    std::call_once(g_encode_once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (!g_encode) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {(cuuint64_t)(K / 4), (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    cuuint32_t box[2] = {(cuuint32_t)box_elems, 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(x), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    const TmapKey k = {x, K / 4, rows, ld * 2, box_elems, 1, 1};
+    return encode_cached(m, k, CU_TENSOR_MAP_DATA_TYPE_UINT64, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Activations [rows][ld] bf16 for the tensor-core path: dims {K, rows}, box {64,
 // box_rows}, 128-byte swizzle (the K-major operand layout tcgen05.mma reads).
 cudaError_t make_act_tmap_sw128(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_rows) {
-    std::call_once(g_encode_once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (!g_encode) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    const TmapKey k = {x, K, rows, ld * 2, 64, box_rows, 2};
+    return encode_cached(m, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace q4k

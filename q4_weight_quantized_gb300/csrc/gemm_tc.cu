@@ -309,7 +309,7 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     if (e != cudaSuccess) return e;
     const int smem = Cfg<BN>::bytes;
     static_assert(Cfg<BN>::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers");
-    e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = ensure_smem((const void *)gemm_tc_kernel<BN>, smem);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const int64_t tiles = ((N + kTileRows - 1) / kTileRows) * ((M + BN - 1) / BN);

@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
 }
 
 cudaError_t launch(const CUtensorMap &tmW, const CUtensorMap &tmX, const Params &p, int grid, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tcp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = ensure_smem((const void *)gemm_tcp_kernel, kSmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(gemm_tcp_kernel, dim3(grid), dim3(kThreads), kSmem, s, dim3(1), tmW, tmX, p);
 }

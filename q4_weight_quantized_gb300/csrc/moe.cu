@@ -233,7 +233,7 @@ size_t route_smem_bytes(int E) { return (size_t)(E + 1) * (2 + kWhStride) * 4; }
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
                              bool invalid_tail, int4 *tiles, int *n_tiles, cudaStream_t s) {
     const size_t smem = route_smem_bytes(E);
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem((const void *)route_kernel, (int)smem);
     if (e != cudaSuccess) return e;
     // ranges of a multiple of 512 items, at most kRouteMaxCtas of them
     int64_t range = (n_items + kRouteMaxCtas - 1) / kRouteMaxCtas;

@@ -112,6 +112,11 @@ cudaError_t launch_pdl(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem,
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Raises `kern`'s dynamic shared-memory limit on the current device to at least
+// `bytes`; calls cudaFuncSetAttribute only the first time a larger limit is
+// needed (process-wide cache, thread-safe).
+cudaError_t ensure_smem(const void *kern, int bytes);
+
 // TMA descriptor of a Q4_K matrix viewed as uint32 words: dims {K/256*36, N},
 // row pitch K/256*144 bytes, box {box_words, box_rows}, zero fill outside.
 cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K, int box_rows, int box_words);

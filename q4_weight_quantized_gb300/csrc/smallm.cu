@@ -470,7 +470,7 @@ cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CU
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
     const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE);
     auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmX, ra, N, KB, nx,
                       status);
@@ -485,7 +485,7 @@ int resident_ctas(const DeviceInfo &di) {
         const int smem = Geo<ROWS>::smem_total(1, 2, false);
         auto kern = smallm_kernel<1, false, true, 2, ROWS>;
         int n = 0;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = ensure_smem((const void *)kern, smem);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
         slot = e == cudaSuccess && n > 0 ? n : 1;
     }
