@@ -69,8 +69,10 @@ struct Geo {
     __host__ __device__ static constexpr int red_off(int nx, int slots) {
         return bars_off(nx, slots) + kWarps * slots * 8 + 64;
     }
-    __host__ __device__ static constexpr int smem_total(int nx, int slots, bool moe) {
-        return red_off(nx, slots) + (moe ? kRedBytes : 0);
+    // `red`: the MoE K-split mode's reduction buffer (the row-split mode stages its
+    // outputs in each warp's scale table, the dense mode reuses the rings)
+    __host__ __device__ static constexpr int smem_total(int nx, int slots, bool red) {
+        return red_off(nx, slots) + (red ? kRedBytes : 0);
     }
     static_assert(ROWS % 16 == 0 && ROWS <= 64, "rows per CTA");
     static_assert(kRedBytes <= kWarps * 2 * slot_bytes(1), "dense reduction buffers alias the rings");
@@ -232,8 +234,10 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // only the accumulators that hold it).  SLOTS: ring depth per warp.  ROWS:
 // weight rows per warp tile (32 or 48).  RS (MoE with few K blocks): the warps
 // split rows instead of K - warp w owns rows w*ROWS.. of a 4*ROWS-row CTA over
-// all K blocks and stores its own outputs, with no cross-warp reduction.
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false>
+// all K blocks and stores its own outputs, with no cross-warp reduction.  CH:
+// token slots per chunk (at most 8 * NT; fewer shrinks the activation part of a
+// slot when experts get few items).
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
                                                           int KB, int nx, unsigned int *status) {
@@ -243,7 +247,8 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
 
     using G = Geo<ROWS>;
     constexpr int kRows = ROWS, kRowTiles = G::kRowTiles, kBlkWBytes = G::kBlkWBytes;
-    constexpr int kPerChunk = 8 * NT;
+    constexpr int kPerChunk = CH;
+    static_assert(CH <= 8 * NT && (CH == 8 * NT || (MOE && RS)), "chunk size");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = lane & 3, r = lane >> 2;
     const int S = gridDim.x;       // K split = cluster size (always 1 for MoE)
@@ -363,9 +368,11 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             if (it + SLOTS < total) issue(it + SLOTS, true);
         }
         if constexpr (MOE && RS) {
-            // row split: this warp stores its own rows of the chunk, staged through
-            // its [16][kRows] slice so that the stores coalesce
-            float *mine = reinterpret_cast<float *>(smem + G::red_off(nx, SLOTS)) + warp * 16 * kRows;
+            // row split: this warp stores its own rows of the chunk, staged as
+            // [16][kRows] in its scale table (free until the next chunk's first
+            // block) so that the stores coalesce
+            static_assert(16 * 32 * 4 <= kTableRowBytes * 32, "the stage fits in the table");
+            float *mine = table;
 #pragma unroll
             for (int rt = 0; rt < kRowTiles; ++rt)
 #pragma unroll
@@ -465,11 +472,11 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     }
 }
 
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false>
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
-    const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS>;
+    const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS);
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmX, ra, N, KB, nx,
@@ -577,9 +584,17 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     // layers past the routing's tile count leave at once
     const int layers = (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
     if (rs) {
+        // chunks of 4 token slots while experts get 4 items or fewer on average; a
+        // third ring slot while the CTAs of the experts with items fit on the SMs at once
+        const bool deep = rs_ctas <= di.sm_count;
+        const int n = (int)N;
+        if (items <= 4 * (int64_t)E)
+            return deep ? launch_cfg<1, true, false, 3, 32, true, 4>(1, tiles, layers, 4, s, tmW, tmX, ra, n, KB, di.status)
+                        : launch_cfg<1, true, false, 2, 32, true, 4>(1, tiles, layers, 4, s, tmW, tmX, ra, n, KB, di.status);
         if (items <= 64 * (int64_t)E)
-            return launch_cfg<1, true, false, 3, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
-        return launch_cfg<2, true, false, 2, 32, true>(1, tiles, layers, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
+            return deep ? launch_cfg<1, true, false, 3, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status)
+                        : launch_cfg<1, true, false, 2, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status);
+        return launch_cfg<2, true, false, 2, 32, true>(1, tiles, layers, 16, s, tmW, tmX, ra, n, KB, di.status);
     }
     if (items <= 64 * (int64_t)E)
         return launch_cfg<1, true, false, 3, 32>(1, tiles, layers, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
