@@ -584,14 +584,16 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     // layers past the routing's tile count leave at once
     const int layers = (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
     if (rs) {
-        // chunks of 4 token slots while experts get 4 items or fewer on average; a
-        // third ring slot while the CTAs of the experts with items fit on the SMs at once
+        // chunks of 4, 8 or 16 token slots for up to 4, 8 or more items per expert
+        // on average (every chunk streams the weights once); a third ring slot while
+        // the CTAs of the experts with items fit on the SMs at once
         const bool deep = rs_ctas <= di.sm_count;
         const int n = (int)N;
-        if (items <= 4 * (int64_t)E)
+        const int64_t per_expert = (items + (items < E ? items : E) - 1) / (items < E ? items : E);
+        if (per_expert <= 4)
             return deep ? launch_cfg<1, true, false, 3, 32, true, 4>(1, tiles, layers, 4, s, tmW, tmX, ra, n, KB, di.status)
                         : launch_cfg<1, true, false, 2, 32, true, 4>(1, tiles, layers, 4, s, tmW, tmX, ra, n, KB, di.status);
-        if (items <= 64 * (int64_t)E)
+        if (per_expert <= 8)
             return deep ? launch_cfg<1, true, false, 3, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status)
                         : launch_cfg<1, true, false, 2, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status);
         return launch_cfg<2, true, false, 2, 32, true>(1, tiles, layers, 16, s, tmW, tmX, ra, n, KB, di.status);
