@@ -352,14 +352,16 @@ static q4k_status moe_common(const void *w_experts, int32_t n_experts, int64_t N
     const bool per_slot = y_mode == Q4K_MOE_Y_PER_SLOT;
     float *slot_out = per_slot ? y : reinterpret_cast<float *>(p);
     cudaError_t e = cudaSuccess;
-    if (route) e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, true, tiles, n_tiles, s);
+    // with very few items the expert kernel reads the ids directly: nothing to sort
+    if (route && (tc || !moe_direct(T * topk)))
+        e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, true, tiles, n_tiles, s);
     if (e == cudaSuccess && tc)
         e = launch_moe_gather(di, x, x_mode, topk, perm, offsets, n_experts, T * topk, K, x_sorted,
                               per_slot ? y : nullptr, N, s);
     if (e == cudaSuccess)
         e = tc ? launch_moe_tcp(di, w_experts, n_experts, N, K, x_sorted, T * topk, perm, tiles, n_tiles, slot_out, s)
-               : launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, tiles, n_tiles, T, topk,
-                                   slot_out, per_slot, s);
+               : launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, tiles, n_tiles, topk_ids,
+                                   T, topk, slot_out, per_slot, s);
     if (e == cudaSuccess && !per_slot) e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }

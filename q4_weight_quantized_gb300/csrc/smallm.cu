@@ -211,7 +211,15 @@ struct RowArgs {
     int n_items;             // MoE: T * topk
     int zero_invalid;        // MoE: zero the per-slot rows of the invalid items
     int early_w;          // dense: copy the first weight blocks before waiting on the previous kernel
+    // MoE with very few items: grid layer z is item z itself (no routing); its
+    // expert is ids[z], and an id outside [0, E) zeroes the item's per-slot row
+    int direct;
+    const int32_t *ids;
+    int E;
 };
+
+// The (token, k-slot) item at position p of the expert-sorted order (MoE).
+__device__ __forceinline__ int item_at(const RowArgs &ra, int p) { return ra.direct ? p : __ldg(ra.perm + p); }
 
 // Activation row and output offset of token slot n (-1 if the slot is empty).
 template <bool MOE>
@@ -220,7 +228,7 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
     yoff = -1;
     if (n < cnt) {
         if constexpr (MOE) {
-            const int item = __ldg(ra.perm + off0 + n);
+            const int item = item_at(ra, off0 + n);
             xrow = ra.x_per_slot ? item : item / ra.topk;
             yoff = (long long)item * ra.ldy;
         } else {
@@ -263,7 +271,20 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
 
     if constexpr (MOE) pdl_wait();  // the routing comes from the previous kernel
     int off0 = 0, cnt = ra.M, tma_row = wrow0;
-    if constexpr (MOE) {
+    if constexpr (MOE) if (ra.direct) {
+        // grid layer z = item z
+        const int item = blockIdx.z, e = __ldg(ra.ids + item);
+        if (e < 0 || e >= ra.E) {  // invalid id: zero this CTA's part of the row, leave before any barrier
+            if (ra.zero_invalid)
+                for (int col = threadIdx.x; col < kRows * (RS ? kWarps : 1); col += kThreads)
+                    if (row0 + col < N) ra.y[(long long)item * ra.ldy + row0 + col] = 0.0f;
+            return;
+        }
+        off0 = item;
+        cnt = 1;
+        tma_row = e * N + wrow0;
+    }
+    if constexpr (MOE) if (!ra.direct) {
         // grid layer z = token tile z of the routing (only tiles of experts that have items);
         // the layer right after the last tile zeroes the invalid items' rows of this row tile
         const int n_tl = __ldg(ra.n_tiles);
@@ -386,7 +407,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             __syncwarp();
             if (!aborted && wrow0 + lane < N)
                 for (int tk = 0; tk < nvalid; ++tk)
-                    ra.y[(long long)__ldg(ra.perm + off0 + ch * kPerChunk + tk) * ra.ldy + wrow0 + lane] =
+                    ra.y[(long long)item_at(ra, off0 + ch * kPerChunk + tk) * ra.ldy + wrow0 + lane] =
                         mine[tk * kRows + lane];
             __syncwarp();  // the slice is reused by the next chunk
         } else if constexpr (MOE) {
@@ -558,8 +579,8 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
 
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
-                              const int4 *tok_tiles, const int *n_tiles, int64_t T, int topk, float *out,
-                              bool zero_invalid, cudaStream_t s) {
+                              const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
+                              float *out, bool zero_invalid, cudaStream_t s) {
     CUtensorMap tmW, tmX;
     // all experts stacked: E*N rows of the same pitch
     constexpr int kRows = 32;
@@ -580,9 +601,11 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     ra.x_per_slot = x_per_slot; ra.topk = topk; ra.perm = perm; ra.tiles = tok_tiles; ra.n_tiles = n_tiles;
     const int64_t items = T * topk;
     ra.n_valid = offsets + E; ra.n_items = (int)items; ra.zero_invalid = zero_invalid ? 1 : 0;
-    // one grid layer per possible token tile (+1 to zero the invalid items' rows);
-    // layers past the routing's tile count leave at once
-    const int layers = (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
+    ra.direct = moe_direct(items) ? 1 : 0; ra.ids = ids; ra.E = E;
+    // one grid layer per item (direct), or per possible token tile (+1 to zero the
+    // invalid items' rows); layers past the routing's tile count leave at once
+    const int layers = ra.direct ? (int)items : (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
+    const int nx1 = ra.direct ? 1 : 0;  // a direct layer has one token: one activation row per slot
     if (rs) {
         // chunks of 4, 8 or 16 token slots for up to 4, 8 or more items per expert
         // on average (every chunk streams the weights once); a third ring slot while
@@ -590,16 +613,18 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
         const bool deep = rs_ctas <= di.sm_count;
         const int n = (int)N;
         const int64_t per_expert = (items + (items < E ? items : E) - 1) / (items < E ? items : E);
-        if (per_expert <= 4)
-            return deep ? launch_cfg<1, true, false, 3, 32, true, 4>(1, tiles, layers, 4, s, tmW, tmX, ra, n, KB, di.status)
-                        : launch_cfg<1, true, false, 2, 32, true, 4>(1, tiles, layers, 4, s, tmW, tmX, ra, n, KB, di.status);
+        if (per_expert <= 4 || ra.direct) {
+            const int nx = nx1 ? 1 : 4;
+            return deep ? launch_cfg<1, true, false, 3, 32, true, 4>(1, tiles, layers, nx, s, tmW, tmX, ra, n, KB, di.status)
+                        : launch_cfg<1, true, false, 2, 32, true, 4>(1, tiles, layers, nx, s, tmW, tmX, ra, n, KB, di.status);
+        }
         if (per_expert <= 8)
             return deep ? launch_cfg<1, true, false, 3, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status)
                         : launch_cfg<1, true, false, 2, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status);
         return launch_cfg<2, true, false, 2, 32, true>(1, tiles, layers, 16, s, tmW, tmX, ra, n, KB, di.status);
     }
     if (items <= 64 * (int64_t)E)
-        return launch_cfg<1, true, false, 3, 32>(1, tiles, layers, 8, s, tmW, tmX, ra, (int)N, KB, di.status);
+        return launch_cfg<1, true, false, 3, 32>(1, tiles, layers, nx1 ? 1 : 8, s, tmW, tmX, ra, (int)N, KB, di.status);
     return launch_cfg<2, true, false, 2, 32>(1, tiles, layers, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
 }
 

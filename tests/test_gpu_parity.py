@@ -354,7 +354,7 @@ def moe_down():
     return G.moe_experts(4, 5, N, K)
 
 
-@pytest.mark.parametrize("T", [1, 16])
+@pytest.mark.parametrize("T", [1, 2, 3, 16])
 def test_moe_gate_up_per_slot(ref, syn, moe_up, T):
     N, K = G.MOE_UP
     ids, gates = syn.routing(syn.seed(4, 2) + T, syn.seed(4, 3) + T, T, G.MOE_E, G.MOE_TOPK)
@@ -364,7 +364,7 @@ def test_moe_gate_up_per_slot(ref, syn, moe_up, T):
     assert G.rel_err(y, want) <= TOL_SMALL
 
 
-@pytest.mark.parametrize("T", [1, 16])
+@pytest.mark.parametrize("T", [1, 2, 3, 16])
 def test_moe_down_combine(ref, syn, moe_down, T):
     N, K = G.MOE_DOWN
     ids, gates = syn.routing(syn.seed(4, 2) + T, syn.seed(4, 3) + T, T, G.MOE_E, G.MOE_TOPK)
@@ -467,6 +467,25 @@ def test_moe_reuse_routing_same_bits(syn, moe_up, moe_down, T):
     for y in shared[:2]:
         h = G.host(y)
         assert np.all(h[0, 3] == 0) and np.all(h[T - 1, 0] == 0)
+
+
+
+@pytest.mark.parametrize("K", [768, 2048])
+def test_moe_few_items_direct(ref, syn, K):
+    # up to 16 items: every item is its own grid layer, its expert read from the ids
+    # (no routing); ragged N, invalid ids give zero rows and no combine contribution
+    E, N, T, topk = 12, 200, 2, 8
+    w = np.concatenate([G.weights(4, 80 + e, N, K) for e in range(E)])
+    ids, gates = syn.routing(91, 92, T, E, topk)
+    ids[0, 2] = -4
+    ids[1, 7] = E
+    x = G.activations(4, 13, T, K)
+    y = run_moe(w, E, N, K, x, q4k.Q4K_MOE_X_PER_TOKEN, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT)
+    assert np.all(y[0, 2] == 0) and np.all(y[1, 7] == 0)
+    assert G.rel_err(y, ref.moe_slots(w, E, N, K, x, False, ids)) <= TOL_SMALL
+    xs = G.activations(4, 14, T * topk, K)
+    yc = run_moe(w, E, N, K, xs, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_COMBINE)
+    assert G.rel_err(yc, ref.moe(w, E, N, K, xs, True, ids, gates)) <= TOL_SMALL
 
 
 def test_moe_determinism(syn, moe_up):
