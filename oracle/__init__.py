@@ -72,6 +72,10 @@ def _load():
             lib.q4k_ref_moe_slots.restype = ctypes.c_int
             lib.q4k_ref_moe_combine.argtypes = [P, P, i64, i32, i64, P]
             lib.q4k_ref_moe_combine.restype = None
+            lib.q4k_ref_f64_to_bf16.argtypes = [ctypes.c_double]
+            lib.q4k_ref_f64_to_bf16.restype = ctypes.c_uint16
+            lib.q4k_ref_moe_ffn.argtypes = [P, P, P, i32, i64, i64, P, P, P, i64, i32, P, ctypes.c_int]
+            lib.q4k_ref_moe_ffn.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -181,3 +185,22 @@ def moe(w_experts, E, N, K, x_bf16, x_per_slot, ids, gates=None, threads: int = 
     """Per-slot outputs, or (with gates) their weighted combine [T, N]."""
     out = moe_slots(w_experts, E, N, K, x_bf16, x_per_slot, ids, threads)
     return out if gates is None else moe_combine(out, gates)
+
+
+def f64_to_bf16(v: float) -> int:
+    """The bf16 nearest to a double (ties to even), rounded once; its bits."""
+    return int(_load().q4k_ref_f64_to_bf16(float(v)))
+
+
+def moe_ffn(w_gate, w_up, w_down, E: int, H: int, D: int, x_bf16, ids, gates, threads: int = 1) -> np.ndarray:
+    """Routed SwiGLU expert layer y [T, D] fp64 (q4k_ref_moe_ffn)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, topk = ids.shape
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    gates = np.ascontiguousarray(gates, dtype=np.float32)
+    y = np.empty((T, D), dtype=np.float64)
+    rc = _load().q4k_ref_moe_ffn(_p(_blocks(w_gate)), _p(_blocks(w_up)), _p(_blocks(w_down)), E, H, D, _p(x),
+                                 _p(ids), _p(gates), T, topk, _p(y), threads)
+    if rc != 0:
+        raise ValueError("bad shape")
+    return y

@@ -266,3 +266,33 @@ void q4k_ref_moe_combine(const double *out, const float *gates, int64_t T, int32
             y[t * N + n] = acc;
         }
 }
+
+uint16_t q4k_ref_f64_to_bf16(double v) {
+    if (v == 0.0) return signbit(v) ? 0x8000u : 0u;
+    int e;
+    const double m = frexp(v, &e);             /* v = m * 2^e, 0.5 <= |m| < 1 */
+    const double r = nearbyint(ldexp(m, 8));   /* 8 significant bits, ties to even */
+    const float f = (float)ldexp(r, e - 8);    /* exact in fp32 (and in bf16) */
+    return q4k_ref_f32_to_bf16(f);
+}
+
+int q4k_ref_moe_ffn(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, int32_t E, int64_t H,
+                    int64_t D, const uint16_t *x, const int32_t *ids, const float *gates, int64_t T, int32_t topk,
+                    double *y, int threads) {
+    if (!shape_ok(H, D) || !shape_ok(D, H) || T < 0 || topk < 1 || E < 1) return -1;
+    const int64_t items = T * topk;
+    double *g = (double *)malloc(sizeof(double) * (size_t)(items * H > 0 ? items * H : 1));
+    double *u = (double *)malloc(sizeof(double) * (size_t)(items * H > 0 ? items * H : 1));
+    uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(items * H > 0 ? items * H : 1));
+    double *out = (double *)malloc(sizeof(double) * (size_t)(items * D > 0 ? items * D : 1));
+    int rc = (g && u && h && out) ? 0 : -2;
+    if (rc == 0) rc = q4k_ref_moe_slots(w_gate, E, H, D, x, 0, ids, T, topk, g, threads);
+    if (rc == 0) rc = q4k_ref_moe_slots(w_up, E, H, D, x, 0, ids, T, topk, u, threads);
+    if (rc == 0) {
+        for (int64_t i = 0; i < items * H; ++i) h[i] = q4k_ref_f64_to_bf16(g[i] / (1.0 + exp(-g[i])) * u[i]);
+        rc = q4k_ref_moe_slots(w_down, E, D, H, h, 1, ids, T, topk, out, threads);
+    }
+    if (rc == 0) q4k_ref_moe_combine(out, gates, T, topk, D, y);
+    free(g); free(u); free(h); free(out);
+    return rc;
+}

@@ -79,6 +79,25 @@ int q4k_ref_moe_slots(const uint8_t *w_experts, int32_t E, int64_t N, int64_t K,
 /* y[T][N] = sum_{j=0..topk-1} gates[t][j] * out[t][j][:], in j order, fp64 */
 void q4k_ref_moe_combine(const double *out, const float *gates, int64_t T, int32_t topk, int64_t N, double *y);
 
+/* Round a double to the nearest bf16 (ties to even), once; returns its bits.
+ * Finite normal range only (|v| from 2^-126 to the bf16 maximum, or 0). */
+uint16_t q4k_ref_f64_to_bf16(double v);
+
+/* Routed SwiGLU expert layer: the projections on either side of the routed
+ * grouped GEMM and its combine (sparkinfer-server README, "Determinism": the
+ * routed MoE down projection and its combine).  The activation between the
+ * projections is not on the pages; the reading taken is SwiGLU.  For every item
+ * (t, j) whose expert e = ids[t][j] is in [0, E):
+ *     g = x[t] . W_gate[e]^T,  u = x[t] . W_up[e]^T        (H values each, fp64)
+ *     h = bf16( g / (1 + exp(-g)) * u )                   (rounded once, ties to even)
+ *     out[t][j] = h . W_down[e]^T                          (D values, fp64)
+ * and y[T][D] = sum_j gates[t][j] * out[t][j] in j order (items with an invalid
+ * id have out = 0).  w_gate, w_up are [E][H][D/256] blocks, w_down [E][D][H/256];
+ * x is [T][D] bf16.  Returns 0, or -1 on a bad shape. */
+int q4k_ref_moe_ffn(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, int32_t E, int64_t H,
+                    int64_t D, const uint16_t *x, const int32_t *ids, const float *gates, int64_t T, int32_t topk,
+                    double *y, int threads);
+
 #ifdef __cplusplus
 }
 #endif

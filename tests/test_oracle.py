@@ -7,7 +7,9 @@
   - reference-quantizer round trip bounded by each sub-block's step d*sc;
   - GEMM vs exact rational arithmetic (fractions) and vs numpy matmul;
   - one-hot and all-ones activations (closed forms);
-  - MoE routing vs Python's stable sort, slots and combine vs numpy.
+  - MoE routing vs Python's stable sort, slots and combine vs numpy;
+  - the routed SwiGLU layer vs its pinned pieces, scipy's logistic function and an
+    exact-rational bf16 rounding.
 """
 from fractions import Fraction
 
@@ -270,6 +272,67 @@ def test_moe_combine(ref, syn):
     onehot[np.arange(T), [0, 3, 7, 5]] = 1.0
     y1 = ref.moe_combine(out, onehot)
     assert np.array_equal(y1, out[np.arange(T), [0, 3, 7, 5]])
+
+
+
+def exact_bf16(v: float) -> int:
+    """The bf16 nearest to v (ties to even), in exact rational arithmetic; its bits."""
+    if v == 0.0:
+        return 0x8000 if np.signbit(v) else 0
+    q = Fraction(v)
+    sign = 0x8000 if q < 0 else 0
+    q = abs(q)
+    e = 0
+    while q >= 2:
+        q /= 2
+        e += 1
+    while q < 1:
+        q *= 2
+        e -= 1
+    m = q * 128                                        # 128 <= m < 256: 8 significant bits
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    r = fl + (1 if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1) else 0)
+    if r == 256:
+        r, e = 128, e + 1
+    return sign | ((e + 127) << 7) | (r - 128)
+
+
+def test_f64_to_bf16_exact(ref):
+    rng = np.random.default_rng(31)
+    vals = list(rng.standard_normal(3000) * np.exp(rng.uniform(-30, 30, 3000)))
+    for b in range(0x3F80, 0x3F90):                    # exact ties between neighbours near 1
+        lo = bf16_bits_to_f64(np.array([b], np.uint16))[0]
+        hi = bf16_bits_to_f64(np.array([b + 1], np.uint16))[0]
+        vals += [(lo + hi) / 2, -(lo + hi) / 2, np.nextafter((lo + hi) / 2, 0.0), np.nextafter((lo + hi) / 2, 9.0)]
+    vals += [0.0, -0.0, 1.0, 3.0e38, 1.0e-37]
+    for v in vals:
+        assert ref.f64_to_bf16(v) == exact_bf16(float(v)), v
+    # on values exactly representable in fp32 it agrees with the pinned fp32 rounding
+    f = rng.standard_normal(500).astype(np.float32)
+    assert all(ref.f64_to_bf16(float(a)) == ref.f32_to_bf16(float(a)) for a in f)
+
+
+def test_moe_ffn_vs_pinned_pieces(ref, syn):
+    # the layer = gate and up slots (pinned above), SwiGLU with scipy's logistic
+    # function, bf16 rounding (exact rationals), down slots on h, ordered combine
+    from scipy.special import expit
+    E, H, D, T, topk = 5, 256, 512, 4, 3
+    wg = np.concatenate([syn.weights(100 + e, H, D) for e in range(E)])
+    wu = np.concatenate([syn.weights(110 + e, H, D) for e in range(E)])
+    wd = np.concatenate([syn.weights(120 + e, D, H) for e in range(E)])
+    ids, gates = syn.routing(130, 131, T, E, topk)
+    ids[2, 1] = -1                                     # an invalid id adds nothing
+    x = syn.normal_bf16(132, T * D).reshape(T, D)
+    y = ref.moe_ffn(wg, wu, wd, E, H, D, x, ids, gates)
+    g = ref.moe_slots(wg, E, H, D, x, False, ids)
+    u = ref.moe_slots(wu, E, H, D, x, False, ids)
+    hv = g * expit(g) * u
+    h = np.array([exact_bf16(float(v)) for v in hv.reshape(-1)], dtype=np.uint16).reshape(T * topk, H)
+    out = ref.moe_slots(wd, E, D, H, h, True, ids)
+    want = ref.moe_combine(out, gates)
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+    assert np.any(h != 0) and np.abs(y).max() > 0
 
 
 # ------------------------------------------------------------ input module

@@ -32,6 +32,10 @@ MUTANTS = {
     "route_histogram_offset": ("offsets[ids[i] + 1] += 1;", "offsets[ids[i]] += 1;"),
     "f16_subnormal_scale": ("v = ldexpf((float)f, -24);", "v = ldexpf((float)f, -25);"),
     "bf16_ties_away": ("(lower == 0x8000 && (upper & 1))", "(lower == 0x8000)"),
+    "f64_bf16_seven_bits": ("nearbyint(ldexp(m, 8))", "nearbyint(ldexp(m, 7))"),
+    "ffn_no_silu": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "g[i] * u[i]"),
+    "ffn_down_reads_token_rows": ("rc = q4k_ref_moe_slots(w_down, E, D, H, h, 1, ids, T, topk, out, threads);",
+                                  "rc = q4k_ref_moe_slots(w_down, E, D, H, h, 0, ids, T, topk, out, threads);"),
 }
 
 
