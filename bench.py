@@ -10,7 +10,9 @@ Other workloads (for measurement, not the headline line): `verify` (M-token
 speculative-verify GEMM, K 5120 -> N 17408, --m, default 4), `prefill` (M x K
 5120 -> N 17408 then M x K 17408 -> N 5120, --m, default 4096, TFLOP/s) and
 `moe` (128 experts, top-8: gate, up and down with the weighted combine, --m
-tokens, default 2048).
+tokens, default 2048) and `moe_ffn` (the same layer as one routed SwiGLU expert
+feed-forward call: gate, up with the SwiGLU epilogue, down on the bf16 h rows,
+weighted combine).
 
 Timing: W warm-up steps, then exactly K steps between a barrier plus
 cudaDeviceSynchronize on both sides, timed with CUDA events on the launching
@@ -180,17 +182,20 @@ class Workload:
                                                                          10.0, synth.seed(3, 9)),
                           synth.normal_bf16(synth.seed(3, 6), m * 17408).reshape(m, 17408))]
             self.unit, self.config = "TFLOP/s", {"workload": f"prefill GEMM M={m}: K5120->N17408 then K17408->N5120"}
-        elif name == "moe":
+        elif name in ("moe", "moe_ffn"):
             E, topk = 128, 8
             ids, gates = synth.routing(synth.seed(4, 2) + m, synth.seed(4, 3) + m, m, E, topk)
             mk = lambda s, N, K: np.concatenate(  # noqa: E731
                 [synth.weights(synth.seed(4, s) + 1000 * (e + 1), N, K) for e in range(E)])
-            self.moe = dict(E=E, topk=topk, T=m, ids=ids, gates=gates,
+            self.moe = dict(E=E, topk=topk, T=m, ids=ids, gates=gates, ffn=name == "moe_ffn",
                             gate=mk(0, 768, 2048), up=mk(7, 768, 2048), down=mk(5, 2048, 768),
                             x=synth.normal_bf16(synth.seed(4, 1), m * 2048).reshape(m, 2048),
                             xd=synth.normal_bf16(synth.seed(4, 6), m * topk * 768).reshape(m * topk, 768))
             self.unit, self.config = "GB/s", {"workload": f"MoE 128 experts top-8 T={m}: gate+up K2048->N768 "
                                                           "per slot, down K768->N2048 with weighted combine"}
+            if name == "moe_ffn":
+                self.config = {"workload": f"routed SwiGLU expert FFN, 128 experts top-8 T={m}: gate+up "
+                                           "K2048->H768, SwiGLU to bf16, down K768->D2048, weighted combine"}
         else:
             raise SystemExit(f"unknown workload {name}")
 
@@ -243,7 +248,8 @@ class GpuRunner:
             self.y_up = torch.empty((T, topk, 768), dtype=torch.float32, device=device)
             self.y_down = torch.empty((T, 2048), dtype=torch.float32, device=device)
             wsb = max(q4k.q4k_moe_workspace_size(mo["E"], 768, 2048, T, topk, 0),
-                      q4k.q4k_moe_workspace_size(mo["E"], 2048, 768, T, topk, 1))
+                      q4k.q4k_moe_workspace_size(mo["E"], 2048, 768, T, topk, 1),
+                      q4k.q4k_moe_ffn_workspace_size(mo["E"], 768, 2048, T, topk))
             self.moe_ws = torch.empty(wsb, dtype=torch.uint8, device=device)
             self.moe_wsb = wsb
         else:
@@ -259,10 +265,15 @@ class GpuRunner:
     def launches_per_step(self) -> int:
         if self.wl.moe:
             mo = self.wl.moe
-            # one routing; per grouped GEMM the expert GEMM (+ the activation gather
-            # on the tensor-core path, from 32 items per expert); + the combine
-            tc = mo["T"] * mo["topk"] >= 32 * mo["E"]
-            return 1 + 3 * (2 if tc else 1) + 1
+            # one routing (none for up to 16 items); per grouped GEMM the expert GEMM
+            # (+ the activation gather on the tensor-core path, from 32 items per
+            # expert; the FFN call gathers once); + the combine
+            items = mo["T"] * mo["topk"]
+            tc = items >= 32 * mo["E"]
+            route = 1 if (tc or items > 16) else 0
+            if mo["ffn"]:
+                return route + (1 if tc else 0) + 3 + 1
+            return route + 3 * (2 if tc else 1) + 1
         return len(self.wl.mats)  # one kernel per matrix
 
     def step_one(self, r: int, i: int):
@@ -284,6 +295,12 @@ class GpuRunner:
             E, T, topk = mo["E"], mo["T"], mo["topk"]
             if mark:
                 mark(0)
+            if mo["ffn"]:
+                q4k.q4k_moe_ffn(s["gate"], s["up"], s["down"], E, 768, 2048, self.xg, self.ids, self.gates, T, topk,
+                                self.y_down, self.moe_ws, self.moe_wsb)
+                if mark:
+                    mark(1)
+                return
             # the layer's three projections share one routing: the first call sorts
             # the items, the other two reuse the sort left in the workspace
             q4k.q4k_moe_grouped_gemm(s["gate"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk, self.y_gate,
@@ -561,13 +578,13 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "verify", "prefill", "moe"], default="decode")
+    ap.add_argument("--workload", choices=["decode", "verify", "prefill", "moe", "moe_ffn"], default="decode")
     ap.add_argument("--m", type=int, default=None, help="tokens (verify: 4, prefill: 4096, moe: 2048)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.m is None:
-        args.m = {"decode": 1, "verify": 4, "prefill": 4096, "moe": 2048}[args.workload]
+        args.m = {"decode": 1, "verify": 4, "prefill": 4096, "moe": 2048, "moe_ffn": 2048}[args.workload]
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, local_rank, world = env_rank()

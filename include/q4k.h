@@ -224,6 +224,40 @@ q4k_status q4k_moe_grouped_gemm_reuse_routing(const void *w_experts, int32_t n_e
                                               const float *gates, int64_t T, int32_t topk, float *y, int y_mode,
                                               void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------- routed expert FFN layer --
+ * One routed SwiGLU feed-forward layer of the pages' MoE models (sparkinfer-server
+ * README, "Determinism": discrete top-k expert routing and the routed MoE
+ * down-projection combine).  For every token t and slot j with a valid expert
+ * e = topk_ids[t][j]:
+ *   g = x[t] . Wg_e^T,  u = x[t] . Wu_e^T                     (fp32, H values)
+ *   h = bf16(silu(g) * u), silu(g) = g / (1 + e^-g)           (rounded to nearest even)
+ *   o = h . Wd_e^T                                            (fp32, D values)
+ *   y[t] = sum_{j=0..topk-1} gates[t][j] * o[t][j], summed in increasing j.
+ * Slots whose id is outside [0,E) contribute nothing (a token whose ids are all
+ * invalid gets a zero row).  The routing is computed once for the three
+ * projections; the up projection's epilogue applies SwiGLU to the gate
+ * projection's output and stores h in bf16, so u is never written out.
+ *   w_gate, w_up  device, E*H*q4k_row_bytes(D) bytes each: expert e's H x D matrix
+ *                 starts at byte e*H*q4k_row_bytes(D); 16-byte aligned
+ *   w_down        device, E*D*q4k_row_bytes(H) bytes: expert e's D x H matrix at
+ *                 byte e*D*q4k_row_bytes(H); 16-byte aligned
+ *   x             device bf16 [T][D], dense, 16-byte aligned
+ *   topk_ids      device int32 [T][topk];  gates  device fp32 [T][topk]
+ *   y             device fp32 [T][D], dense, 16-byte aligned
+ *   ws            device scratch, >= q4k_moe_ffn_workspace_size(...) bytes,
+ *                 256-byte aligned, contents need not be initialized: the
+ *                 routing, g (4*T*topk*H bytes), h (2*T*topk*H), the per-slot
+ *                 outputs o (4*T*topk*D) and, from 32*E items on, the
+ *                 expert-sorted copy of x (2*T*topk*D)
+ * Errors: NULL, SHAPE (E < 1 or E > 1024, topk < 1 or topk > E, T < 1,
+ * T*topk >= 2^31, H or D not a positive multiple of 256, E*H or E*D >= 2^31),
+ * ALIGN, WORKSPACE, DEVICE, CUDA.  q4k_moe_ffn_workspace_size returns 0 for
+ * arguments that would give SHAPE. */
+size_t q4k_moe_ffn_workspace_size(int32_t n_experts, int64_t H, int64_t D, int64_t T, int32_t topk);
+q4k_status q4k_moe_ffn(const void *w_gate, const void *w_up, const void *w_down, int32_t n_experts, int64_t H,
+                       int64_t D, const uint16_t *x, const int32_t *topk_ids, const float *gates, int64_t T,
+                       int32_t topk, float *y, void *ws, size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------- allocation-free MoE --
  * No counterpart on the pages: an addition for callers that cannot provide a
  * workspace - code that must not call cudaMalloc/cudaFree (they synchronize the

@@ -27,7 +27,7 @@ EXPORTS = (
     "q4k_status_string", "q4k_last_cuda_error", "q4k_row_bytes", "q4k_version", "q4k_check_device",
     "q4k_set_static_weights", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
     "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_reuse_routing",
-    "q4k_moe_grouped_gemm_noalloc",
+    "q4k_moe_grouped_gemm_noalloc", "q4k_moe_ffn_workspace_size", "q4k_moe_ffn",
 )
 
 # fixed scratch capacity of q4k_moe_grouped_gemm_noalloc (Q4K_MOE_NOALLOC_SCRATCH_BYTES)
@@ -71,6 +71,8 @@ def load(path: str | None = None):
         "q4k_moe_grouped_gemm": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P, sz, P], st),
         "q4k_moe_grouped_gemm_reuse_routing": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P, sz, P], st),
         "q4k_moe_grouped_gemm_noalloc": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P], st),
+        "q4k_moe_ffn_workspace_size": ([i32, i64, i64, i64, i32], sz),
+        "q4k_moe_ffn": ([P, P, P, i32, i64, i64, P, P, P, i64, i32, P, P, sz, P], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -190,3 +192,16 @@ def q4k_moe_grouped_gemm_noalloc(w_experts, n_experts: int, N: int, K: int, x, x
     _check(load().q4k_moe_grouped_gemm_noalloc(_ptr(w_experts), n_experts, N, K, _ptr(x), x_mode, _ptr(topk_ids),
                                                _ptr(gates), T, topk, _ptr(y), y_mode, _stream(stream)),
            "q4k_moe_grouped_gemm_noalloc")
+
+
+def q4k_moe_ffn_workspace_size(n_experts: int, H: int, D: int, T: int, topk: int) -> int:
+    return load().q4k_moe_ffn_workspace_size(n_experts, H, D, T, topk)
+
+
+def q4k_moe_ffn(w_gate, w_up, w_down, n_experts: int, H: int, D: int, x, topk_ids, gates, T: int, topk: int, y,
+                ws, ws_bytes: int, stream=None) -> None:
+    """One routed SwiGLU expert layer: y[t] = sum_j gates[t][j] * down_e(bf16(silu(gate_e(x[t])) * up_e(x[t]))),
+    e = topk_ids[t][j]; x bf16 [T][D], y fp32 [T][D]."""
+    _check(load().q4k_moe_ffn(_ptr(w_gate), _ptr(w_up), _ptr(w_down), n_experts, H, D, _ptr(x), _ptr(topk_ids),
+                              _ptr(gates), T, topk, _ptr(y), _ptr(ws), ws_bytes, _stream(stream)),
+           "q4k_moe_ffn")

@@ -381,4 +381,86 @@ q4k_status q4k_moe_grouped_gemm_reuse_routing(const void *w_experts, int32_t n_e
                       false);
 }
 
+// routing part of the workspace: [offsets E+1][perm T*topk][tile list][tile count]
+static size_t moe_routing_bytes(int32_t E, int64_t n_items) {
+    return align256((size_t)(E + 1) * 4) + align256((size_t)n_items * 4) +
+           align256((size_t)moe_max_tiles(E, n_items) * sizeof(int4)) + 256;
+}
+
+// FFN workspace: [routing][g fp32 T*topk*H][h bf16 T*topk*H][o fp32 T*topk*D]
+// [expert-sorted x bf16 T*topk*D (tensor-core path only)]
+size_t q4k_moe_ffn_workspace_size(int32_t n_experts, int64_t H, int64_t D, int64_t T, int32_t topk) {
+    if (!moe_shape_ok(n_experts, H, D, T, topk) || !moe_shape_ok(n_experts, D, H, T, topk)) return 0;
+    const size_t n = (size_t)(T * topk);
+    size_t b = moe_routing_bytes(n_experts, T * topk) + align256(n * (size_t)H * 4) + align256(n * (size_t)H * 2) +
+               align256(n * (size_t)D * 4);
+    if (moe_uses_tc(n_experts, T, topk)) b += align256(n * (size_t)D * 2);
+    return b;
+}
+
+q4k_status q4k_moe_ffn(const void *w_gate, const void *w_up, const void *w_down, int32_t n_experts, int64_t H,
+                       int64_t D, const uint16_t *x, const int32_t *topk_ids, const float *gates, int64_t T,
+                       int32_t topk, float *y, void *ws, size_t ws_bytes, void *stream) {
+    if (!w_gate || !w_up || !w_down || !x || !topk_ids || !gates || !y || !ws) return Q4K_ERR_NULL;
+    if (!moe_shape_ok(n_experts, H, D, T, topk) || !moe_shape_ok(n_experts, D, H, T, topk)) return Q4K_ERR_SHAPE;
+    if (!aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16) || !aligned(x, 16) || !aligned(y, 16) ||
+        !aligned(topk_ids, 4) || !aligned(gates, 4) || !aligned(ws, 256))
+        return Q4K_ERR_ALIGN;
+    if (ws_bytes < q4k_moe_ffn_workspace_size(n_experts, H, D, T, topk)) return Q4K_ERR_WORKSPACE;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t n = T * topk;
+    const int E = n_experts;
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    int32_t *offsets = reinterpret_cast<int32_t *>(p);
+    p += align256((size_t)(E + 1) * 4);
+    int32_t *perm = reinterpret_cast<int32_t *>(p);
+    p += align256((size_t)n * 4);
+    int4 *tiles = reinterpret_cast<int4 *>(p);
+    p += align256((size_t)moe_max_tiles(E, n) * sizeof(int4));
+    int *n_tiles = reinterpret_cast<int *>(p);
+    p += 256;
+    float *g = reinterpret_cast<float *>(p);
+    p += align256((size_t)n * (size_t)H * 4);
+    uint16_t *h = reinterpret_cast<uint16_t *>(p);
+    p += align256((size_t)n * (size_t)H * 2);
+    float *o = reinterpret_cast<float *>(p);
+    p += align256((size_t)n * (size_t)D * 4);
+    const bool tc = moe_uses_tc(E, T, topk);
+    cudaError_t e = cudaSuccess;
+    if (tc || !moe_direct(n)) e = launch_moe_route(topk_ids, n, E, offsets, perm, true, tiles, n_tiles, s);
+    if (tc) {
+        // gate and up read one expert-sorted copy of x; up stores h in that order too,
+        // which is the down projection's expert-sorted activation matrix
+        uint16_t *x_sorted = reinterpret_cast<uint16_t *>(p);
+        GluOut glu;
+        glu.g = g;
+        glu.h = h;
+        glu.h_sorted = 1;
+        if (e == cudaSuccess)
+            e = launch_moe_gather(di, x, 0, topk, perm, offsets, E, n, D, x_sorted, nullptr, H, s);
+        if (e == cudaSuccess) e = launch_moe_tcp(di, w_gate, E, H, D, x_sorted, n, perm, tiles, n_tiles, g, s);
+        if (e == cudaSuccess)
+            e = launch_moe_tcp(di, w_up, E, H, D, x_sorted, n, perm, tiles, n_tiles, nullptr, s, glu);
+        if (e == cudaSuccess) e = launch_moe_tcp(di, w_down, E, D, H, h, n, perm, tiles, n_tiles, o, s);
+    } else {
+        GluOut glu;
+        glu.g = g;
+        glu.h = h;
+        if (e == cudaSuccess)
+            e = launch_moe_smallm(di, w_gate, E, H, D, x, 0, perm, offsets, tiles, n_tiles, topk_ids, T, topk, g,
+                                  false, s);
+        if (e == cudaSuccess)
+            e = launch_moe_smallm(di, w_up, E, H, D, x, 0, perm, offsets, tiles, n_tiles, topk_ids, T, topk, nullptr,
+                                  false, s, glu);
+        if (e == cudaSuccess)
+            e = launch_moe_smallm(di, w_down, E, D, H, h, 1, perm, offsets, tiles, n_tiles, topk_ids, T, topk, o,
+                                  false, s);
+    }
+    if (e == cudaSuccess) e = launch_moe_combine(di, o, gates, topk_ids, E, T, topk, D, y, s);
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
 }  // extern "C"

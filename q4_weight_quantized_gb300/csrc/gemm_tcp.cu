@@ -60,6 +60,7 @@ struct Params {
     const int4 *tiles;     // MoE: (expert, first item, count, -)
     const int *n_tiles;    // number of token tiles
     unsigned int *status;
+    GluOut glu;            // SwiGLU epilogue (up projection of an expert FFN)
 };
 
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<__nv_bfloat162 *>(&u); }
@@ -305,20 +306,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
             for (int j = et; j < t.cnt; j += kEpWarps * 32) orw[j] = __ldg(p.perm + t.m0 + j);
             asm volatile("bar.sync 2, %0;" ::"n"(kEpWarps * 32) : "memory");
             const int n = t.n0 + 32 * q + lane;
+            if (!p.glu.h) {
 #pragma unroll 1
-            for (int cc = 0; cc < (t.cnt + 31) / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld32(tmem + (uint32_t)(buf * kBN) + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
-                tmem_ld_wait();
-                if (n < p.N) {
+                for (int cc = 0; cc < (t.cnt + 31) / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (uint32_t)(buf * kBN) + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
+                    tmem_ld_wait();
+                    if (n < p.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = 32 * cc + j;
-                        if (col < t.cnt) {
-                            const int64_t yrow = orw[col];
-                            p.y[yrow * p.ldy + n] = __uint_as_float(v[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = 32 * cc + j;
+                            if (col < t.cnt) p.y[(int64_t)orw[col] * p.ldy + n] = __uint_as_float(v[j]);
                         }
                     }
+                }
+            } else {
+                // SwiGLU epilogue: the 32 gate values of column group cc + 1 are
+                // loaded while group cc is converted and stored
+                const int nch = (t.cnt + 31) / 32;
+                float gv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    gv[j] = n < p.N && j < t.cnt ? __ldg(p.glu.g + (int64_t)orw[j] * p.ldy + n) : 0.0f;
+#pragma unroll 1
+                for (int cc = 0; cc < nch; ++cc) {
+                    float gn[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = 32 * (cc + 1) + j;
+                        gn[j] = n < p.N && col < t.cnt ? __ldg(p.glu.g + (int64_t)orw[col] * p.ldy + n) : 0.0f;
+                    }
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (uint32_t)(buf * kBN) + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
+                    tmem_ld_wait();
+                    if (n < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = 32 * cc + j;
+                            if (col < t.cnt) {
+                                const int64_t hrow = p.glu.h_sorted ? (int64_t)(t.m0 + col) : (int64_t)orw[col];
+                                p.glu.h[hrow * p.ldy + n] = swiglu_bf16(gv[j], __uint_as_float(v[j]));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) gv[j] = gn[j];
                 }
             }
             tc_fence_before();
@@ -345,7 +377,7 @@ cudaError_t launch(const CUtensorMap &tmW, const CUtensorMap &tmX, const Params 
 
 cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                            const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
-                           const int *n_tiles, float *out, cudaStream_t s) {
+                           const int *n_tiles, float *out, cudaStream_t s, const GluOut &glu) {
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kTileRows, kBlockBytes / 4);
     if (e != cudaSuccess) return e;
@@ -361,6 +393,7 @@ cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, i
     p.tiles = tiles;
     p.n_tiles = n_tiles;
     p.status = di.status;
+    p.glu = glu;
     return launch(tmW, tmX, p, di.sm_count, s);
 }
 

@@ -36,12 +36,24 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
 
+// SwiGLU epilogue of a routed expert's up projection: instead of its fp32
+// output u, the kernel stores h = swiglu_bf16(g, u), g being the gate
+// projection's fp32 output at the same row and column (rows of N, addressed
+// like the output).  h_sorted (tensor-core path only): h's row is the item's
+// position in the expert-sorted order rather than the item, so the down
+// projection reads h as its expert-sorted activations without a gather.
+struct GluOut {
+    const float *g = nullptr;
+    uint16_t *h = nullptr;  // null: plain fp32 output
+    int h_sorted = 0;
+};
+
 // MoE expert GEMM on the tensor cores: a persistent kernel (one CTA per SM,
 // double-buffered tensor-memory accumulators) walking the routing's token tiles
 // over the expert-sorted activation rows x_sorted (gemm_tcp.cu).
 cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                            const uint16_t *x_sorted, int64_t n_items, const int32_t *perm, const int4 *tiles,
-                           const int *n_tiles, float *out, cudaStream_t s);
+                           const int *n_tiles, float *out, cudaStream_t s, const GluOut &glu = GluOut());
 
 // MoE: all experts stacked as E*N rows; rows of x and of out are chosen through
 // the routing permutation (perm/offsets from launch_moe_route).
@@ -52,7 +64,7 @@ inline bool moe_direct(int64_t n_items) { return n_items <= 16; }
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
-                              float *out, bool zero_invalid, cudaStream_t s);
+                              float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu = GluOut());
 
 // Stable counting sort of items by expert (E <= 1024).  Items with an id
 // outside [0, E) are left out of offsets; with invalid_tail they follow the

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +22,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// SwiGLU of one element of a routed expert's feed-forward layer, rounded once
+// to bf16 (nearest, ties to even): silu(g) * u with silu(g) = g / (1 + e^-g),
+// in fp32.  The rounding is there because the down projection reads bf16.
+__device__ __forceinline__ uint16_t swiglu_bf16(float g, float u) {
+    const float h = g / (1.0f + expf(-g)) * u;
+    return __bfloat16_as_ushort(__float2bfloat16_rn(h));
 }
 
 // ------------------------------------------------------------------ mbarrier

@@ -216,10 +216,35 @@ struct RowArgs {
     int direct;
     const int32_t *ids;
     int E;
+    GluOut glu;  // MoE: SwiGLU epilogue (up projection of an expert FFN)
 };
 
 // The (token, k-slot) item at position p of the expert-sorted order (MoE).
 __device__ __forceinline__ int item_at(const RowArgs &ra, int p) { return ra.direct ? p : __ldg(ra.perm + p); }
+
+// Stores n <= NMAX MoE output elements, element i = (offset off(i) in the output
+// rows, value val(i)): fp32 y, or with GLU the SwiGLU epilogue's bf16 h.  For h,
+// every gate value is loaded before the first store, so the loads overlap.
+template <bool GLU, int NMAX, typename Off, typename Val>
+__device__ __forceinline__ void store_out(const RowArgs &ra, int n, Off &&off, Val &&val) {
+    if constexpr (GLU) {
+        long long o[NMAX];
+        float g[NMAX];
+#pragma unroll
+        for (int i = 0; i < NMAX; ++i) {
+            o[i] = i < n ? off(i) : -1;
+            g[i] = o[i] >= 0 ? __ldg(ra.glu.g + o[i]) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < NMAX; ++i)
+            if (o[i] >= 0) ra.glu.h[o[i]] = swiglu_bf16(g[i], val(i));
+    } else {
+        for (int i = 0; i < n; ++i) {
+            const long long oi = off(i);
+            if (oi >= 0) ra.y[oi] = val(i);
+        }
+    }
+}
 
 // Activation row and output offset of token slot n (-1 if the slot is empty).
 template <bool MOE>
@@ -244,8 +269,8 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // split rows instead of K - warp w owns rows w*ROWS.. of a 4*ROWS-row CTA over
 // all K blocks and stores its own outputs, with no cross-warp reduction.  CH:
 // token slots per chunk (at most 8 * NT; fewer shrinks the activation part of a
-// slot when experts get few items).
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT>
+// slot when experts get few items).  GLU (MoE): the SwiGLU epilogue (RowArgs::glu).
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
                                                           int KB, int nx, unsigned int *status) {
@@ -365,6 +390,21 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         bool live[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) live[nt] = nt * 8 + r < nvalid;
+        // SwiGLU epilogue with row split: lane l holds the item of the chunk's token
+        // slot l, and the gate values of this warp's rows are loaded now, so that
+        // they arrive while the weights stream
+        int my_item = -1;
+        float gpre[GLU && RS ? kPerChunk : 1];
+        if constexpr (MOE && RS && GLU) {
+            if (lane < nvalid) my_item = item_at(ra, off0 + ch * kPerChunk + lane);
+#pragma unroll
+            for (int tk = 0; tk < kPerChunk; ++tk) {
+                const int item = __shfl_sync(0xFFFFFFFFu, my_item, tk);
+                gpre[tk] = tk < nvalid && wrow0 + lane < N
+                               ? __ldg(ra.glu.g + (long long)item * ra.ldy + wrow0 + lane)
+                               : 0.0f;
+            }
+        }
 
         for (int j = 0; j < nblk && !aborted; ++j, ++it) {
             const int slot = it % SLOTS;
@@ -405,10 +445,19 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
                     mine[(tk + 1) * kRows + rA + 8] = acc[rt][nt][3];
                 }
             __syncwarp();
-            if (!aborted && wrow0 + lane < N)
-                for (int tk = 0; tk < nvalid; ++tk)
-                    ra.y[(long long)item_at(ra, off0 + ch * kPerChunk + tk) * ra.ldy + wrow0 + lane] =
-                        mine[tk * kRows + lane];
+            const bool store = !aborted && wrow0 + lane < N;
+            if constexpr (GLU) {
+#pragma unroll
+                for (int tk = 0; tk < kPerChunk; ++tk) {
+                    const long long o = (long long)__shfl_sync(0xFFFFFFFFu, my_item, tk) * ra.ldy + wrow0 + lane;
+                    if (store && tk < nvalid) ra.glu.h[o] = swiglu_bf16(gpre[tk], mine[tk * kRows + lane]);
+                }
+            } else {
+                if (store)
+                    for (int tk = 0; tk < nvalid; ++tk)
+                        ra.y[(long long)item_at(ra, off0 + ch * kPerChunk + tk) * ra.ldy + wrow0 + lane] =
+                            mine[tk * kRows + lane];
+            }
             __syncwarp();  // the slice is reused by the next chunk
         } else if constexpr (MOE) {
             // reduce this chunk across the warps (warp order) and store it
@@ -432,13 +481,22 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             }
             __syncthreads();
             if (!*(volatile int *)&abort_flag) {
-                for (int e2 = threadIdx.x; e2 < nvalid * kRows; e2 += kThreads) {
-                    float v = red_w[e2];
+                // thread i takes elements i, i + 128, ... of the chunk's [tokens][kRows]
+                constexpr int kPer = (16 * kRows + kThreads - 1) / kThreads;
+                const int mine_n = (nvalid * kRows - (int)threadIdx.x + kThreads - 1) / kThreads;
+                store_out<GLU, kPer>(
+                    ra, mine_n,
+                    [&](int i) {
+                        const int e2 = threadIdx.x + i * kThreads, tk = e2 / kRows, rr = e2 % kRows;
+                        return row0 + rr < N ? yoff_s[tk] + row0 + rr : -1LL;
+                    },
+                    [&](int i) {
+                        const int e2 = threadIdx.x + i * kThreads;
+                        float v = red_w[e2];
 #pragma unroll
-                    for (int w = 1; w < kWarps; ++w) v += red_w[w * 16 * kRows + e2];
-                    const int tk = e2 / kRows, rr = e2 % kRows;
-                    if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = v;
-                }
+                        for (int w = 1; w < kWarps; ++w) v += red_w[w * 16 * kRows + e2];
+                        return v;
+                    });
             }
             __syncthreads();  // red_w and the token table are reused by the next chunk
         }
@@ -493,11 +551,11 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     }
 }
 
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT>
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
     const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH>;
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmX, ra, N, KB, nx,
@@ -577,10 +635,50 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
     return launch_cfg<2, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
 }
 
+namespace {
+
+struct MoeShape {
+    bool rs, deep;
+    int64_t per_expert;
+    bool direct, few;
+    int tiles, layers, nx1;
+};
+
+// The MoE kernel variant for a call: row split or not, chunk size, ring depth.
+template <bool GLU>
+cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tmW, const CUtensorMap &tmX,
+                        const RowArgs &ra, int n, int KB, unsigned int *status) {
+    if (m.rs) {
+        // chunks of 4, 8 or 16 token slots for up to 4, 8 or more items per expert
+        // on average (every chunk streams the weights once); a third ring slot while
+        // the CTAs of the experts with items fit on the SMs at once
+        if (m.per_expert <= 4 || m.direct) {
+            const int nx = m.nx1 ? 1 : 4;
+            return m.deep ? launch_cfg<1, true, false, 3, 32, true, 4, GLU>(1, m.tiles, m.layers, nx, s, tmW, tmX, ra,
+                                                                             n, KB, status)
+                          : launch_cfg<1, true, false, 2, 32, true, 4, GLU>(1, m.tiles, m.layers, nx, s, tmW, tmX, ra,
+                                                                             n, KB, status);
+        }
+        if (m.per_expert <= 8)
+            return m.deep ? launch_cfg<1, true, false, 3, 32, true, 8, GLU>(1, m.tiles, m.layers, 8, s, tmW, tmX, ra, n,
+                                                                             KB, status)
+                          : launch_cfg<1, true, false, 2, 32, true, 8, GLU>(1, m.tiles, m.layers, 8, s, tmW, tmX, ra, n,
+                                                                             KB, status);
+        return launch_cfg<2, true, false, 2, 32, true, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB,
+                                                                 status);
+    }
+    if (m.few)
+        return launch_cfg<1, true, false, 3, 32, false, 8, GLU>(1, m.tiles, m.layers, m.nx1 ? 1 : 8, s, tmW, tmX, ra,
+                                                                 n, KB, status);
+    return launch_cfg<2, true, false, 2, 32, false, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB, status);
+}
+
+}  // namespace
+
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
-                              float *out, bool zero_invalid, cudaStream_t s) {
+                              float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu) {
     CUtensorMap tmW, tmX;
     // all experts stacked: E*N rows of the same pitch
     constexpr int kRows = 32;
@@ -602,30 +700,16 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     const int64_t items = T * topk;
     ra.n_valid = offsets + E; ra.n_items = (int)items; ra.zero_invalid = zero_invalid ? 1 : 0;
     ra.direct = moe_direct(items) ? 1 : 0; ra.ids = ids; ra.E = E;
+    ra.glu = glu;
     // one grid layer per item (direct), or per possible token tile (+1 to zero the
     // invalid items' rows); layers past the routing's tile count leave at once
     const int layers = ra.direct ? (int)items : (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
     const int nx1 = ra.direct ? 1 : 0;  // a direct layer has one token: one activation row per slot
-    if (rs) {
-        // chunks of 4, 8 or 16 token slots for up to 4, 8 or more items per expert
-        // on average (every chunk streams the weights once); a third ring slot while
-        // the CTAs of the experts with items fit on the SMs at once
-        const bool deep = rs_ctas <= di.sm_count;
-        const int n = (int)N;
-        const int64_t per_expert = (items + (items < E ? items : E) - 1) / (items < E ? items : E);
-        if (per_expert <= 4 || ra.direct) {
-            const int nx = nx1 ? 1 : 4;
-            return deep ? launch_cfg<1, true, false, 3, 32, true, 4>(1, tiles, layers, nx, s, tmW, tmX, ra, n, KB, di.status)
-                        : launch_cfg<1, true, false, 2, 32, true, 4>(1, tiles, layers, nx, s, tmW, tmX, ra, n, KB, di.status);
-        }
-        if (per_expert <= 8)
-            return deep ? launch_cfg<1, true, false, 3, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status)
-                        : launch_cfg<1, true, false, 2, 32, true>(1, tiles, layers, 8, s, tmW, tmX, ra, n, KB, di.status);
-        return launch_cfg<2, true, false, 2, 32, true>(1, tiles, layers, 16, s, tmW, tmX, ra, n, KB, di.status);
-    }
-    if (items <= 64 * (int64_t)E)
-        return launch_cfg<1, true, false, 3, 32>(1, tiles, layers, nx1 ? 1 : 8, s, tmW, tmX, ra, (int)N, KB, di.status);
-    return launch_cfg<2, true, false, 2, 32>(1, tiles, layers, 16, s, tmW, tmX, ra, (int)N, KB, di.status);
+    const bool deep = rs_ctas <= di.sm_count;
+    const int64_t per_expert = (items + (items < E ? items : E) - 1) / (items < E ? items : E);
+    const MoeShape ms = {rs, deep, per_expert, ra.direct != 0, items <= 64 * (int64_t)E, tiles, layers, nx1};
+    return glu.h ? moe_variant<true>(ms, s, tmW, tmX, ra, (int)N, KB, di.status)
+                 : moe_variant<false>(ms, s, tmW, tmX, ra, (int)N, KB, di.status);
 }
 
 }  // namespace q4k

@@ -69,3 +69,36 @@ def sample_rows(N: int, n: int = 96, seed: int = 0) -> np.ndarray:
 def moe_experts(cfg: int, stream: int, N: int, K: int, E: int = MOE_E) -> np.ndarray:
     """E stacked expert matrices [E*N, K/256*144] (expert e seeded by stream 16 + e)."""
     return np.concatenate([synth.weights(synth.seed(cfg, stream) + 1000 * (e + 1), N, K, 0.02) for e in range(E)])
+
+
+def _bf16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even), back as float64."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def tc_weights(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Model of the tensor-core kernels' bf16 weight operand, float64 [N, K].
+
+    Those kernels form each weight as one bf16 fused multiply-add of the code q
+    with the sub-block's scale and offset, both first rounded to bf16:
+    w = bf16(q * bf16(d*sc) - bf16(dmin*m)).  The field layout follows the Q4_K
+    block (fp16 d and dmin, twelve bytes of 6-bit scale/offset pairs, 128 bytes
+    of codes: sub-blocks 2g and 2g+1 are the low and high nibbles of bytes
+    32g..32g+31).  Used only to separate that rounding from other errors."""
+    nb = K // 256
+    b = np.ascontiguousarray(blocks).reshape(N, nb, 144)
+    d = b[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float32)
+    dmin = b[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float32)
+    s = b[..., 4:16].astype(np.int32)
+    sc = np.empty((N, nb, 8), np.int32)
+    mm = np.empty((N, nb, 8), np.int32)
+    sc[..., :4], mm[..., :4] = s[..., 0:4] & 63, s[..., 4:8] & 63
+    sc[..., 4:] = (s[..., 8:12] & 15) | ((s[..., 0:4] >> 6) << 4)
+    mm[..., 4:] = (s[..., 8:12] >> 4) | ((s[..., 4:8] >> 6) << 4)
+    codes = b[..., 16:].astype(np.int32).reshape(N, nb, 4, 32)
+    q = np.stack([codes & 15, codes >> 4], axis=3).reshape(N, nb, 8, 32)
+    dsc = _bf16(d[..., None] * sc.astype(np.float32))
+    dm = _bf16(dmin[..., None] * mm.astype(np.float32))
+    w = q * dsc[..., None] - dm[..., None]
+    return _bf16(w.astype(np.float32)).reshape(N, K)

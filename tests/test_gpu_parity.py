@@ -18,6 +18,10 @@ pytestmark = pytest.mark.gpu
 
 TOL_SMALL = 2e-3
 TOL_TC = 1e-2
+# the routed SwiGLU layer chains three tensor-core GEMMs: h carries the gate and up
+# projections' errors (each within TOL_TC of its own output) and the down
+# projection adds its own, so the layer's output is held to three times TOL_TC
+TOL_FFN_TC = 3 * TOL_TC
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -517,3 +521,110 @@ def test_moe_tensor_core_path(ref, syn, E, T, topk, N, K):
     assert np.array_equal(yc.view(np.uint32), yc2.view(np.uint32))
     want_c = ref.moe(w, E, N, K, xs, True, ids, gates, threads=16)
     assert G.rel_err(yc, want_c) <= TOL_TC
+
+
+# ------------------------------------------------------- routed expert FFN layer
+def run_ffn(wg, wu, wd, E, H, D, x, ids, gates, devs=None):
+    T, topk = ids.shape
+    if devs is None:
+        devs = (G.dev(wg), G.dev(wu), G.dev(wd))
+    ws_bytes = q4k.q4k_moe_ffn_workspace_size(E, H, D, T, topk)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    y = torch.full((T, D), float("nan"), dtype=torch.float32, device="cuda")
+    q4k.q4k_moe_ffn(*devs, E, H, D, G.dev(x), G.dev(ids), G.dev(gates), T, topk, y, ws, ws_bytes)
+    torch.cuda.synchronize()
+    return G.host(y)
+
+
+@pytest.fixture(scope="module")
+def ffn_layer():
+    # the 128-expert layer: gate and up K 2048 -> H 768, down K 768 -> D 2048
+    (H, D), (D2, H2) = G.MOE_UP, G.MOE_DOWN
+    assert (H, D) == (H2, D2)
+    wg = G.moe_experts(4, 40, H, D)
+    wu = G.moe_experts(4, 41, H, D)
+    wd = G.moe_experts(4, 42, D, H)
+    return wg, wu, wd, (G.dev(wg), G.dev(wu), G.dev(wd))
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 16])
+def test_moe_ffn_layer(ref, syn, ffn_layer, T):
+    # few items (direct and routed small-M paths): gate, up with the SwiGLU
+    # epilogue, down on the bf16 h rows, ordered combine; invalid ids add nothing
+    wg, wu, wd, devs = ffn_layer
+    (H, D), E, topk = G.MOE_UP, G.MOE_E, G.MOE_TOPK
+    ids, gates = syn.routing(300 + T, 301 + T, T, E, topk)
+    if T > 1:
+        ids[1, 4] = -1
+    x = G.activations(4, 43, T, D)
+    y = run_ffn(wg, wu, wd, E, H, D, x, ids, gates, devs)
+    want = ref.moe_ffn(wg, wu, wd, E, H, D, x, ids, gates, threads=16)
+    assert not np.isnan(y).any()
+    assert G.rel_err(y, want) <= TOL_SMALL
+
+
+def test_moe_ffn_t2048_sampled(ref, syn, ffn_layer):
+    # the prefill-sized layer (tensor-core path, h stored expert-sorted), in the
+    # configuration the benchmark times; the oracle computes sampled tokens
+    wg, wu, wd, devs = ffn_layer
+    (H, D), E, topk = G.MOE_UP, G.MOE_E, G.MOE_TOPK
+    T = 2048
+    ids, gates = syn.routing(syn.seed(4, 2) + T, syn.seed(4, 3) + T, T, E, topk)
+    x = G.activations(4, 44, T, D)
+    y = run_ffn(wg, wu, wd, E, H, D, x, ids, gates, devs)
+    assert not np.isnan(y).any()
+    tok = G.sample_rows(T, 32, seed=5)
+    want = ref.moe_ffn(wg, wu, wd, E, H, D, x[tok], ids[tok], gates[tok], threads=16)
+    assert G.rel_err(y[tok], want) <= TOL_FFN_TC
+    # the gap to the oracle is the bf16 weight operand's rounding: with that rounding
+    # modelled (and nothing else), the kernels agree to fp32 accumulation order
+    xb = (x[tok[:6]].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    rb_d, rb_h = D // 256 * 144, H // 256 * 144
+    model = np.zeros((len(xb), D))
+    for i, t in enumerate(tok[:6]):
+        for j in range(topk):
+            e = int(ids[t, j])
+            g = G.tc_weights(wg.reshape(-1)[e * H * rb_d:(e + 1) * H * rb_d], H, D) @ xb[i]
+            u = G.tc_weights(wu.reshape(-1)[e * H * rb_d:(e + 1) * H * rb_d], H, D) @ xb[i]
+            h = G._bf16(g / (1.0 + np.exp(-g)) * u)
+            model[i] += gates[t, j] * (G.tc_weights(wd.reshape(-1)[e * D * rb_h:(e + 1) * D * rb_h], D, H) @ h)
+    assert G.rel_err(y[tok[:6]], model) <= 1e-3
+
+
+@pytest.mark.parametrize("E,T,topk,H,D", [(4, 64, 2, 256, 512), (3, 300, 2, 512, 768), (6, 40, 3, 256, 256)])
+def test_moe_ffn_small_layers(ref, syn, E, T, topk, H, D):
+    # the tensor-core path with several token tiles per expert, and the small-M
+    # path with row-split CTAs (K = 256); invalid ids, a token with no valid id
+    wg = np.concatenate([G.weights(4, 200 + e, H, D, outliers=True) for e in range(E)])
+    wu = np.concatenate([G.weights(4, 220 + e, H, D) for e in range(E)])
+    wd = np.concatenate([G.weights(4, 240 + e, D, H) for e in range(E)])
+    ids, gates = syn.routing(900 + T, 901 + T, T, E, topk)
+    ids[3, 1] = -5
+    ids[5, :] = E
+    x = G.activations(4, 45, T, D)
+    y = run_ffn(wg, wu, wd, E, H, D, x, ids, gates)
+    want = ref.moe_ffn(wg, wu, wd, E, H, D, x, ids, gates, threads=16)
+    assert np.all(y[5] == 0.0)
+    tol = TOL_FFN_TC if T * topk >= 32 * E else TOL_SMALL
+    assert G.rel_err(y, want) <= tol
+
+
+@pytest.mark.parametrize("T", [16, 600])
+def test_moe_ffn_matches_grouped_calls_and_is_deterministic(syn, ffn_layer, T):
+    # same bits on a second call; and the same as the layer written with the
+    # grouped-GEMM calls when h is formed the same way (fp32 SwiGLU rounded to bf16)
+    wg, wu, wd, devs = ffn_layer
+    (H, D), E, topk = G.MOE_UP, G.MOE_E, G.MOE_TOPK
+    ids, gates = syn.routing(500 + T, 501 + T, T, E, topk)
+    x = G.activations(4, 46, T, D)
+    a = run_ffn(wg, wu, wd, E, H, D, x, ids, gates, devs)
+    b = run_ffn(wg, wu, wd, E, H, D, x, ids, gates, devs)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    P, C = q4k.Q4K_MOE_Y_PER_SLOT, q4k.Q4K_MOE_Y_COMBINE
+    g = run_moe(None, E, H, D, x, q4k.Q4K_MOE_X_PER_TOKEN, ids, gates, P, w_dev=devs[0])
+    u = run_moe(None, E, H, D, x, q4k.Q4K_MOE_X_PER_TOKEN, ids, gates, P, w_dev=devs[1])
+    gt, ut = torch.from_numpy(g), torch.from_numpy(u)
+    h = (gt / (1.0 + torch.exp(-gt)) * ut).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    yc = run_moe(None, E, D, H, h.reshape(T * topk, H), q4k.Q4K_MOE_X_PER_SLOT, ids, gates, C, w_dev=devs[2])
+    # h may differ in the last bf16 place where host and device exp differ
+    assert G.rel_err(a, yc) <= TOL_SMALL

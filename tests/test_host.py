@@ -52,6 +52,15 @@ def test_workspace_sizes(lib):
     assert a >= (129 + 128) * 4 and a % 256 == 0
     assert b >= a + 16 * 8 * 2048 * 4
     assert q4k.q4k_gemm_workspace_size(1, 17408, 5120) >= 0
+    # expert FFN: routing + g (fp32) + h (bf16) + per-slot outputs (fp32); + sorted x from 32*E items
+    assert q4k.q4k_moe_ffn_workspace_size(128, 768, 2000, 16, 8) == 0       # D not a multiple of 256
+    assert q4k.q4k_moe_ffn_workspace_size(128, 700, 2048, 16, 8) == 0       # H not a multiple of 256
+    f = q4k.q4k_moe_ffn_workspace_size(128, 768, 2048, 16, 8)
+    n = 16 * 8
+    assert f % 256 == 0 and f >= (129 + n) * 4 + n * 768 * 6 + n * 2048 * 4
+    big = q4k.q4k_moe_ffn_workspace_size(128, 768, 2048, 4096, 8)
+    n = 4096 * 8
+    assert big >= n * 768 * 6 + n * 2048 * 6
 
 
 A16 = 1 << 20  # a 16-byte aligned fake address; never dereferenced by these calls
@@ -84,6 +93,20 @@ A16 = 1 << 20  # a 16-byte aligned fake address; never dereferenced by these cal
     (lambda L: L.q4k_moe_grouped_gemm(A16, 8, 64, 256, A16, 0, A16, A16, 4, 2, A16, 1, A16 + 16, 1 << 20, None),
      q4k.Q4K_ERR_ALIGN),
     (lambda L: L.q4k_moe_grouped_gemm(A16, 8, 64, 256, A16, 0, A16, A16, 4, 2, A16, 1, A16, 64, None),
+     q4k.Q4K_ERR_WORKSPACE),
+    (lambda L: L.q4k_moe_ffn(A16, A16, None, 8, 256, 512, A16, A16, A16, 4, 2, A16, A16, 1 << 24, None),
+     q4k.Q4K_ERR_NULL),
+    (lambda L: L.q4k_moe_ffn(A16, A16, A16, 8, 256, 512, A16, A16, None, 4, 2, A16, A16, 1 << 24, None),
+     q4k.Q4K_ERR_NULL),
+    (lambda L: L.q4k_moe_ffn(A16, A16, A16, 8, 300, 512, A16, A16, A16, 4, 2, A16, A16, 1 << 24, None),
+     q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_moe_ffn(A16, A16, A16, 8, 256, 512, A16, A16, A16, 4, 9, A16, A16, 1 << 24, None),
+     q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_moe_ffn(A16, A16 + 8, A16, 8, 256, 512, A16, A16, A16, 4, 2, A16, A16, 1 << 24, None),
+     q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_moe_ffn(A16, A16, A16, 8, 256, 512, A16, A16, A16, 4, 2, A16, A16 + 64, 1 << 24, None),
+     q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_moe_ffn(A16, A16, A16, 8, 256, 512, A16, A16, A16, 4, 2, A16, A16, 1024, None),
      q4k.Q4K_ERR_WORKSPACE),
 ])
 def test_argument_errors_before_any_device_work(lib, call, status):
