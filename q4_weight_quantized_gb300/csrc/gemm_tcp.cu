@@ -340,12 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                     tmem_ld32(tmem + (uint32_t)(buf * kBN) + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
                     tmem_ld_wait();
                     if (n < p.N) {
+                        if (p.glu.h_sorted) {
+                            // rows t.m0 + col: consecutive, one pitch apart
+                            uint16_t *hp = p.glu.h + (int64_t)(t.m0 + 32 * cc) * p.ldy + n;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int col = 32 * cc + j;
-                            if (col < t.cnt) {
-                                const int64_t hrow = p.glu.h_sorted ? (int64_t)(t.m0 + col) : (int64_t)orw[col];
-                                p.glu.h[hrow * p.ldy + n] = swiglu_bf16(gv[j], __uint_as_float(v[j]));
+                            for (int j = 0; j < 32; ++j) {
+                                if (32 * cc + j < t.cnt) *hp = swiglu_bf16(gv[j], __uint_as_float(v[j]));
+                                hp += p.ldy;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int col = 32 * cc + j;
+                                if (col < t.cnt)
+                                    p.glu.h[(int64_t)orw[col] * p.ldy + n] = swiglu_bf16(gv[j], __uint_as_float(v[j]));
                             }
                         }
                     }

@@ -25,10 +25,26 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // SwiGLU of one element of a routed expert's feed-forward layer, rounded once
-// to bf16 (nearest, ties to even): silu(g) * u with silu(g) = g / (1 + e^-g),
-// in fp32.  The rounding is there because the down projection reads bf16.
+// to bf16 (nearest, ties to even): silu(g) * u with silu(g) = g / (1 + e^-g).
+// e^-g = 2^(-g log2 e) and the reciprocal come from the approximate ex2 and rcp
+// instructions (a few fp32 ulps together, far below the bf16 rounding that
+// follows; the down projection reads bf16).  For g below about -88, e^-g is +inf
+// and its reciprocal +0, so h is a signed zero, the limit of silu.  Seven
+// instructions: the tensor-core kernels' epilogue competes for issue slots with
+// their dequantizing warps.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ uint16_t swiglu_bf16(float g, float u) {
-    const float h = g / (1.0f + expf(-g)) * u;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float h = g * rcp_approx(1.0f + ex2_approx(-kLog2e * g)) * u;
     return __bfloat16_as_ushort(__float2bfloat16_rn(h));
 }
 
