@@ -7,7 +7,8 @@
 //
 //   * warp 0    TMA: per 256-wide K block the raw Q4_K tile of 128 weight rows
 //               (two slots, issued one block ahead, across tile boundaries), per
-//               64-wide stage the 256-token activation tile (128-byte swizzle);
+//               64-wide stage the token tile's activation rows (128-byte swizzle;
+//               one or two 128-row boxes, as the tile's count needs);
 //   * warp 1    MMA: one thread issues 4 x tcgen05.mma (128 x N x 16) per stage
 //               into one of two 256-column accumulators in tensor memory;
 //   * warps 2-9 dequant: two threads per weight row, each taking 16 of the 32
@@ -36,6 +37,8 @@ constexpr int kBN = 256;                            // tokens per tile (MMA N at
 constexpr int kStageK = 64;                         // K per stage: one 128-byte swizzle row of bf16
 constexpr int kNS = 3;                              // stages
 constexpr int kXB = kBN * kStageK * 2;              // 32 KiB activations per stage
+constexpr int kXBox = kBN / 2;                      // activation rows per TMA box
+constexpr int kXBoxBytes = kXBox * kStageK * 2;     // 16 KiB: rows kXBox.. land right after, as one 256-row box would
 constexpr int kAB = kTileRows * kStageK * 2;        // 16 KiB dequantized weights per stage
 constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K per block
 constexpr int kDqWarps = 8, kEpWarps = 4;
@@ -181,8 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(xfull0 + 8 * s, kXB);
-                    tma_load_2d(smem_u32(xs + s * kXB), &tmX, kb * kQK + kStageK * g, t.m0, xfull0 + 8 * s);
+                    // one 128-row box for a tile of at most 128 tokens, two otherwise:
+                    // the MMA reads only the tile's rows
+                    const int nbox = t.cnt > kXBox ? 2 : 1;
+                    mbar_arrive_expect_tx(xfull0 + 8 * s, nbox * kXBoxBytes);
+                    for (int q = 0; q < nbox; ++q)
+                        tma_load_2d(smem_u32(xs + s * kXB + q * kXBoxBytes), &tmX, kb * kQK + kStageK * g,
+                                    t.m0 + q * kXBox, xfull0 + 8 * s);
                     ++x_issued;
                 }
             }
@@ -389,7 +397,7 @@ cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, i
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kTileRows, kBlockBytes / 4);
     if (e != cudaSuccess) return e;
-    e = make_act_tmap_sw128(&tmX, x_sorted, n_items, K, K, kBN);
+    e = make_act_tmap_sw128(&tmX, x_sorted, n_items, K, K, kXBox);
     if (e != cudaSuccess) return e;
     Params p = {};
     p.y = out;
