@@ -446,15 +446,12 @@ q4k_status q4k_moe_ffn(const void *w_gate, const void *w_up, const void *w_down,
             e = launch_moe_tcp(di, w_up, E, H, D, x_sorted, n, perm, tiles, n_tiles, nullptr, s, glu);
         if (e == cudaSuccess) e = launch_moe_tcp(di, w_down, E, D, H, h, n, perm, tiles, n_tiles, o, s);
     } else {
+        // gate and up in one pass: h straight from the two accumulators
         GluOut glu;
-        glu.g = g;
         glu.h = h;
         if (e == cudaSuccess)
-            e = launch_moe_smallm(di, w_gate, E, H, D, x, 0, perm, offsets, tiles, n_tiles, topk_ids, T, topk, g,
-                                  false, s);
-        if (e == cudaSuccess)
-            e = launch_moe_smallm(di, w_up, E, H, D, x, 0, perm, offsets, tiles, n_tiles, topk_ids, T, topk, nullptr,
-                                  false, s, glu);
+            e = launch_moe_smallm(di, w_gate, E, H, D, x, 0, perm, offsets, tiles, n_tiles, topk_ids, T, topk, nullptr,
+                                  false, s, glu, w_up);
         if (e == cudaSuccess)
             e = launch_moe_smallm(di, w_down, E, D, H, h, 1, perm, offsets, tiles, n_tiles, topk_ids, T, topk, o,
                                   false, s);

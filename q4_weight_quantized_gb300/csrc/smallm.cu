@@ -216,35 +216,12 @@ struct RowArgs {
     int direct;
     const int32_t *ids;
     int E;
-    GluOut glu;  // MoE: SwiGLU epilogue (up projection of an expert FFN)
+    GluOut glu;  // MoE with GLU: h (bf16) receives the SwiGLU of the gate and up projections
 };
 
 // The (token, k-slot) item at position p of the expert-sorted order (MoE).
 __device__ __forceinline__ int item_at(const RowArgs &ra, int p) { return ra.direct ? p : __ldg(ra.perm + p); }
 
-// Stores n <= NMAX MoE output elements, element i = (offset off(i) in the output
-// rows, value val(i)): fp32 y, or with GLU the SwiGLU epilogue's bf16 h.  For h,
-// every gate value is loaded before the first store, so the loads overlap.
-template <bool GLU, int NMAX, typename Off, typename Val>
-__device__ __forceinline__ void store_out(const RowArgs &ra, int n, Off &&off, Val &&val) {
-    if constexpr (GLU) {
-        long long o[NMAX];
-        float g[NMAX];
-#pragma unroll
-        for (int i = 0; i < NMAX; ++i) {
-            o[i] = i < n ? off(i) : -1;
-            g[i] = o[i] >= 0 ? __ldg(ra.glu.g + o[i]) : 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < NMAX; ++i)
-            if (o[i] >= 0) ra.glu.h[o[i]] = swiglu_bf16(g[i], val(i));
-    } else {
-        for (int i = 0; i < n; ++i) {
-            const long long oi = off(i);
-            if (oi >= 0) ra.y[oi] = val(i);
-        }
-    }
-}
 
 // Activation row and output offset of token slot n (-1 if the slot is empty).
 template <bool MOE>
@@ -269,9 +246,14 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // split rows instead of K - warp w owns rows w*ROWS.. of a 4*ROWS-row CTA over
 // all K blocks and stores its own outputs, with no cross-warp reduction.  CH:
 // token slots per chunk (at most 8 * NT; fewer shrinks the activation part of a
-// slot when experts get few items).  GLU (MoE): the SwiGLU epilogue (RowArgs::glu).
+// slot when experts get few items).  GLU (MoE): the gate (tmW) and up (tmW2)
+// projections of an expert FFN in one pass - warps 0-1 take the gate matrix,
+// warps 2-3 the up matrix, for the same rows (row split: a 2*ROWS-row CTA, the
+// pairs owning ROWS rows each; K split: each pair splits K) - and the epilogue
+// stores h = bf16(silu(g) * u) (RowArgs::glu.h) instead of fp32 rows.
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                          const __grid_constant__ CUtensorMap tmW2,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
                                                           int KB, int nx, unsigned int *status) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -287,12 +269,17 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const int S = gridDim.x;       // K split = cluster size (always 1 for MoE)
     const int split = blockIdx.x;  // == cluster rank
     static_assert(!RS || (MOE && ROWS == 32), "row split is a MoE mode");
-    const int row0 = blockIdx.y * kRows * (RS ? kWarps : 1);
-    const int wrow0 = row0 + (RS ? warp * kRows : 0);  // this warp's first row
+    static_assert(!GLU || MOE, "the fused gate and up projections are a MoE mode");
+    // GLU: the warp pair of matrix `mat` (0 gate, 1 up); wsub = this warp's index in its pair
+    constexpr int kNw = GLU ? 2 : kWarps;  // warps per weight matrix
+    const int mat = GLU ? warp >> 1 : 0, wsub = GLU ? warp & 1 : warp;
+    const CUtensorMap *tw = mat ? &tmW2 : &tmW;
+    const int row0 = blockIdx.y * kRows * (RS ? kNw : 1);
+    const int wrow0 = row0 + (RS ? wsub * kRows : 0);  // this warp's first row
     const int kb0 = (int)((int64_t)KB * split / S), kb1 = (int)((int64_t)KB * (split + 1) / S);
-    // this warp's blocks: all of them (row split), or blocks warp, warp+4, ... of the split
-    const int nblk = RS ? kb1 - kb0 : (kb1 - kb0 > warp ? (kb1 - kb0 - warp + kWarps - 1) / kWarps : 0);
-    const int kb_first = RS ? kb0 : kb0 + warp, kb_step = RS ? 1 : kWarps;
+    // this warp's blocks: all of them (row split), or blocks wsub, wsub+kNw, ... of the split
+    const int nblk = RS ? kb1 - kb0 : (kb1 - kb0 > wsub ? (kb1 - kb0 - wsub + kNw - 1) / kNw : 0);
+    const int kb_first = RS ? kb0 : kb0 + wsub, kb_step = RS ? 1 : kNw;
 
     if constexpr (MOE) pdl_wait();  // the routing comes from the previous kernel
     int off0 = 0, cnt = ra.M, tma_row = wrow0;
@@ -301,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         const int item = blockIdx.z, e = __ldg(ra.ids + item);
         if (e < 0 || e >= ra.E) {  // invalid id: zero this CTA's part of the row, leave before any barrier
             if (ra.zero_invalid)
-                for (int col = threadIdx.x; col < kRows * (RS ? kWarps : 1); col += kThreads)
+                for (int col = threadIdx.x; col < kRows * (RS ? kNw : 1); col += kThreads)
                     if (row0 + col < N) ra.y[(long long)item * ra.ldy + row0 + col] = 0.0f;
             return;
         }
@@ -337,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     if (lane == 0) {
         for (int i = 0; i < SLOTS; ++i) mbar_init(bar0 + 8 * i, 1);
         fence_mbar_init();
-        prefetch_tmap(&tmW);
+        prefetch_tmap(tw);
         prefetch_tmap(&tmX);
         if constexpr (!MOE) {
             // static weights: the weight halves of the first slots go out before the
@@ -346,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
                 for (int it = 0; it < SLOTS && it < total; ++it) {
                     const uint32_t bar = bar0 + 8 * (it % SLOTS);
                     mbar_arrive_expect_tx(bar, kBlkWBytes + min(kPerChunk, cnt) * kXBlkBytes);
-                    tma_load_2d(smem_u32(region + (it % SLOTS) * sbytes), &tmW, (kb_first + kb_step * it) * kBlkWords,
+                    tma_load_2d(smem_u32(region + (it % SLOTS) * sbytes), tw, (kb_first + kb_step * it) * kBlkWords,
                                 tma_row, bar);
                 }
         }
@@ -367,7 +354,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         const uint32_t dst = smem_u32(region + slot * sbytes);
         if (lane == 0 && weights) {
             mbar_arrive_expect_tx(bar0 + 8 * slot, kBlkWBytes + nvalid * kXBlkBytes);
-            tma_load_2d(dst, &tmW, kb * kBlkWords, tma_row, bar0 + 8 * slot);
+            tma_load_2d(dst, tw, kb * kBlkWords, tma_row, bar0 + 8 * slot);
         }
         __syncwarp();
         if (lane < nvalid) tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes, &tmX, kb * (kQK / 4), xrow, bar0 + 8 * slot);
@@ -390,21 +377,6 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         bool live[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) live[nt] = nt * 8 + r < nvalid;
-        // SwiGLU epilogue with row split: lane l holds the item of the chunk's token
-        // slot l, and the gate values of this warp's rows are loaded now, so that
-        // they arrive while the weights stream
-        int my_item = -1;
-        float gpre[GLU && RS ? kPerChunk : 1];
-        if constexpr (MOE && RS && GLU) {
-            if (lane < nvalid) my_item = item_at(ra, off0 + ch * kPerChunk + lane);
-#pragma unroll
-            for (int tk = 0; tk < kPerChunk; ++tk) {
-                const int item = __shfl_sync(0xFFFFFFFFu, my_item, tk);
-                gpre[tk] = tk < nvalid && wrow0 + lane < N
-                               ? __ldg(ra.glu.g + (long long)item * ra.ldy + wrow0 + lane)
-                               : 0.0f;
-            }
-        }
 
         for (int j = 0; j < nblk && !aborted; ++j, ++it) {
             const int slot = it % SLOTS;
@@ -445,15 +417,24 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
                     mine[(tk + 1) * kRows + rA + 8] = acc[rt][nt][3];
                 }
             __syncwarp();
-            const bool store = !aborted && wrow0 + lane < N;
             if constexpr (GLU) {
-#pragma unroll
-                for (int tk = 0; tk < kPerChunk; ++tk) {
-                    const long long o = (long long)__shfl_sync(0xFFFFFFFFu, my_item, tk) * ra.ldy + wrow0 + lane;
-                    if (store && tk < nvalid) ra.glu.h[o] = swiglu_bf16(gpre[tk], mine[tk * kRows + lane]);
+                // the gate warp of each pair forms h from its own rows and those of the
+                // up warp two places on (same rows), once both are staged
+                __syncthreads();
+                if (mat == 0 && !*(volatile int *)&abort_flag) {  // warp-uniform
+                    const float *mine_u =
+                        reinterpret_cast<const float *>(smem + (warp + 2) * G::warp_bytes(nx, SLOTS) + SLOTS * sbytes);
+                    const int my_item = lane < nvalid ? item_at(ra, off0 + ch * kPerChunk + lane) : 0;
+                    const bool in = wrow0 + lane < N;
+                    for (int tk = 0; tk < nvalid; ++tk) {
+                        const long long o =
+                            (long long)__shfl_sync(0xFFFFFFFFu, my_item, tk) * ra.ldy + wrow0 + lane;
+                        if (in) ra.glu.h[o] = swiglu_bf16(mine[tk * kRows + lane], mine_u[tk * kRows + lane]);
+                    }
                 }
+                __syncthreads();  // the up warps' tables are rewritten by the next chunk
             } else {
-                if (store)
+                if (!aborted && wrow0 + lane < N)
                     for (int tk = 0; tk < nvalid; ++tk)
                         ra.y[(long long)item_at(ra, off0 + ch * kPerChunk + tk) * ra.ldy + wrow0 + lane] =
                             mine[tk * kRows + lane];
@@ -481,22 +462,23 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             }
             __syncthreads();
             if (!*(volatile int *)&abort_flag) {
-                // thread i takes elements i, i + 128, ... of the chunk's [tokens][kRows]
-                constexpr int kPer = (16 * kRows + kThreads - 1) / kThreads;
-                const int mine_n = (nvalid * kRows - (int)threadIdx.x + kThreads - 1) / kThreads;
-                store_out<GLU, kPer>(
-                    ra, mine_n,
-                    [&](int i) {
-                        const int e2 = threadIdx.x + i * kThreads, tk = e2 / kRows, rr = e2 % kRows;
-                        return row0 + rr < N ? yoff_s[tk] + row0 + rr : -1LL;
-                    },
-                    [&](int i) {
-                        const int e2 = threadIdx.x + i * kThreads;
+                if constexpr (GLU) {
+                    // g: the gate pair's partials (warps 0, 1), u: the up pair's (2, 3)
+                    for (int e2 = threadIdx.x; e2 < nvalid * kRows; e2 += kThreads) {
+                        const float g = red_w[e2] + red_w[16 * kRows + e2];
+                        const float u = red_w[2 * 16 * kRows + e2] + red_w[3 * 16 * kRows + e2];
+                        const int tk = e2 / kRows, rr = e2 % kRows;
+                        if (row0 + rr < N) ra.glu.h[yoff_s[tk] + row0 + rr] = swiglu_bf16(g, u);
+                    }
+                } else {
+                    for (int e2 = threadIdx.x; e2 < nvalid * kRows; e2 += kThreads) {
                         float v = red_w[e2];
 #pragma unroll
                         for (int w = 1; w < kWarps; ++w) v += red_w[w * 16 * kRows + e2];
-                        return v;
-                    });
+                        const int tk = e2 / kRows, rr = e2 % kRows;
+                        if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = v;
+                    }
+                }
             }
             __syncthreads();  // red_w and the token table are reused by the next chunk
         }
@@ -553,12 +535,14 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
 
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
-                       const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status) {
+                       const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status,
+                       const CUtensorMap *tmW2 = nullptr) {
     const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS);
     auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmX, ra, N, KB, nx,
+    return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmW2 ? *tmW2 : tmW, tmX,
+                      ra, N, KB, nx,
                       status);
 }
 
@@ -646,8 +630,8 @@ struct MoeShape {
 
 // The MoE kernel variant for a call: row split or not, chunk size, ring depth.
 template <bool GLU>
-cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tmW, const CUtensorMap &tmX,
-                        const RowArgs &ra, int n, int KB, unsigned int *status) {
+cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tmW, const CUtensorMap *tmW2,
+                        const CUtensorMap &tmX, const RowArgs &ra, int n, int KB, unsigned int *status) {
     if (m.rs) {
         // chunks of 4, 8 or 16 token slots for up to 4, 8 or more items per expert
         // on average (every chunk streams the weights once); a third ring slot while
@@ -655,22 +639,22 @@ cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tm
         if (m.per_expert <= 4 || m.direct) {
             const int nx = m.nx1 ? 1 : 4;
             return m.deep ? launch_cfg<1, true, false, 3, 32, true, 4, GLU>(1, m.tiles, m.layers, nx, s, tmW, tmX, ra,
-                                                                             n, KB, status)
+                                                                             n, KB, status, tmW2)
                           : launch_cfg<1, true, false, 2, 32, true, 4, GLU>(1, m.tiles, m.layers, nx, s, tmW, tmX, ra,
-                                                                             n, KB, status);
+                                                                             n, KB, status, tmW2);
         }
         if (m.per_expert <= 8)
             return m.deep ? launch_cfg<1, true, false, 3, 32, true, 8, GLU>(1, m.tiles, m.layers, 8, s, tmW, tmX, ra, n,
-                                                                             KB, status)
+                                                                             KB, status, tmW2)
                           : launch_cfg<1, true, false, 2, 32, true, 8, GLU>(1, m.tiles, m.layers, 8, s, tmW, tmX, ra, n,
-                                                                             KB, status);
+                                                                             KB, status, tmW2);
         return launch_cfg<2, true, false, 2, 32, true, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB,
-                                                                 status);
+                                                                 status, tmW2);
     }
     if (m.few)
         return launch_cfg<1, true, false, 3, 32, false, 8, GLU>(1, m.tiles, m.layers, m.nx1 ? 1 : 8, s, tmW, tmX, ra,
-                                                                 n, KB, status);
-    return launch_cfg<2, true, false, 2, 32, false, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB, status);
+                                                                 n, KB, status, tmW2);
+    return launch_cfg<2, true, false, 2, 32, false, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB, status, tmW2);
 }
 
 }  // namespace
@@ -678,12 +662,19 @@ cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tm
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
-                              float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu) {
-    CUtensorMap tmW, tmX;
+                              float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu,
+                              const void *w_up) {
+    CUtensorMap tmW, tmW2, tmX;
     // all experts stacked: E*N rows of the same pitch
     constexpr int kRows = 32;
     cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kRows, kBlkWords);
     if (e != cudaSuccess) return e;
+    const bool fused = glu.h != nullptr;  // gate (w_experts) and up (w_up) in one pass
+    if (fused) {
+        if (!w_up) return cudaErrorInvalidValue;
+        e = make_weight_tmap(&tmW2, w_up, (int64_t)E * N, K, kRows, kBlkWords);
+        if (e != cudaSuccess) return e;
+    }
     e = make_act_tmap(&tmX, x, x_per_slot ? T * topk : T, K, K, kQK / 4);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
@@ -693,7 +684,9 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     const int64_t items_all = T * topk;
     const int64_t rs_ctas = (N + kRows * kWarps - 1) / (kRows * kWarps) * (items_all < E ? items_all : E);
     const bool rs = KB < 2 * kWarps || (KB < 4 * kWarps && rs_ctas >= 2 * (int64_t)di.sm_count);
-    const int tiles = (int)((N + kRows * (rs ? kWarps : 1) - 1) / (kRows * (rs ? kWarps : 1)));
+    // rows per CTA: 32 (K split), 128 (row split), 64 (row split, gate and up fused)
+    const int cta_rows = kRows * (rs ? (fused ? 2 : kWarps) : 1);
+    const int tiles = (int)((N + cta_rows - 1) / cta_rows);
     RowArgs ra = {};
     ra.y = out; ra.ldy = N; ra.M = 0;
     ra.x_per_slot = x_per_slot; ra.topk = topk; ra.perm = perm; ra.tiles = tok_tiles; ra.n_tiles = n_tiles;
@@ -708,8 +701,8 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     const bool deep = rs_ctas <= di.sm_count;
     const int64_t per_expert = (items + (items < E ? items : E) - 1) / (items < E ? items : E);
     const MoeShape ms = {rs, deep, per_expert, ra.direct != 0, items <= 64 * (int64_t)E, tiles, layers, nx1};
-    return glu.h ? moe_variant<true>(ms, s, tmW, tmX, ra, (int)N, KB, di.status)
-                 : moe_variant<false>(ms, s, tmW, tmX, ra, (int)N, KB, di.status);
+    return fused ? moe_variant<true>(ms, s, tmW, &tmW2, tmX, ra, (int)N, KB, di.status)
+                 : moe_variant<false>(ms, s, tmW, nullptr, tmX, ra, (int)N, KB, di.status);
 }
 
 }  // namespace q4k
