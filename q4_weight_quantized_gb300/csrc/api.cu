@@ -358,11 +358,15 @@ static q4k_status moe_common(const void *w_experts, int32_t n_experts, int64_t N
     if (e == cudaSuccess && tc)
         e = launch_moe_gather(di, x, x_mode, topk, perm, offsets, n_experts, T * topk, K, x_sorted,
                               per_slot ? y : nullptr, N, s);
+    // with very few items the small-M kernel combines in the CTA, straight into y
+    const bool dcomb = !tc && !per_slot && moe_direct(T * topk);
     if (e == cudaSuccess)
         e = tc ? launch_moe_tcp(di, w_experts, n_experts, N, K, x_sorted, T * topk, perm, tiles, n_tiles, slot_out, s)
                : launch_moe_smallm(di, w_experts, n_experts, N, K, x, x_mode, perm, offsets, tiles, n_tiles, topk_ids,
-                                   T, topk, slot_out, per_slot, s);
-    if (e == cudaSuccess && !per_slot) e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);
+                                   T, topk, dcomb ? y : slot_out, per_slot, s, GluOut(), nullptr,
+                                   dcomb ? gates : nullptr);
+    if (e == cudaSuccess && !per_slot && !dcomb)
+        e = launch_moe_combine(di, slot_out, gates, topk_ids, n_experts, T, topk, N, y, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 
@@ -452,9 +456,13 @@ q4k_status q4k_moe_ffn(const void *w_gate, const void *w_up, const void *w_down,
         if (e == cudaSuccess)
             e = launch_moe_smallm(di, w_gate, E, H, D, x, 0, perm, offsets, tiles, n_tiles, topk_ids, T, topk, nullptr,
                                   false, s, glu, w_up);
+        // very few items: the down projection combines in the CTA, straight into y
+        const bool dcomb = moe_direct(n);
         if (e == cudaSuccess)
-            e = launch_moe_smallm(di, w_down, E, D, H, h, 1, perm, offsets, tiles, n_tiles, topk_ids, T, topk, o,
-                                  false, s);
+            e = launch_moe_smallm(di, w_down, E, D, H, h, 1, perm, offsets, tiles, n_tiles, topk_ids, T, topk,
+                                  dcomb ? y : o, false, s, GluOut(), nullptr, dcomb ? gates : nullptr);
+        if (e == cudaSuccess && !dcomb) e = launch_moe_combine(di, o, gates, topk_ids, E, T, topk, D, y, s);
+        return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
     }
     if (e == cudaSuccess) e = launch_moe_combine(di, o, gates, topk_ids, E, T, topk, D, y, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);

@@ -59,7 +59,10 @@ cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, i
 // the routing permutation (perm/offsets from launch_moe_route).  With glu.h set,
 // w_experts and w_up are an expert FFN's gate and up matrices (same shape),
 // computed in one pass, and h = bf16(silu(g) * u) is stored instead of out
-// (glu.g is not used).
+// (glu.g is not used).  With gates set and very few items (moe_direct), out is
+// the combined y [T][N]: y[t] = sum_j gates[t][j] * (slot j's row), j in
+// increasing order and invalid ids skipped, the same bits as launch_moe_combine
+// over the per-slot rows.
 // With zero_invalid, the per-slot rows of the items with an invalid id
 // (perm[offsets[E] .. T*topk)) are zeroed.  With very few items (moe_direct),
 // no routing is read: each item is its own grid layer, its expert ids[item].
@@ -68,7 +71,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
                               float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu = GluOut(),
-                              const void *w_up = nullptr);
+                              const void *w_up = nullptr, const float *gates = nullptr);
 
 // Stable counting sort of items by expert (E <= 1024).  Items with an id
 // outside [0, E) are left out of offsets; with invalid_tail they follow the

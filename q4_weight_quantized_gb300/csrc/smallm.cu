@@ -217,6 +217,7 @@ struct RowArgs {
     const int32_t *ids;
     int E;
     GluOut glu;  // MoE with GLU: h (bf16) receives the SwiGLU of the gate and up projections
+    const float *gates;  // MoE with DC: the combine weights [T][topk]
 };
 
 // The (token, k-slot) item at position p of the expert-sorted order (MoE).
@@ -250,8 +251,13 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // projections of an expert FFN in one pass - warps 0-1 take the gate matrix,
 // warps 2-3 the up matrix, for the same rows (row split: a 2*ROWS-row CTA, the
 // pairs owning ROWS rows each; K split: each pair splits K) - and the epilogue
-// stores h = bf16(silu(g) * u) (RowArgs::glu.h) instead of fp32 rows.
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false>
+// stores h = bf16(silu(g) * u) (RowArgs::glu.h) instead of fp32 rows.  DC (MoE
+// with very few items, the down projection): grid layer z is token z, warp w
+// takes the token's slots w, w+4, ... whole (all K blocks of its expert's rows),
+// and the CTA sums g[t][j] * out[t][j] over j in increasing order into y[t]:
+// the weighted combine, in the CTA, with the bits of the separate combine pass.
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
+          bool DC = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmW2,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
@@ -270,6 +276,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const int split = blockIdx.x;  // == cluster rank
     static_assert(!RS || (MOE && ROWS == 32), "row split is a MoE mode");
     static_assert(!GLU || MOE, "the fused gate and up projections are a MoE mode");
+    static_assert(!DC || (MOE && !RS && !GLU && NT == 1 && ONE), "the in-CTA combine is a one-token MoE mode");
     // GLU: the warp pair of matrix `mat` (0 gate, 1 up); wsub = this warp's index in its pair
     constexpr int kNw = GLU ? 2 : kWarps;  // warps per weight matrix
     const int mat = GLU ? warp >> 1 : 0, wsub = GLU ? warp & 1 : warp;
@@ -278,12 +285,25 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const int wrow0 = row0 + (RS ? wsub * kRows : 0);  // this warp's first row
     const int kb0 = (int)((int64_t)KB * split / S), kb1 = (int)((int64_t)KB * (split + 1) / S);
     // this warp's blocks: all of them (row split), or blocks wsub, wsub+kNw, ... of the split
-    const int nblk = RS ? kb1 - kb0 : (kb1 - kb0 > wsub ? (kb1 - kb0 - wsub + kNw - 1) / kNw : 0);
-    const int kb_first = RS ? kb0 : kb0 + wsub, kb_step = RS ? 1 : kNw;
+    const int nblk = RS || DC ? kb1 - kb0 : (kb1 - kb0 > wsub ? (kb1 - kb0 - wsub + kNw - 1) / kNw : 0);
+    const int kb_first = RS || DC ? kb0 : kb0 + wsub, kb_step = RS || DC ? 1 : kNw;
 
     if constexpr (MOE) pdl_wait();  // the routing comes from the previous kernel
     int off0 = 0, cnt = ra.M, tma_row = wrow0;
-    if constexpr (MOE) if (ra.direct) {
+    // DC: bit j of dc_mask marks this warp's j-th slot (slot warp + 4j) as valid;
+    // its chunks are the valid ones, in order
+    unsigned dc_mask = 0;
+    if constexpr (DC) {
+        const int j = warp + kWarps * lane;
+        bool v = false;
+        if (lane < 4 && j < ra.topk) {
+            const int e = __ldg(ra.ids + (int)blockIdx.z * ra.topk + j);
+            v = e >= 0 && e < ra.E;
+        }
+        dc_mask = __ballot_sync(0xFFFFFFFFu, v);
+        cnt = 1;
+    }
+    if constexpr (MOE && !DC) if (ra.direct) {
         // grid layer z = item z
         const int item = blockIdx.z, e = __ldg(ra.ids + item);
         if (e < 0 || e >= ra.E) {  // invalid id: zero this CTA's part of the row, leave before any barrier
@@ -296,7 +316,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         cnt = 1;
         tma_row = e * N + wrow0;
     }
-    if constexpr (MOE) if (!ra.direct) {
+    if constexpr (MOE && !DC) if (!ra.direct) {
         // grid layer z = token tile z of the routing (only tiles of experts that have items);
         // the layer right after the last tile zeroes the invalid items' rows of this row tile
         const int n_tl = __ldg(ra.n_tiles);
@@ -313,8 +333,14 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         if (cnt <= 0) return;  // expert without tokens: the whole CTA leaves before any barrier
         tma_row = e * N + wrow0;
     }
-    const int chunks = (cnt + kPerChunk - 1) / kPerChunk;
+    const int chunks = DC ? __popc(dc_mask) : (cnt + kPerChunk - 1) / kPerChunk;
     const int total = chunks * nblk;  // this warp's (chunk, block) iterations
+    // DC: the token slot of chunk ch
+    auto dc_slot = [&](int ch) {
+        unsigned m = dc_mask;
+        for (int i = 0; i < ch; ++i) m &= m - 1;  // drop the ch lowest valid slots
+        return warp + kWarps * (__ffs(m) - 1);
+    };
 
     const int sbytes = G::slot_bytes(nx);
     uint8_t *region = smem + warp * G::warp_bytes(nx, SLOTS);
@@ -347,14 +373,21 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     auto issue = [&](int it, bool weights) {
         const int ch = it / nblk, kb = kb_first + kb_step * (it % nblk);
         const int slot = it % SLOTS;
-        const int nvalid = min(kPerChunk, cnt - ch * kPerChunk);
+        const int nvalid = DC ? 1 : min(kPerChunk, cnt - ch * kPerChunk);
         int xrow;
         long long unused;
-        slot_rows<MOE>(ra, off0, cnt, ch * kPerChunk + lane, xrow, unused);
+        int row_w = tma_row;
+        if constexpr (DC) {
+            const int item = (int)blockIdx.z * ra.topk + dc_slot(ch);
+            xrow = ra.x_per_slot ? item : item / ra.topk;
+            row_w = __ldg(ra.ids + item) * N + wrow0;
+        } else {
+            slot_rows<MOE>(ra, off0, cnt, ch * kPerChunk + lane, xrow, unused);
+        }
         const uint32_t dst = smem_u32(region + slot * sbytes);
         if (lane == 0 && weights) {
             mbar_arrive_expect_tx(bar0 + 8 * slot, kBlkWBytes + nvalid * kXBlkBytes);
-            tma_load_2d(dst, tw, kb * kBlkWords, tma_row, bar0 + 8 * slot);
+            tma_load_2d(dst, tw, kb * kBlkWords, row_w, bar0 + 8 * slot);
         }
         __syncwarp();
         if (lane < nvalid) tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes, &tmX, kb * (kQK / 4), xrow, bar0 + 8 * slot);
@@ -373,7 +406,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[rt][nt][q] = 0.0f;
-        const int nvalid = min(kPerChunk, cnt - ch * kPerChunk);
+        const int nvalid = DC ? 1 : min(kPerChunk, cnt - ch * kPerChunk);
         bool live[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) live[nt] = nt * 8 + r < nvalid;
@@ -400,7 +433,17 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             fence_proxy_async_smem();
             if (it + SLOTS < total) issue(it + SLOTS, true);
         }
-        if constexpr (MOE && RS) {
+        if constexpr (DC) {
+            // this slot's complete output rows (token 0 of the fragment: lanes with
+            // c == 0, accumulators 0 and 2) into row dc_slot(ch) of the [16][kRows] stage
+            float *o = reinterpret_cast<float *>(smem + G::red_off(nx, SLOTS)) + dc_slot(ch) * kRows;
+            if (c == 0)
+#pragma unroll
+                for (int rt = 0; rt < kRowTiles; ++rt) {
+                    o[rt * 16 + r] = acc[rt][0][0];
+                    o[rt * 16 + r + 8] = acc[rt][0][2];
+                }
+        } else if constexpr (MOE && RS) {
             // row split: this warp stores its own rows of the chunk, staged as
             // [16][kRows] in its scale table (free until the next chunk's first
             // block) so that the stores coalesce
@@ -484,6 +527,22 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         }
     }
     if (aborted) drain_ring<SLOTS>(bar0, it, min(total, it + SLOTS), status);
+    if constexpr (DC) {
+        // the weighted combine of token t over its slots, in slot order
+        __syncthreads();
+        const int t = blockIdx.z;
+        if (!*(volatile int *)&abort_flag && threadIdx.x < kRows && row0 + (int)threadIdx.x < N) {
+            const float *o = reinterpret_cast<const float *>(smem + G::red_off(nx, SLOTS));
+            float v = 0.0f;
+            for (int j = 0; j < ra.topk; ++j) {
+                const int e = __ldg(ra.ids + t * ra.topk + j);
+                if (e < 0 || e >= ra.E) continue;
+                v = fmaf(__ldg(ra.gates + t * ra.topk + j), o[j * kRows + threadIdx.x], v);
+            }
+            ra.y[(long long)t * ra.ldy + row0 + threadIdx.x] = v;
+        }
+        return;
+    }
     if constexpr (MOE) return;
 
     __syncthreads();  // all slots consumed: the rings become reduction space
@@ -533,12 +592,13 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     }
 }
 
-template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false>
+template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
+          bool DC = false>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status,
                        const CUtensorMap *tmW2 = nullptr) {
     const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU>;
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU, DC>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmW2 ? *tmW2 : tmW, tmX,
@@ -663,7 +723,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
                               float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu,
-                              const void *w_up) {
+                              const void *w_up, const float *gates) {
     CUtensorMap tmW, tmW2, tmX;
     // all experts stacked: E*N rows of the same pitch
     constexpr int kRows = 32;
@@ -698,6 +758,14 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     // invalid items' rows); layers past the routing's tile count leave at once
     const int layers = ra.direct ? (int)items : (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
     const int nx1 = ra.direct ? 1 : 0;  // a direct layer has one token: one activation row per slot
+    if (ra.direct && gates && !fused) {
+        // the weighted combine in the CTA: one grid layer per token, 32-row CTAs
+        ra.gates = gates;
+        ra.zero_invalid = 0;
+        const int t32 = (int)((N + kRows - 1) / kRows);
+        return launch_cfg<1, true, true, 3, 32, false, 8, false, true>(1, t32, (int)T, 1, s, tmW, tmX, ra, (int)N,
+                                                                        KB, di.status);
+    }
     const bool deep = rs_ctas <= di.sm_count;
     const int64_t per_expert = (items + (items < E ? items : E) - 1) / (items < E ? items : E);
     const MoeShape ms = {rs, deep, per_expert, ra.direct != 0, items <= 64 * (int64_t)E, tiles, layers, nx1};

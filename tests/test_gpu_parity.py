@@ -492,6 +492,42 @@ def test_moe_few_items_direct(ref, syn, K):
     assert G.rel_err(yc, ref.moe(w, E, N, K, xs, True, ids, gates)) <= TOL_SMALL
 
 
+def _fma_f32(a: float, b: float, c: float) -> float:
+    """fmaf: a*b + c rounded once to binary32 (nearest, ties to even), exactly."""
+    from fractions import Fraction
+    v = Fraction(a) * Fraction(b) + Fraction(c)
+    if v == 0:
+        return 0.0 if (a * b == 0 and c == 0 and not np.signbit(c)) else float(np.float32(float(v)))
+    lo = float(np.float32(float(v)))          # a binary32 neighbour of v
+    cands = {lo, float(np.nextafter(np.float32(lo), np.float32(np.inf))),
+             float(np.nextafter(np.float32(lo), np.float32(-np.inf)))}
+    best = min(cands, key=lambda f: (abs(Fraction(f) - v),
+                                     int(np.array([f], np.float32).view(np.uint32)[0]) & 1))
+    return best
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_moe_combine_in_cta_same_bits(syn, moe_down, T):
+    # up to 16 items: the down projection sums the slots in the CTA; the result must be
+    # the fp32 fma chain over the per-slot rows in slot order, invalid ids skipped
+    N, K = G.MOE_DOWN
+    E, topk = G.MOE_E, G.MOE_TOPK
+    ids, gates = syn.routing(syn.seed(4, 2) + 50 + T, syn.seed(4, 3) + 50 + T, T, E, topk)
+    ids[0, 5] = -1
+    x = G.activations(4, 9, T * topk, K)
+    w = G.dev(moe_down)
+    y = run_moe(None, E, N, K, x, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_COMBINE, w_dev=w)
+    o = run_moe(None, E, N, K, x, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT, w_dev=w)
+    cols = G.sample_rows(N, 48, seed=T)
+    for t in range(T):
+        for n in cols:
+            acc = 0.0
+            for j in range(topk):
+                if 0 <= ids[t, j] < E:
+                    acc = _fma_f32(float(gates[t, j]), float(o[t, j, n]), acc)
+            assert np.float32(acc).view(np.uint32) == np.float32(y[t, n]).view(np.uint32), (t, n)
+
+
 def test_moe_determinism(syn, moe_up):
     N, K = G.MOE_UP
     T = 16
