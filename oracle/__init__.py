@@ -76,6 +76,10 @@ def _load():
             lib.q4k_ref_f64_to_bf16.restype = ctypes.c_uint16
             lib.q4k_ref_moe_ffn.argtypes = [P, P, P, i32, i64, i64, P, P, P, i64, i32, P, ctypes.c_int]
             lib.q4k_ref_moe_ffn.restype = ctypes.c_int
+            lib.q4k_ref_quantize_x8.argtypes = [P, i64, i64, P, P]
+            lib.q4k_ref_quantize_x8.restype = None
+            lib.q4k_ref_gemm_x8.argtypes = [P, i64, i64, P, P, i64, P]
+            lib.q4k_ref_gemm_x8.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -202,5 +206,27 @@ def moe_ffn(w_gate, w_up, w_down, E: int, H: int, D: int, x_bf16, ids, gates, th
     rc = _load().q4k_ref_moe_ffn(_p(_blocks(w_gate)), _p(_blocks(w_up)), _p(_blocks(w_down)), E, H, D, _p(x),
                                  _p(ids), _p(gates), T, topk, _p(y), threads)
     if rc != 0:
+        raise ValueError("bad shape")
+    return y
+
+
+def quantize_x8(x_bf16) -> tuple:
+    """Per-32 int8 quantization of bf16 rows [M, K]: (q int8 [M, K], s fp32 [M, K/32])
+    (q4k_ref_quantize_x8)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.int8)
+    sc = np.empty((M, K // 32), dtype=np.float32)
+    _load().q4k_ref_quantize_x8(_p(x), M, K, _p(q), _p(sc))
+    return q, sc
+
+
+def gemm_x8(w: np.ndarray, N: int, K: int, q, s) -> np.ndarray:
+    """y [M, N] fp64 = W . (s * q)^T over the int8 activations (q4k_ref_gemm_x8)."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    M = q.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    if _load().q4k_ref_gemm_x8(_p(_blocks(w)), N, K, _p(q), _p(s), M, _p(y)) != 0:
         raise ValueError("bad shape")
     return y

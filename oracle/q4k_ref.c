@@ -296,3 +296,42 @@ int q4k_ref_moe_ffn(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w
     free(g); free(u); free(h); free(out);
     return rc;
 }
+
+void q4k_ref_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int8_t *q, float *s) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < K / 32; ++b) {
+            const uint16_t *xb = x + m * K + 32 * b;
+            float a = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                const float v = fabsf(q4k_ref_bf16_to_f32(xb[i]));
+                if (v > a) a = v;
+            }
+            const float sc = a / 127.0f;
+            s[m * (K / 32) + b] = sc;
+            for (int i = 0; i < 32; ++i) {
+                float r = 0.0f;
+                if (a > 0.0f) r = rintf(q4k_ref_bf16_to_f32(xb[i]) / sc);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                q[m * K + 32 * b + i] = (int8_t)r;
+            }
+        }
+}
+
+int q4k_ref_gemm_x8(const uint8_t *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, double *y) {
+    if (!shape_ok(N, K) || M < 0) return -1;
+    float *wrow = (float *)malloc(sizeof(float) * (size_t)K);
+    if (!wrow) return -2;
+    const int64_t row_bytes = (K / QK) * BB;
+    for (int64_t n = 0; n < N; ++n) {
+        q4k_ref_dequant(w + n * row_bytes, 1, K, wrow);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)wrow[k] * ((double)s[m * (K / 32) + k / 32] * (double)q[m * K + k]);
+            y[m * N + n] = acc;
+        }
+    }
+    free(wrow);
+    return 0;
+}

@@ -79,6 +79,20 @@ int q4k_ref_moe_slots(const uint8_t *w_experts, int32_t E, int64_t N, int64_t K,
 /* y[T][N] = sum_{j=0..topk-1} gates[t][j] * out[t][j][:], in j order, fp64 */
 void q4k_ref_moe_combine(const double *out, const float *gates, int64_t T, int32_t topk, int64_t N, double *y);
 
+/* int8 activations (sparkinfer-server README, "Determinism": the pipeline
+ * requantizes activations to int8 at each layer).  The pages do not give the
+ * format; the reading taken: blocks of 32 consecutive elements of a row (the
+ * span of one Q4_K sub-block), in fp32 arithmetic:
+ *     a = max |x_i|,  s = a / 127,  q_i = rint(x_i / s)  (ties to even),
+ * and q_i = 0, s = 0 for an all-zero block.  |q_i| <= 127.  x is [M][K] bf16,
+ * q [M][K], s [M][K/32].  K must be a multiple of 32. */
+void q4k_ref_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int8_t *q, float *s);
+
+/* y[m][n] = sum_k w[n][k] * xh[m][k] with xh[m][k] = s[m][k/32] * q[m][k], the
+ * dequantized int8 activations, in fp64 over the fp32 dequantized weights.
+ * Returns 0, or -1 on a bad shape. */
+int q4k_ref_gemm_x8(const uint8_t *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, double *y);
+
 /* Round a double to the nearest bf16 (ties to even), once; returns its bits.
  * Finite normal range only (|v| from 2^-126 to the bf16 maximum, or 0). */
 uint16_t q4k_ref_f64_to_bf16(double v);

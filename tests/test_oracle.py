@@ -9,7 +9,10 @@
   - one-hot and all-ones activations (closed forms);
   - MoE routing vs Python's stable sort, slots and combine vs numpy;
   - the routed SwiGLU layer vs its pinned pieces, scipy's logistic function and an
-    exact-rational bf16 rounding.
+    exact-rational bf16 rounding;
+  - int8 activations: quantization invariants, exact ties, sign and power-of-two
+    symmetries; the int8 GEMM equals the pinned GEMM where the dequantized
+    activations are exact in bf16, and exact rationals on a small case.
 """
 from fractions import Fraction
 
@@ -333,6 +336,88 @@ def test_moe_ffn_vs_pinned_pieces(ref, syn):
     want = ref.moe_combine(out, gates)
     assert np.allclose(y, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
     assert np.any(h != 0) and np.abs(y).max() > 0
+
+
+
+# ------------------------------------------------------------ int8 activations
+
+def _to_bf16_bits(vals):
+    """Exactly bf16-representable float values -> bf16 bits (asserts exactness)."""
+    f = np.asarray(vals, dtype=np.float32)
+    u = f.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0)
+    return (u >> 16).astype(np.uint16)
+
+
+def test_quantize_x8_invariants(ref, syn):
+    M, K = 3, 1024
+    x = syn.normal_bf16(41, M * K).reshape(M, K).copy()
+    x[0, 32:64] = 0                                            # all-zero block
+    x[1, 64:96] = _to_bf16_bits(-np.abs(bf16_bits_to_f64(x[1, 64:96])))  # all negative
+    x[2, 96:128] = 0
+    x[2, 100] = _to_bf16_bits([3.0])[0]                        # a single non-zero
+    q, sc = ref.quantize_x8(x)
+    xf = bf16_bits_to_f64(x)
+    assert q.dtype == np.int8 and np.abs(q.astype(np.int32)).max() <= 127
+    for m in range(M):
+        for b in range(K // 32):
+            blk, qb, s = xf[m, 32 * b:32 * b + 32], q[m, 32 * b:32 * b + 32].astype(np.int64), float(sc[m, b])
+            a = np.abs(blk).max()
+            if a == 0:
+                assert s == 0 and np.all(qb == 0)
+                continue
+            assert abs(s - a / 127) <= a / 127 * 2.0 ** -23        # the scale is a/127 to fp32 precision
+            i = int(np.argmax(np.abs(blk)))
+            assert qb[i] == (127 if blk[i] > 0 else -127)           # the largest element maps to +-127
+            # nearest integer to x/s, up to the fp32 rounding of x/s (|x/s| <= 127: 127 * 2^-24)
+            assert np.all(np.abs(blk - s * qb) <= s * (0.5 + 2.0 ** -16))
+            assert np.all(np.sign(qb) * np.sign(blk) >= 0)
+    assert np.all(q[2, 96:128][np.arange(32) != 4] == 0) and q[2, 100] == 127
+
+
+def test_quantize_x8_ties_to_even_and_symmetries(ref, syn):
+    # a block whose largest magnitude is 127 * 2^-3: s = 2^-3 exactly, so k.5 * s are exact ties
+    vals = np.zeros(32)
+    vals[0] = 127 * 0.125
+    vals[1:9] = np.array([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5]) * 0.125
+    x = _to_bf16_bits(vals).reshape(1, 32)
+    q, sc = ref.quantize_x8(x)
+    assert float(sc[0, 0]) == 0.125
+    assert list(q[0, :9]) == [127, 0, 2, 2, 4, 0, -2, -2, 126]
+    # q(-x) = -q(x), s(-x) = s(x); q(2x) = q(x), s(2x) = 2 s(x)
+    y = syn.normal_bf16(43, 2 * 256).reshape(2, 256)
+    q1, s1 = ref.quantize_x8(y)
+    q2, s2 = ref.quantize_x8(y ^ np.uint16(0x8000))
+    assert np.array_equal(q2, -q1) and np.array_equal(s2, s1)
+    y2 = _to_bf16_bits(2.0 * bf16_bits_to_f64(y))
+    q3, s3 = ref.quantize_x8(y2)
+    assert np.array_equal(q3, q1) and np.array_equal(s3, 2 * s1)
+
+
+def test_gemm_x8_equals_gemm_on_exact_activations(ref, syn):
+    # power-of-two scales make s * q exact in bf16, so the int8 GEMM must give the
+    # pinned bf16 GEMM's result on those activations, bit for bit
+    N, K, M = 7, 768, 3
+    w = syn.weights(44, N, K)
+    rng = np.random.default_rng(45)
+    q = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    sc = np.ldexp(1.0, rng.integers(-9, 2, size=(M, K // 32))).astype(np.float32)
+    xh = np.repeat(sc, 32, axis=1).astype(np.float64) * q
+    got = ref.gemm_x8(w, N, K, q, sc)
+    want = ref.gemm(w, N, K, _to_bf16_bits(xh))
+    assert np.array_equal(got, want)
+
+
+def test_gemm_x8_exact_rational(ref, syn):
+    N, K = 2, 512
+    w = syn.weights(46, N, K)
+    x = syn.normal_bf16(47, K).reshape(1, K)
+    q, sc = ref.quantize_x8(x)
+    wd = ref.dequant(w, N, K)
+    got = ref.gemm_x8(w, N, K, q, sc)
+    for n in range(N):
+        exact = sum(Fraction(float(wd[n, k])) * Fraction(float(sc[0, k // 32])) * int(q[0, k]) for k in range(K))
+        assert abs(Fraction(float(got[0, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 40) + Fraction(1, 2 ** 60)
 
 
 # ------------------------------------------------------------ input module

@@ -36,6 +36,10 @@ MUTANTS = {
     "ffn_no_silu": ("g[i] / (1.0 + exp(-g[i])) * u[i]", "g[i] * u[i]"),
     "ffn_down_reads_token_rows": ("rc = q4k_ref_moe_slots(w_down, E, D, H, h, 1, ids, T, topk, out, threads);",
                                   "rc = q4k_ref_moe_slots(w_down, E, D, H, h, 0, ids, T, topk, out, threads);"),
+    "x8_ties_away": ("if (a > 0.0f) r = rintf(", "if (a > 0.0f) r = roundf("),
+    "x8_scale_128": ("const float sc = a / 127.0f;", "const float sc = a / 128.0f;"),
+    "x8_signed_max": ("const float v = fabsf(q4k_ref_bf16_to_f32(xb[i]));", "const float v = q4k_ref_bf16_to_f32(xb[i]);"),
+    "x8_scale_block": ("(double)s[m * (K / 32) + k / 32]", "(double)s[m * (K / 32) + ((k / 32) ^ 1)]"),
 }
 
 
