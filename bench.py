@@ -12,7 +12,8 @@ speculative-verify GEMM, K 5120 -> N 17408, --m, default 4), `prefill` (M x K
 `moe` (128 experts, top-8: gate, up and down with the weighted combine, --m
 tokens, default 2048) and `moe_ffn` (the same layer as one routed SwiGLU expert
 feed-forward call: gate, up with the SwiGLU epilogue, down on the bf16 h rows,
-weighted combine).
+weighted combine), and `decode_x8` (the decode step with int8 activations:
+per-32 quantization of each matrix's input, then the int8 GEMV).
 
 Timing: W warm-up steps, then exactly K steps between a barrier plus
 cudaDeviceSynchronize on both sides, timed with CUDA events on the launching
@@ -164,12 +165,17 @@ class Workload:
         self.np = np
         self.mats = []   # list of (tag, N, K, M, blocks, x) for dense GEMM steps
         self.moe = None
-        if name == "decode":
+        self.x8 = name == "decode_x8"
+        if name in ("decode", "decode_x8"):
             self.mats = [("gate_up", 17408, 5120, 1, synth.weights(synth.seed(1, 0), 17408, 5120),
                           synth.normal_bf16(synth.seed(1, 1), 5120).reshape(1, 5120)),
                          ("down", 5120, 17408, 1, synth.weights(synth.seed(1, 5), 5120, 17408),
                           synth.normal_bf16(synth.seed(1, 6), 17408).reshape(1, 17408))]
             self.unit, self.config = "GB/s", {"workload": "decode GEMV M=1: K5120->N17408 then K17408->N5120"}
+            if self.x8:
+                self.config = {"workload": "decode GEMV M=1 with int8 activations (per-32 scales, quantized in "
+                                           "the step): K5120->N17408 then K17408->N5120"}
+                self.mats = [(tag + "_x8",) + tuple(rest) for (tag, *rest) in self.mats]
         elif name == "verify":
             self.mats = [("verify", 17408, 5120, m, synth.weights(synth.seed(2, 0), 17408, 5120),
                           synth.normal_bf16(synth.seed(2, 1), m * 5120).reshape(m, 5120))]
@@ -256,9 +262,13 @@ class GpuRunner:
             base = [d(b) for (_, _, _, _, b, _) in wl.mats]
             for r in range(self.R):
                 self.sets.append(base if r == 0 else [t.clone() for t in base])
+            self.q, self.sx = [], []
             for (_, N, K, M, _, x) in wl.mats:
                 self.x.append(d(x))
                 self.y.append(torch.empty((M, N), dtype=torch.float32, device=device))
+                if wl.x8:
+                    self.q.append(torch.empty((M, K), dtype=torch.int8, device=device))
+                    self.sx.append(torch.empty((M, K // 32), dtype=torch.float32, device=device))
                 wsb = q4k.q4k_gemm_workspace_size(M, N, K)
                 self.ws.append((torch.empty(max(wsb, 1), dtype=torch.uint8, device=device), wsb))
 
@@ -274,13 +284,15 @@ class GpuRunner:
             if mo["ffn"]:
                 return route + (1 if tc else 0) + 3 + 1
             return route + 3 * (2 if tc else 1) + 1
-        return len(self.wl.mats)  # one kernel per matrix
+        return len(self.wl.mats) * (2 if self.wl.x8 else 1)  # per matrix: (quantize +) GEMV
 
     def step_one(self, r: int, i: int):
         """Enqueue only matrix i of the step, with weight set r."""
         q4k, wl = self.q4k, self.wl
         _, N, K, M, _, _ = wl.mats[i]
-        if M == 1:
+        if wl.x8:
+            q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N)
+        elif M == 1:
             q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i])
         else:
             ws, wsb = self.ws[i]
@@ -315,7 +327,10 @@ class GpuRunner:
         for i, (_, N, K, M, _, _) in enumerate(wl.mats):
             if mark:
                 mark(i)
-            if M == 1:
+            if wl.x8:
+                q4k.q4k_quantize_x8(self.x[i], M, K, K, self.q[i], self.sx[i])
+                q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N)
+            elif M == 1:
                 q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i])
             else:
                 ws, wsb = self.ws[i]
@@ -466,7 +481,8 @@ def run_gpu(args, rank, local_rank, world):
     line = {
         "metric": METRIC, "value": wl.value(sec_per_step) * world, "unit": wl.unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x Q4_K -> fp32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 (per-32 fp32 scales) x Q4_K -> fp32" if wl.x8 else "bf16 x Q4_K -> fp32",
         "data": "synthetic (seeded N(0,0.02^2) weights quantized to Q4_K; N(0,1) bf16 activations)",
         "config": dict(wl.config, l2="rotating %d weight sets, %.0f MB total > 129 MB L2" %
                        (gr.R, gr.R * (wl.weight_bytes() if not wl.moe else sum(
@@ -486,7 +502,7 @@ def run_gpu(args, rank, local_rank, world):
                                 "frac": ach / bf16, "traffic": profiled_traffic(tag), "kernel": tag,
                                 "kernel_us": kernel_ms[i_dom] * 1e3, "peak_source": src + " (burst)"}
         else:
-            algo = N * K * 144 / 256 + M * K * 2 + M * N * 4
+            algo = N * K * 144 / 256 + (M * K + M * K // 32 * 4 if wl.x8 else M * K * 2) + M * N * 4
             ach = algo / (kernel_ms[i_dom] / 1e3) / 1e9
             line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                                 "traffic": profiled_traffic(tag), "kernel": tag,
@@ -578,13 +594,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "verify", "prefill", "moe", "moe_ffn"], default="decode")
+    ap.add_argument("--workload", choices=["decode", "decode_x8", "verify", "prefill", "moe", "moe_ffn"],
+                    default="decode")
     ap.add_argument("--m", type=int, default=None, help="tokens (verify: 4, prefill: 4096, moe: 2048)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.m is None:
-        args.m = {"decode": 1, "verify": 4, "prefill": 4096, "moe": 2048, "moe_ffn": 2048}[args.workload]
+        args.m = {"decode": 1, "decode_x8": 1, "verify": 4, "prefill": 4096, "moe": 2048,
+                  "moe_ffn": 2048}[args.workload]
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, local_rank, world = env_rank()

@@ -152,6 +152,32 @@ size_t q4k_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M, int64_t ldx, float *y,
                     int64_t ldy, void *ws, size_t ws_bytes, void *stream);
 
+/* -------------------------------------------------------- int8 activations --
+ * The pages' serving pipeline requantizes activations to int8 at each layer
+ * (sparkinfer-server README, "Determinism"); their format is not given.  The
+ * reading taken: blocks of 32 consecutive elements of a row (one Q4_K
+ * sub-block's span), in fp32: a = max |x|, s = a / 127, q = rint(x / s) with
+ * ties to even, and q = 0, s = 0 for an all-zero block.
+ *
+ * q4k_quantize_x8: x -> (q, s).
+ *   x  device bf16 [M][ldx], ldx >= K, 4-byte aligned
+ *   q  device int8 [M][K], dense, 16-byte aligned
+ *   s  device fp32 [M][K/32], dense, 16-byte aligned
+ * Bit-exact: every q and s follows from the IEEE round-to-nearest divisions
+ * above.  Errors: NULL, SHAPE (M < 1, K not a positive multiple of 256,
+ * ldx < K), ALIGN, DEVICE, CUDA. */
+q4k_status q4k_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q, float *s, void *stream);
+
+/* q4k_gemm_x8: y = xh . W^T for M in [1, 16] tokens, where xh[m][k] =
+ * s[m][k/32] * q[m][k] are the int8 activations (layouts as q4k_quantize_x8).
+ * The integer dot products of each 32-weight sub-block are exact; the scaling
+ * and accumulation are fp32.  y: fp32 [M][ldy], ldy >= N, 4-byte aligned.
+ * Batch-invariant like q4k_gemm: row m of the result does not depend on M.
+ * Errors: NULL, SHAPE (M outside [1, 16], N < 1, bad K, ldy < N), ALIGN,
+ * DEVICE, CUDA. */
+q4k_status q4k_gemm_x8(const void *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, float *y,
+                       int64_t ldy, void *stream);
+
 /* --------------------------------------------------------------------- MoE --
  * Routed-expert layer over E experts, each an N x K Q4_K matrix; the pages' MoE
  * models route each token to its top-k experts and combine the experts' outputs

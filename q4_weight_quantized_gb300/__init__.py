@@ -27,7 +27,7 @@ EXPORTS = (
     "q4k_status_string", "q4k_last_cuda_error", "q4k_row_bytes", "q4k_version", "q4k_check_device",
     "q4k_set_static_weights", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
     "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_reuse_routing",
-    "q4k_moe_grouped_gemm_noalloc", "q4k_moe_ffn_workspace_size", "q4k_moe_ffn",
+    "q4k_moe_grouped_gemm_noalloc", "q4k_moe_ffn_workspace_size", "q4k_moe_ffn", "q4k_quantize_x8", "q4k_gemm_x8",
 )
 
 # fixed scratch capacity of q4k_moe_grouped_gemm_noalloc (Q4K_MOE_NOALLOC_SCRATCH_BYTES)
@@ -73,6 +73,8 @@ def load(path: str | None = None):
         "q4k_moe_grouped_gemm_noalloc": ([P, i32, i64, i64, P, st, P, P, i64, i32, P, st, P], st),
         "q4k_moe_ffn_workspace_size": ([i32, i64, i64, i64, i32], sz),
         "q4k_moe_ffn": ([P, P, P, i32, i64, i64, P, P, P, i64, i32, P, P, sz, P], st),
+        "q4k_quantize_x8": ([P, i64, i64, i64, P, P, P], st),
+        "q4k_gemm_x8": ([P, i64, i64, P, P, i64, P, i64, P], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -205,3 +207,13 @@ def q4k_moe_ffn(w_gate, w_up, w_down, n_experts: int, H: int, D: int, x, topk_id
     _check(load().q4k_moe_ffn(_ptr(w_gate), _ptr(w_up), _ptr(w_down), n_experts, H, D, _ptr(x), _ptr(topk_ids),
                               _ptr(gates), T, topk, _ptr(y), _ptr(ws), ws_bytes, _stream(stream)),
            "q4k_moe_ffn")
+
+
+def q4k_quantize_x8(x, M: int, K: int, ldx: int, q, s, stream=None) -> None:
+    """Per-32 int8 quantization of bf16 rows: q int8 [M][K], s fp32 [M][K/32]."""
+    _check(load().q4k_quantize_x8(_ptr(x), M, K, ldx, _ptr(q), _ptr(s), _stream(stream)), "q4k_quantize_x8")
+
+
+def q4k_gemm_x8(w, N: int, K: int, q, s, M: int, y, ldy: int, stream=None) -> None:
+    """y = (s * q) . W^T over int8 activations, M in [1, 16]."""
+    _check(load().q4k_gemm_x8(_ptr(w), N, K, _ptr(q), _ptr(s), M, _ptr(y), ldy, _stream(stream)), "q4k_gemm_x8")

@@ -155,6 +155,12 @@ cudaError_t make_act_tmap(CUtensorMap *m, const void *x, int64_t rows, int64_t K
     return encode_cached(m, k, CU_TENSOR_MAP_DATA_TYPE_UINT64, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+cudaError_t make_bytes_tmap(CUtensorMap *m, const void *p, int64_t rows, int64_t row_bytes, int64_t pitch,
+                            int box_bytes) {
+    const TmapKey k = {p, row_bytes / 8, rows, pitch, box_bytes / 8, 1, 3};
+    return encode_cached(m, k, CU_TENSOR_MAP_DATA_TYPE_UINT64, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // Activations [rows][ld] bf16 for the tensor-core path: dims {K, rows}, box {64,
 // box_rows}, 128-byte swizzle (the K-major operand layout tcgen05.mma reads).
 cudaError_t make_act_tmap_sw128(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_rows) {
@@ -270,6 +276,31 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
     cudaError_t e;
     if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, g_static_weights.load(std::memory_order_relaxed) != 0, s);
     else e = launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, s);
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+q4k_status q4k_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q, float *s, void *stream) {
+    if (!x || !q || !s) return Q4K_ERR_NULL;
+    if (M < 1 || !k_ok(K) || ldx < K || M > ((int64_t)1 << 31) - 1) return Q4K_ERR_SHAPE;
+    if (!aligned(x, 4) || !aligned(q, 16) || !aligned(s, 16)) return Q4K_ERR_ALIGN;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaError_t e = launch_quantize_x8(di, x, M, K, ldx, q, s, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+q4k_status q4k_gemm_x8(const void *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, float *y,
+                       int64_t ldy, void *stream) {
+    if (!w || !q || !s || !y) return Q4K_ERR_NULL;
+    if (M < 1 || M > 16 || N < 1 || !k_ok(K) || ldy < N || N > ((int64_t)1 << 31) - 1) return Q4K_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(q, 16) || !aligned(s, 16) || !aligned(y, 4)) return Q4K_ERR_ALIGN;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaError_t e = launch_smallm_x8(di, w, N, K, q, s, M, y, ldy,
+                                     g_static_weights.load(std::memory_order_relaxed) != 0,
+                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 

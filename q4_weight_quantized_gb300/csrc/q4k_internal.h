@@ -32,6 +32,15 @@ cudaError_t launch_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *o
 cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                           int64_t ldx, float *y, int64_t ldy, bool early_weights, cudaStream_t s);
 
+// M in [1, 16] with int8 activations: q [M][K] int8 and sx [M][K/32] fp32 scales,
+// both dense and 16-byte aligned (smallm.cu, int8 mode).
+cudaError_t launch_smallm_x8(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const int8_t *q,
+                             const float *sx, int64_t M, float *y, int64_t ldy, bool early_weights, cudaStream_t s);
+
+// Per-32 int8 quantization of bf16 rows (x8.cu).
+cudaError_t launch_quantize_x8(const DeviceInfo &di, const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q,
+                               float *sx, cudaStream_t s);
+
 // M > 16: per-tile dequantization into shared memory + tcgen05 MMA (gemm_tc.cu)
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
@@ -145,6 +154,10 @@ cudaError_t make_weight_tmap(CUtensorMap *m, const void *w, int64_t N, int64_t K
 // TMA descriptor of bf16 activations [rows][ld] viewed as uint64 (4 activations
 // each): dims {K/4, rows}, box {box_elems, 1} = one row segment of 4*box_elems.
 cudaError_t make_act_tmap(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_elems);
+// Rows of raw bytes [rows][pitch] (row_bytes used) as a 2-D uint64 tensor: box
+// {box_bytes / 8, 1 row}.  row_bytes, pitch and box_bytes multiples of 16.
+cudaError_t make_bytes_tmap(CUtensorMap *m, const void *p, int64_t rows, int64_t row_bytes, int64_t pitch,
+                            int box_bytes);
 
 // bf16 activations [rows][ld], box {64, box_rows}, 128-byte swizzle (tcgen05 operand)
 cudaError_t make_act_tmap_sw128(CUtensorMap *m, const void *x, int64_t rows, int64_t K, int64_t ld, int box_rows);

@@ -78,14 +78,17 @@ struct Geo {
     static_assert(kRedBytes <= kWarps * 2 * slot_bytes(1), "dense reduction buffers alias the rings");
 };
 
+// F16: fp16 pairs 1024 + q (magic 0x6400) instead of bf16 pairs 128 + q (0x4300).
+template <bool F16 = false>
 __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t &lo23, uint32_t &hi01,
                                             uint32_t &hi23) {
+    constexpr uint32_t kMagic = F16 ? 0x64006400u : 0x43004300u;
     const uint32_t t01 = prmt(w, 0u, 0x4140u);  // bytes 0,1 -> 16-bit lanes
     const uint32_t t23 = prmt(w, 0u, 0x4342u);  // bytes 2,3
-    lo01 = lop3_and_or(t01, 0x000F000Fu, 0x43004300u);
-    lo23 = lop3_and_or(t23, 0x000F000Fu, 0x43004300u);
-    hi01 = lop3_and_or(t01 >> 4, 0x000F000Fu, 0x43004300u);
-    hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
+    lo01 = lop3_and_or(t01, 0x000F000Fu, kMagic);
+    lo23 = lop3_and_or(t23, 0x000F000Fu, kMagic);
+    hi01 = lop3_and_or(t01 >> 4, 0x000F000Fu, kMagic);
+    hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, kMagic);
 }
 
 // byte i of w as an fp32 2^23 + byte (exponent 150, the byte in the low mantissa bits)
@@ -94,8 +97,9 @@ __device__ __forceinline__ float byte_magic(uint32_t w, int i) {
 }
 
 // Decode one row's block header (d, dmin, 12 scale bytes) into 8 (d*sc, bias)
-// pairs, bias = 128*d*sc + dmin*m.  d*sc and dmin*m are exact: fma(2^23+b, d,
-// -2^23*d) rounds d*b, which has at most 17 significant bits.
+// pairs, bias = 128*d*sc + dmin*m (MIN: bias = dmin*m).  d*sc and dmin*m are
+// exact: fma(2^23+b, d, -2^23*d) rounds d*b, which has at most 17 significant bits.
+template <bool MIN = false>
 __device__ __forceinline__ void decode_scales(const uint8_t *blk, float *table_row) {
     const uint4 h = *reinterpret_cast<const uint4 *>(blk);
     const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
@@ -111,7 +115,7 @@ __device__ __forceinline__ void decode_scales(const uint8_t *blk, float *table_r
         const float dsc = fmaf(byte_magic(j < 4 ? sc_lo : sc_hi, j & 3), d, nd);
         const float dm = fmaf(byte_magic(j < 4 ? m_lo : m_hi, j & 3), dmin, ndm);
         v[2 * j] = dsc;
-        v[2 * j + 1] = fmaf(128.0f, dsc, dm);
+        v[2 * j + 1] = MIN ? dm : fmaf(128.0f, dsc, dm);
     }
     float4 *dst = reinterpret_cast<float4 *>(table_row);
 #pragma unroll
@@ -194,6 +198,96 @@ __device__ __forceinline__ void block_mma(const uint8_t *wst, const uint8_t *xs,
     }
 }
 
+// int8 activations (slot: 256 int8 values, then the block's 8 fp32 scales, per
+// token).  The fragment walk of block_mma with fp16 operands: A = 1024 + q and
+// B = the int8 values, both exact in fp16, so C = sum (1024 + q) x and S = sum x
+// are exact integers (below 2^24) in the fp32 accumulators.  Per 32-weight
+// sub-block s: acc += s_x * (d sc_s (C - 1024 S) - dmin m_s S), s_x being the
+// activation block's scale; C - 1024 S = sum q x is formed exactly first.
+template <int NT, bool ONE, int RT>
+__device__ __forceinline__ void block_mma_x8(const uint8_t *wst, const uint8_t *xs, const float *table,
+                                             const bool (&live)[NT], int nvalid, float (&acc)[RT][NT][4], int r,
+                                             int c) {
+    constexpr int kRowTiles = RT;
+    const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    const __half2 k1152 = __float2half2_rn(1152.0f);
+    // int8 pair -> fp16 pair holding the exact value: (b ^ 0x80) = b + 128 in 0..255
+    // as the low mantissa byte of 1024.0 (0x64xx), minus 1152
+    auto cvt = [&](uint32_t u, uint32_t sel) -> uint32_t {
+        const uint32_t h = prmt(u, 0x64646464u, sel);
+        const __half2 v = __hsub2(*reinterpret_cast<const __half2 *>(&h), k1152);
+        return *reinterpret_cast<const uint32_t *>(&v);
+    };
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint32_t xl[NT][4], xh[NT][4];
+        float sl[NT][4], sh[NT][4];
+        float2 s0[NT], s1[NT];  // scales of sub-blocks (2g, 2g+1) for tokens 2c and 2c+1 of the tile
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            uint2 a = make_uint2(0, 0), b = make_uint2(0, 0);
+            s0[nt] = make_float2(0.f, 0.f);
+            s1[nt] = make_float2(0.f, 0.f);
+            if (live[nt]) {
+                const uint8_t *xp = xs + (nt * 8 + r) * kXBlkBytes + 64 * g + 8 * c;
+                a = *reinterpret_cast<const uint2 *>(xp);       // sub-block 2g, elements 8c..8c+7
+                b = *reinterpret_cast<const uint2 *>(xp + 32);  // sub-block 2g+1
+            }
+            // only the slot's tokens have scales (the others get 0: their x is 0 too)
+            const int t0 = nt * 8 + 2 * c;
+            const uint8_t *sp = xs + t0 * kXBlkBytes + 256 + 8 * g;
+            if (t0 < nvalid) s0[nt] = *reinterpret_cast<const float2 *>(sp);
+            if (!ONE && t0 + 1 < nvalid) s1[nt] = *reinterpret_cast<const float2 *>(sp + kXBlkBytes);
+            const uint32_t a0 = a.x ^ 0x80808080u, a1 = a.y ^ 0x80808080u;
+            const uint32_t b0 = b.x ^ 0x80808080u, b1 = b.y ^ 0x80808080u;
+            xl[nt][0] = cvt(a0, 0x5140u); xl[nt][1] = cvt(a0, 0x7362u);
+            xl[nt][2] = cvt(a1, 0x5140u); xl[nt][3] = cvt(a1, 0x7362u);
+            xh[nt][0] = cvt(b0, 0x5140u); xh[nt][1] = cvt(b0, 0x7362u);
+            xh[nt][2] = cvt(b1, 0x5140u); xh[nt][3] = cvt(b1, 0x7362u);
+            mma_f16_16816(sl[nt], ones, xl[nt][0], xl[nt][1], zero4);
+            mma_f16_16816(sl[nt], ones, xl[nt][2], xl[nt][3], sl[nt]);
+            mma_f16_16816(sh[nt], ones, xh[nt][0], xh[nt][1], zero4);
+            mma_f16_16816(sh[nt], ones, xh[nt][2], xh[nt][3], sh[nt]);
+        }
+#pragma unroll
+        for (int rt = 0; rt < kRowTiles; ++rt) {
+            const int rA = rt * 16 + r, rB = rA + 8;
+            const uint2 wa = *reinterpret_cast<const uint2 *>(wst + rA * kBlockBytes + 16 + 32 * g + 8 * c);
+            const uint2 wb = *reinterpret_cast<const uint2 *>(wst + rB * kBlockBytes + 16 + 32 * g + 8 * c);
+            uint32_t alo0[4], alo1[4], ahi0[4], ahi1[4];
+            unpack_word<true>(wa.x, alo0[0], alo0[2], ahi0[0], ahi0[2]);
+            unpack_word<true>(wb.x, alo0[1], alo0[3], ahi0[1], ahi0[3]);
+            unpack_word<true>(wa.y, alo1[0], alo1[2], ahi1[0], ahi1[2]);
+            unpack_word<true>(wb.y, alo1[1], alo1[3], ahi1[1], ahi1[3]);
+            // (d sc, dmin m) of sub-blocks 2g and 2g+1
+            const float4 sa = *reinterpret_cast<const float4 *>(table + rA * (kTableRowBytes / 4) + 4 * g);
+            const float4 sb = *reinterpret_cast<const float4 *>(table + rB * (kTableRowBytes / 4) + 4 * g);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float cl[4], chh[4];
+                mma_f16_16816(cl, alo0, xl[nt][0], xl[nt][1], zero4);
+                mma_f16_16816(cl, alo1, xl[nt][2], xl[nt][3], cl);
+                mma_f16_16816(chh, ahi0, xh[nt][0], xh[nt][1], zero4);
+                mma_f16_16816(chh, ahi1, xh[nt][2], xh[nt][3], chh);
+                float *a4 = acc[rt][nt];
+                // element e: row rA (e < 2) or rB, token 2c + (e & 1)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (ONE && (e & 1)) continue;
+                    const float4 &sw = e < 2 ? sa : sb;
+                    const float2 &sx = (e & 1) ? s1[nt] : s0[nt];
+                    const float dl = fmaf(-1024.0f, sl[nt][e], cl[e]);   // sum q x, sub-block 2g
+                    const float dh = fmaf(-1024.0f, sh[nt][e], chh[e]);  // sub-block 2g+1
+                    a4[e] = fmaf(sx.x, fmaf(sw.x, dl, -sw.y * sl[nt][e]), a4[e]);
+                    a4[e] = fmaf(sx.y, fmaf(sw.z, dh, -sw.w * sh[nt][e]), a4[e]);
+                }
+            }
+        }
+    }
+}
+
+
 // Where each token slot of a chunk reads its activation row and writes its
 // output row.  Dense: slot n is token n.  MoE: slot n of a token tile is the
 // (token, k-slot) item perm[first + n], first being the tile's first position
@@ -247,7 +341,7 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // split rows instead of K - warp w owns rows w*ROWS.. of a 4*ROWS-row CTA over
 // all K blocks and stores its own outputs, with no cross-warp reduction.  CH:
 // token slots per chunk (at most 8 * NT; fewer shrinks the activation part of a
-// slot when experts get few items).  GLU (MoE): the gate (tmW) and up (tmW2)
+// slot when experts get few items).  GLU (MoE): the gate (tmW) and up (tmAux)
 // projections of an expert FFN in one pass - warps 0-1 take the gate matrix,
 // warps 2-3 the up matrix, for the same rows (row split: a 2*ROWS-row CTA, the
 // pairs owning ROWS rows each; K split: each pair splits K) - and the epilogue
@@ -256,10 +350,13 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // takes the token's slots w, w+4, ... whole (all K blocks of its expert's rows),
 // and the CTA sums g[t][j] * out[t][j] over j in increasing order into y[t]:
 // the weighted combine, in the CTA, with the bits of the separate combine pass.
+// X8 (dense): int8 activations with per-32 fp32 scales (tmX: the int8 rows,
+// tmAux: the scale rows), multiplied through block_mma_x8.
+// tmAux: GLU: the up matrix; X8: the activation scales; otherwise unused.
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
-          bool DC = false>
+          bool DC = false, bool X8 = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                          const __grid_constant__ CUtensorMap tmW2,
+                                                          const __grid_constant__ CUtensorMap tmAux,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
                                                           int KB, int nx, unsigned int *status) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -277,10 +374,13 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     static_assert(!RS || (MOE && ROWS == 32), "row split is a MoE mode");
     static_assert(!GLU || MOE, "the fused gate and up projections are a MoE mode");
     static_assert(!DC || (MOE && !RS && !GLU && NT == 1 && ONE), "the in-CTA combine is a one-token MoE mode");
+    static_assert(!X8 || !MOE, "int8 activations are a dense mode");
+    // activation bytes copied per token slot and block: 512 bf16, or 256 int8 + 32 of scales
+    constexpr int kXTx = X8 ? 256 + 32 : kXBlkBytes;
     // GLU: the warp pair of matrix `mat` (0 gate, 1 up); wsub = this warp's index in its pair
     constexpr int kNw = GLU ? 2 : kWarps;  // warps per weight matrix
     const int mat = GLU ? warp >> 1 : 0, wsub = GLU ? warp & 1 : warp;
-    const CUtensorMap *tw = mat ? &tmW2 : &tmW;
+    const CUtensorMap *tw = mat ? &tmAux : &tmW;
     const int row0 = blockIdx.y * kRows * (RS ? kNw : 1);
     const int wrow0 = row0 + (RS ? wsub * kRows : 0);  // this warp's first row
     const int kb0 = (int)((int64_t)KB * split / S), kb1 = (int)((int64_t)KB * (split + 1) / S);
@@ -358,7 +458,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             if (ra.early_w)
                 for (int it = 0; it < SLOTS && it < total; ++it) {
                     const uint32_t bar = bar0 + 8 * (it % SLOTS);
-                    mbar_arrive_expect_tx(bar, kBlkWBytes + min(kPerChunk, cnt) * kXBlkBytes);
+                    mbar_arrive_expect_tx(bar, kBlkWBytes + min(kPerChunk, cnt) * kXTx);
                     tma_load_2d(smem_u32(region + (it % SLOTS) * sbytes), tw, (kb_first + kb_step * it) * kBlkWords,
                                 tma_row, bar);
                 }
@@ -386,11 +486,19 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         }
         const uint32_t dst = smem_u32(region + slot * sbytes);
         if (lane == 0 && weights) {
-            mbar_arrive_expect_tx(bar0 + 8 * slot, kBlkWBytes + nvalid * kXBlkBytes);
+            mbar_arrive_expect_tx(bar0 + 8 * slot, kBlkWBytes + nvalid * kXTx);
             tma_load_2d(dst, tw, kb * kBlkWords, row_w, bar0 + 8 * slot);
         }
         __syncwarp();
-        if (lane < nvalid) tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes, &tmX, kb * (kQK / 4), xrow, bar0 + 8 * slot);
+        if (lane < nvalid) {
+            if constexpr (X8) {
+                // 256 int8 values (32 x 8-byte elements), then the 8 scales (4 x 8 bytes)
+                tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes, &tmX, kb * (kQK / 8), xrow, bar0 + 8 * slot);
+                tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes + 256, &tmAux, kb * 4, xrow, bar0 + 8 * slot);
+            } else {
+                tma_load_2d(dst + kBlkWBytes + lane * kXBlkBytes, &tmX, kb * (kQK / 4), xrow, bar0 + 8 * slot);
+            }
+        }
     };
 
     const bool early = !MOE && ra.early_w;
@@ -421,13 +529,16 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             }
             const uint8_t *wst = region + slot * sbytes;
             const uint8_t *xs = wst + kBlkWBytes;
-            decode_scales(wst + lane * kBlockBytes, table + lane * (kTableRowBytes / 4));
+            decode_scales<X8>(wst + lane * kBlockBytes, table + lane * (kTableRowBytes / 4));
             if constexpr (kRows > 32) {
                 if (lane < kRows - 32)
-                    decode_scales(wst + (lane + 32) * kBlockBytes, table + (lane + 32) * (kTableRowBytes / 4));
+                    decode_scales<X8>(wst + (lane + 32) * kBlockBytes, table + (lane + 32) * (kTableRowBytes / 4));
             }
             __syncwarp();
-            block_mma<NT, ONE, kRowTiles>(wst, xs, table, live, acc, r, c);
+            if constexpr (X8)
+                block_mma_x8<NT, ONE, kRowTiles>(wst, xs, table, live, nvalid, acc, r, c);
+            else
+                block_mma<NT, ONE, kRowTiles>(wst, xs, table, live, acc, r, c);
             // the slot is consumed: order the reads before the copy that refills it
             __syncwarp();
             fence_proxy_async_smem();
@@ -593,15 +704,15 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
 }
 
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
-          bool DC = false>
+          bool DC = false, bool X8 = false>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status,
-                       const CUtensorMap *tmW2 = nullptr) {
+                       const CUtensorMap *tmAux = nullptr) {
     const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU, DC>;
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU, DC, X8>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmW2 ? *tmW2 : tmW, tmX,
+    return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmAux ? *tmAux : tmW, tmX,
                       ra, N, KB, nx,
                       status);
 }
@@ -679,6 +790,42 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
     return launch_cfg<2, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
 }
 
+cudaError_t launch_smallm_x8(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const int8_t *q,
+                             const float *sx, int64_t M, float *y, int64_t ldy, bool early_weights, cudaStream_t s) {
+    const int KB = (int)(K / kQK);
+    const Split sp = split_for(di, N, KB);
+    const int S = sp.S, tiles = (int)((N + sp.rows - 1) / sp.rows);
+    CUtensorMap tmW, tmX, tmS;
+    cudaError_t e = make_weight_tmap(&tmW, w, N, K, sp.rows, kBlkWords);
+    if (e != cudaSuccess) return e;
+    e = make_bytes_tmap(&tmX, q, M, K, K, kQK);  // per block: 256 int8 values
+    if (e != cudaSuccess) return e;
+    e = make_bytes_tmap(&tmS, sx, M, K / 8, K / 8, 32);  // per block: 8 fp32 scales
+    if (e != cudaSuccess) return e;
+    RowArgs ra = {};
+    ra.y = y; ra.ldy = ldy; ra.M = (int)M;
+    ra.early_w = early_weights ? 1 : 0;
+    const int nx = (int)M, n = (int)N;
+    if (sp.rows == 48) {
+        if (M == 1)
+            return launch_cfg<1, false, true, 2, 48, false, 8, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra, n,
+                                                                                   KB, di.status, &tmS);
+        if (M <= 8)
+            return launch_cfg<1, false, false, 2, 48, false, 8, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra,
+                                                                                    n, KB, di.status, &tmS);
+        return launch_cfg<2, false, false, 2, 48, false, 16, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra, n,
+                                                                                 KB, di.status, &tmS);
+    }
+    if (M == 1)
+        return launch_cfg<1, false, true, 2, 32, false, 8, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB,
+                                                                               di.status, &tmS);
+    if (M <= 8)
+        return launch_cfg<1, false, false, 2, 32, false, 8, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra, n,
+                                                                                KB, di.status, &tmS);
+    return launch_cfg<2, false, false, 2, 32, false, 16, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB,
+                                                                             di.status, &tmS);
+}
+
 namespace {
 
 struct MoeShape {
@@ -690,7 +837,7 @@ struct MoeShape {
 
 // The MoE kernel variant for a call: row split or not, chunk size, ring depth.
 template <bool GLU>
-cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tmW, const CUtensorMap *tmW2,
+cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tmW, const CUtensorMap *tmAux,
                         const CUtensorMap &tmX, const RowArgs &ra, int n, int KB, unsigned int *status) {
     if (m.rs) {
         // chunks of 4, 8 or 16 token slots for up to 4, 8 or more items per expert
@@ -699,22 +846,22 @@ cudaError_t moe_variant(const MoeShape &m, cudaStream_t s, const CUtensorMap &tm
         if (m.per_expert <= 4 || m.direct) {
             const int nx = m.nx1 ? 1 : 4;
             return m.deep ? launch_cfg<1, true, false, 3, 32, true, 4, GLU>(1, m.tiles, m.layers, nx, s, tmW, tmX, ra,
-                                                                             n, KB, status, tmW2)
+                                                                             n, KB, status, tmAux)
                           : launch_cfg<1, true, false, 2, 32, true, 4, GLU>(1, m.tiles, m.layers, nx, s, tmW, tmX, ra,
-                                                                             n, KB, status, tmW2);
+                                                                             n, KB, status, tmAux);
         }
         if (m.per_expert <= 8)
             return m.deep ? launch_cfg<1, true, false, 3, 32, true, 8, GLU>(1, m.tiles, m.layers, 8, s, tmW, tmX, ra, n,
-                                                                             KB, status, tmW2)
+                                                                             KB, status, tmAux)
                           : launch_cfg<1, true, false, 2, 32, true, 8, GLU>(1, m.tiles, m.layers, 8, s, tmW, tmX, ra, n,
-                                                                             KB, status, tmW2);
+                                                                             KB, status, tmAux);
         return launch_cfg<2, true, false, 2, 32, true, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB,
-                                                                 status, tmW2);
+                                                                 status, tmAux);
     }
     if (m.few)
         return launch_cfg<1, true, false, 3, 32, false, 8, GLU>(1, m.tiles, m.layers, m.nx1 ? 1 : 8, s, tmW, tmX, ra,
-                                                                 n, KB, status, tmW2);
-    return launch_cfg<2, true, false, 2, 32, false, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB, status, tmW2);
+                                                                 n, KB, status, tmAux);
+    return launch_cfg<2, true, false, 2, 32, false, 16, GLU>(1, m.tiles, m.layers, 16, s, tmW, tmX, ra, n, KB, status, tmAux);
 }
 
 }  // namespace
@@ -724,7 +871,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
                               float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu,
                               const void *w_up, const float *gates) {
-    CUtensorMap tmW, tmW2, tmX;
+    CUtensorMap tmW, tmAux, tmX;
     // all experts stacked: E*N rows of the same pitch
     constexpr int kRows = 32;
     cudaError_t e = make_weight_tmap(&tmW, w_experts, (int64_t)E * N, K, kRows, kBlkWords);
@@ -732,7 +879,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     const bool fused = glu.h != nullptr;  // gate (w_experts) and up (w_up) in one pass
     if (fused) {
         if (!w_up) return cudaErrorInvalidValue;
-        e = make_weight_tmap(&tmW2, w_up, (int64_t)E * N, K, kRows, kBlkWords);
+        e = make_weight_tmap(&tmAux, w_up, (int64_t)E * N, K, kRows, kBlkWords);
         if (e != cudaSuccess) return e;
     }
     e = make_act_tmap(&tmX, x, x_per_slot ? T * topk : T, K, K, kQK / 4);
@@ -769,7 +916,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     const bool deep = rs_ctas <= di.sm_count;
     const int64_t per_expert = (items + (items < E ? items : E) - 1) / (items < E ? items : E);
     const MoeShape ms = {rs, deep, per_expert, ra.direct != 0, items <= 64 * (int64_t)E, tiles, layers, nx1};
-    return fused ? moe_variant<true>(ms, s, tmW, &tmW2, tmX, ra, (int)N, KB, di.status)
+    return fused ? moe_variant<true>(ms, s, tmW, &tmAux, tmX, ra, (int)N, KB, di.status)
                  : moe_variant<false>(ms, s, tmW, nullptr, tmX, ra, (int)N, KB, di.status);
 }
 

@@ -22,6 +22,10 @@ TOL_TC = 1e-2
 # projections' errors (each within TOL_TC of its own output) and the down
 # projection adds its own, so the layer's output is held to three times TOL_TC
 TOL_FFN_TC = 3 * TOL_TC
+# int8 activations: the sub-block dot products are exact integers on both sides;
+# only the fp32 scaling and the fp32 sum over K/32 terms differ from the oracle's
+# fp64 (at most ~(K/32) * 2^-24 of the sum of |terms|, typically far less)
+TOL_X8 = TOL_SMALL / 10
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -664,3 +668,98 @@ def test_moe_ffn_matches_grouped_calls_and_is_deterministic(syn, ffn_layer, T):
     yc = run_moe(None, E, D, H, h.reshape(T * topk, H), q4k.Q4K_MOE_X_PER_SLOT, ids, gates, C, w_dev=devs[2])
     # h may differ in the last bf16 place where host and device exp differ
     assert G.rel_err(a, yc) <= TOL_SMALL
+
+
+# ------------------------------------------------------------ int8 activations
+def gpu_quantize_x8(x, ldx=None):
+    M, K = x.shape
+    ldx = ldx or K
+    xp = np.zeros((M, ldx), np.uint16)
+    xp[:, :K] = x
+    q = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    sc = torch.full((M, K // 32), float("nan"), dtype=torch.float32, device="cuda")
+    q4k.q4k_quantize_x8(G.dev(xp), M, K, ldx, q, sc)
+    torch.cuda.synchronize()
+    return G.host(q), G.host(sc)
+
+
+def gpu_gemm_x8(blocks, N, K, q, sc, w_dev=None, ldy=None):
+    M = q.shape[0]
+    ldy = ldy or N
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    w = w_dev if w_dev is not None else G.dev(blocks)
+    q4k.q4k_gemm_x8(w, N, K, G.dev(np.ascontiguousarray(q)), G.dev(np.ascontiguousarray(sc)), M, y, ldy)
+    torch.cuda.synchronize()
+    out = G.host(y)
+    if ldy > N:
+        assert np.all(np.isnan(out[:, N:]))
+    return out[:, :N]
+
+
+def test_quantize_x8_bitexact(ref):
+    M, K = 5, 1024
+    x = G.activations(6, 1, M, K).copy()
+    x[0, 32:64] = 0                                   # an all-zero block
+    x[1, 64:96] = 0
+    x[1, 70] = 0x4040                                 # a single non-zero (3.0)
+    # exact ties: largest 127/8, then k.5/8
+    tie = np.zeros(32)
+    tie[0] = 127 / 8
+    tie[1:9] = np.array([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5]) / 8
+    x[2, 0:32] = (np.asarray(tie, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    x[3, :] = 0x0001                                  # tiny subnormal bf16 values
+    for ldx in (K, K + 64):
+        q, sc = gpu_quantize_x8(x, ldx)
+        rq, rs = ref.quantize_x8(x)
+        assert np.array_equal(q, rq)
+        assert np.array_equal(sc.view(np.uint32), rs.view(np.uint32))
+    assert list(q[2, :9]) == [127, 0, 2, 2, 4, 0, -2, -2, 126]
+
+
+def test_quantize_x8_full_size_bitexact(ref):
+    M, K = 16, 17408
+    x = G.activations(6, 2, M, K)
+    q, sc = gpu_quantize_x8(x)
+    rq, rs = ref.quantize_x8(x)
+    assert np.array_equal(q, rq) and np.array_equal(sc.view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 16])
+def test_gemm_x8_ragged(ref, M):
+    N, K = 200, 1024
+    w = G.weights(6, 3, N, K, outliers=True)
+    x = G.activations(6, 4, M, K)
+    q, sc = ref.quantize_x8(x)
+    y = gpu_gemm_x8(w, N, K, q, sc, ldy=N + 8)
+    assert G.rel_err(y, ref.gemm_x8(w, N, K, q, sc)) <= TOL_X8
+
+
+@pytest.mark.parametrize("shape", [G.DECODE_UP, G.DECODE_DOWN], ids=["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 4])
+def test_gemm_x8_full_size(ref, shape, M):
+    # the decode and verify shapes in the benchmark's configuration, sampled rows
+    _, N, K = shape
+    w = G.weights(1, 0 if N == 17408 else 5, N, K)
+    x = G.activations(6, 5, M, K)
+    q, sc = gpu_quantize_x8(x)
+    y = gpu_gemm_x8(w, N, K, q, sc)
+    rows = G.sample_rows(N, 64, seed=M)
+    want = ref.gemm_x8(G.rows_of(w, rows), len(rows), K, q, sc)
+    assert G.rel_err(y[:, rows], want) <= TOL_X8
+
+
+def test_gemm_x8_batch_invariant_and_close_to_bf16(ref):
+    # row m of an M-token call equals the 1-token call, bit for bit; and the int8
+    # path stays within the activations' quantization error of the bf16 path
+    N, K, M = 640, 4096, 7
+    w = G.weights(6, 6, N, K)
+    wd = G.dev(w)
+    x = G.activations(6, 7, M, K)
+    q, sc = ref.quantize_x8(x)
+    ym = gpu_gemm_x8(w, N, K, q, sc, w_dev=wd)
+    for m in (0, 3, 6):
+        y1 = gpu_gemm_x8(w, N, K, q[m:m + 1], sc[m:m + 1], w_dev=wd)
+        assert np.array_equal(y1[0].view(np.uint32), ym[m].view(np.uint32))
+    yb = ref.gemm(w, N, K, x)
+    # |sum w (x - xh)| <= sum |w| * s / 2 per row; checked in aggregate
+    assert G.rel_err(ym, yb) <= 2e-2

@@ -108,6 +108,14 @@ A16 = 1 << 20  # a 16-byte aligned fake address; never dereferenced by these cal
      q4k.Q4K_ERR_ALIGN),
     (lambda L: L.q4k_moe_ffn(A16, A16, A16, 8, 256, 512, A16, A16, A16, 4, 2, A16, A16, 1024, None),
      q4k.Q4K_ERR_WORKSPACE),
+    (lambda L: L.q4k_quantize_x8(None, 2, 256, 256, A16, A16, None), q4k.Q4K_ERR_NULL),
+    (lambda L: L.q4k_quantize_x8(A16, 2, 300, 300, A16, A16, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_quantize_x8(A16, 2, 256, 128, A16, A16, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_quantize_x8(A16, 2, 256, 256, A16 + 8, A16, None), q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, None, 1, A16, 4, None), q4k.Q4K_ERR_NULL),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 17, A16, 4, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 0, A16, 4, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16 + 4, 1, A16, 4, None), q4k.Q4K_ERR_ALIGN),
 ])
 def test_argument_errors_before_any_device_work(lib, call, status):
     assert call(lib) == status
