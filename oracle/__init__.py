@@ -80,6 +80,16 @@ def _load():
             lib.q4k_ref_quantize_x8.restype = None
             lib.q4k_ref_gemm_x8.argtypes = [P, i64, i64, P, P, i64, P]
             lib.q4k_ref_gemm_x8.restype = ctypes.c_int
+            lib.q4k_ref_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+            lib.q4k_ref_e2m1_to_f32.restype = ctypes.c_float
+            lib.q4k_ref_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            lib.q4k_ref_e4m3_to_f32.restype = ctypes.c_float
+            lib.q4k_ref_nvfp4_dequant_block.argtypes = [P, ctypes.c_float, P]
+            lib.q4k_ref_nvfp4_dequant_block.restype = None
+            lib.q4k_ref_nvfp4_dequant.argtypes = [P, ctypes.c_float, i64, i64, P]
+            lib.q4k_ref_nvfp4_dequant.restype = ctypes.c_int
+            lib.q4k_ref_nvfp4_gemm.argtypes = [P, ctypes.c_float, i64, i64, P, i64, P, ctypes.c_int]
+            lib.q4k_ref_nvfp4_gemm.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -228,5 +238,38 @@ def gemm_x8(w: np.ndarray, N: int, K: int, q, s) -> np.ndarray:
     M = q.shape[0]
     y = np.empty((M, N), dtype=np.float64)
     if _load().q4k_ref_gemm_x8(_p(_blocks(w)), N, K, _p(q), _p(s), M, _p(y)) != 0:
+        raise ValueError("bad shape")
+    return y
+
+
+def e2m1_to_f32(code: int) -> float:
+    return float(_load().q4k_ref_e2m1_to_f32(code))
+
+
+def e4m3_to_f32(bits: int) -> float:
+    return float(_load().q4k_ref_e4m3_to_f32(bits))
+
+
+def nvfp4_dequant_block(blk: np.ndarray, g: float) -> np.ndarray:
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    out = np.empty(256, dtype=np.float32)
+    _load().q4k_ref_nvfp4_dequant_block(_p(blk), g, _p(out))
+    return out
+
+
+def nvfp4_dequant(w: np.ndarray, g: float, N: int, K: int) -> np.ndarray:
+    """NVFP4 blocks [N, K/256*144] -> fp32 [N, K] (q4k_ref_nvfp4_dequant)."""
+    out = np.empty((N, K), dtype=np.float32)
+    if _load().q4k_ref_nvfp4_dequant(_p(_blocks(w)), g, N, K, _p(out)) != 0:
+        raise ValueError("bad shape")
+    return out
+
+
+def nvfp4_gemm(w: np.ndarray, g: float, N: int, K: int, x_bf16, threads: int = 1) -> np.ndarray:
+    """y [M, N] fp64 over NVFP4 weights (q4k_ref_nvfp4_gemm)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M = x.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    if _load().q4k_ref_nvfp4_gemm(_p(_blocks(w)), g, N, K, _p(x), M, _p(y), threads) != 0:
         raise ValueError("bad shape")
     return y

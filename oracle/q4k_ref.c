@@ -335,3 +335,87 @@ int q4k_ref_gemm_x8(const uint8_t *w, int64_t N, int64_t K, const int8_t *q, con
     free(wrow);
     return 0;
 }
+
+/* e2m1: bit 3 sign, bits 2-1 exponent (bias 1), bit 0 mantissa; exponent 0 is
+ * subnormal (0 or 0.5) */
+float q4k_ref_e2m1_to_f32(uint8_t code) {
+    const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const float v = e == 0 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
+    return sign ? -v : v;
+}
+
+/* e4m3 (the finite variant): bit 7 sign, bits 6-3 exponent (bias 7), bits 2-0
+ * mantissa; exponent 0 is subnormal (m * 2^-9); exponent 15 with mantissa 7 is NaN */
+float q4k_ref_e4m3_to_f32(uint8_t bits) {
+    const int sign = (bits >> 7) & 1, e = (bits >> 3) & 15, m = bits & 7;
+    float v;
+    if (e == 15 && m == 7) v = NAN;
+    else if (e == 0) v = ldexpf((float)m, -9);
+    else v = ldexpf((float)(8 + m), e - 10);
+    return sign ? -v : v;
+}
+
+void q4k_ref_nvfp4_dequant_block(const uint8_t *blk, float g, float *out) {
+    for (int i = 0; i < 256; ++i) {
+        const uint8_t byte = blk[16 + i / 2];
+        const uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+        const float sv = q4k_ref_e4m3_to_f32(blk[i / 16]) * q4k_ref_e2m1_to_f32(code); /* exact */
+        out[i] = g * sv;
+    }
+}
+
+int q4k_ref_nvfp4_dequant(const uint8_t *w, float g, int64_t N, int64_t K, float *out) {
+    if (!shape_ok(N, K)) return -1;
+    const int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b) q4k_ref_nvfp4_dequant_block(w + (n * nb + b) * BB, g, out + n * K + b * QK);
+    return 0;
+}
+
+typedef struct {
+    const uint8_t *w;
+    double g;
+    int64_t N, K, M, n0, n1;
+    const uint16_t *x;
+    double *y;
+} nvfp4_job;
+
+static void *nvfp4_worker(void *arg) {
+    nvfp4_job *j = (nvfp4_job *)arg;
+    const int64_t nb = j->K / QK;
+    double *wrow = (double *)malloc(sizeof(double) * (size_t)j->K);
+    for (int64_t n = j->n0; n < j->n1 && wrow; ++n) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t *blk = j->w + (n * nb + b) * BB;
+            for (int i = 0; i < 256; ++i) {
+                const uint8_t byte = blk[16 + i / 2];
+                const uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+                wrow[b * QK + i] = j->g * (double)q4k_ref_e4m3_to_f32(blk[i / 16]) * (double)q4k_ref_e2m1_to_f32(code);
+            }
+        }
+        for (int64_t m = 0; m < j->M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < j->K; ++k) acc += wrow[k] * (double)q4k_ref_bf16_to_f32(j->x[m * j->K + k]);
+            j->y[m * j->N + n] = acc;
+        }
+    }
+    free(wrow);
+    return NULL;
+}
+
+int q4k_ref_nvfp4_gemm(const uint8_t *w, float g, int64_t N, int64_t K, const uint16_t *x, int64_t M, double *y,
+                       int threads) {
+    if (!shape_ok(N, K) || M < 0) return -1;
+    if (threads < 1) threads = 1;
+    if (threads > 256) threads = 256;
+    pthread_t tid[256];
+    nvfp4_job jobs[256];
+    for (int t = 0; t < threads; ++t) {
+        jobs[t] = (nvfp4_job){w, (double)g, N, K, M, N * t / threads, N * (t + 1) / threads, x, y};
+        if (threads == 1) nvfp4_worker(&jobs[t]);
+        else pthread_create(&tid[t], NULL, nvfp4_worker, &jobs[t]);
+    }
+    if (threads > 1)
+        for (int t = 0; t < threads; ++t) pthread_join(tid[t], NULL);
+    return 0;
+}

@@ -93,6 +93,26 @@ void q4k_ref_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int8_t *q, flo
  * Returns 0, or -1 on a bad shape. */
 int q4k_ref_gemm_x8(const uint8_t *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, double *y);
 
+/* NVFP4 weights (the pages serve NVFP4 checkpoints next to GGUF Q4_K:
+ * sparkinfer-server README, "Serve a GGUF instead of NVFP4"; the format is not
+ * spelled out there).  Reading taken: NVIDIA's NVFP4 - 4-bit e2m1 values (sign,
+ * 2-bit exponent with bias 1, 1-bit mantissa: magnitudes 0, 0.5, 1, 1.5, 2, 3,
+ * 4, 6), one e4m3 scale (sign, 4-bit exponent with bias 7, 3-bit mantissa;
+ * exponent 0 subnormal; 0x7F/0xFF NaN) per 16 consecutive weights, and one fp32
+ * scale g per tensor: w = g * e4m3 * e2m1.  Byte layout (this library's, like
+ * GGUF's for Q4_K): a row is K/256 blocks of 144 bytes, each 16 scale bytes
+ * (scale j for weights 16j..16j+15) then 128 value bytes (weight 2i in the low
+ * nibble of byte i, 2i+1 in the high nibble). */
+float q4k_ref_e2m1_to_f32(uint8_t code);
+float q4k_ref_e4m3_to_f32(uint8_t bits);
+/* 256 weights of one block, each g * (e4m3 * e2m1) rounded once to fp32 (the
+ * product e4m3 * e2m1 is exact in fp32) */
+void q4k_ref_nvfp4_dequant_block(const uint8_t *blk, float g, float *out);
+int q4k_ref_nvfp4_dequant(const uint8_t *w, float g, int64_t N, int64_t K, float *out);
+/* y[m][n] = sum_k w[n][k] * x[m][k], with w = g * e4m3 * e2m1 exact in fp64 */
+int q4k_ref_nvfp4_gemm(const uint8_t *w, float g, int64_t N, int64_t K, const uint16_t *x, int64_t M, double *y,
+                       int threads);
+
 /* Round a double to the nearest bf16 (ties to even), once; returns its bits.
  * Finite normal range only (|v| from 2^-126 to the bf16 maximum, or 0). */
 uint16_t q4k_ref_f64_to_bf16(double v);

@@ -156,3 +156,47 @@ def weights(seed_: int, N: int, K: int, std: float = 0.02, outlier_frac: float =
 
 def row_bytes(K: int) -> int:
     return K // QK * BLOCK_BYTES
+
+
+# ----------------------------------------------------------------- NVFP4 inputs
+# Input generation only: a simple nearest-value NVFP4 quantizer (e2m1 values,
+# one e4m3 scale per 16 weights, one fp32 scale per tensor) packed in 144-byte
+# blocks of 256 weights: 16 scale bytes, then 128 value bytes (weight 2i in the
+# low nibble of byte i).
+
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e4m3_positive_table():
+    codes = np.arange(0x7F, dtype=np.int64)  # 0x00 .. 0x7E: every finite non-negative value
+    e, m = (codes >> 3) & 15, codes & 7
+    vals = np.where(e == 0, m * 2.0 ** -9, (8 + m) * np.exp2(e - 10.0))
+    order = np.argsort(vals, kind="stable")
+    return vals[order], codes[order].astype(np.uint8)
+
+
+def nvfp4_quantize(w: np.ndarray) -> tuple:
+    """fp32 [N, K] -> (NVFP4 blocks [N, K/256*144] uint8, per-tensor fp32 scale g)."""
+    w = np.asarray(w, dtype=np.float64)
+    N, K = w.shape
+    amax = float(np.abs(w).max()) if w.size else 0.0
+    g = np.float32(amax / (6.0 * 448.0) if amax > 0 else 1.0)
+    grp = w.reshape(N, K // 16, 16) / float(g)
+    tv, tc = _e4m3_positive_table()
+    want = np.abs(grp).max(axis=2) / 6.0                    # scale that maps the group's max to 6
+    idx = np.clip(np.searchsorted(tv, want), 0, len(tv) - 1)  # smallest table value >= want
+    sval, scode = tv[idx], tc[idx]
+    r = np.abs(grp) / np.where(sval > 0, sval, 1.0)[..., None]
+    mid = (_E2M1_MAG[1:] + _E2M1_MAG[:-1]) / 2
+    mag = np.searchsorted(mid, np.minimum(r, 6.0))          # nearest e2m1 magnitude
+    code = (mag | np.where(grp < 0, 8, 0)).astype(np.uint8).reshape(N, K)
+    out = np.empty((N, K // 256, 144), dtype=np.uint8)
+    out[:, :, :16] = scode.reshape(N, K // 256, 16)
+    pairs = code.reshape(N, K // 256, 128, 2)
+    out[:, :, 16:] = pairs[..., 0] | (pairs[..., 1] << 4)
+    return out.reshape(N, K // 256 * 144), g
+
+
+def nvfp4_weights(seed_: int, N: int, K: int, std: float = 0.02) -> tuple:
+    """NVFP4 blocks of an N x K matrix drawn from N(0, std^2), and its tensor scale g."""
+    return nvfp4_quantize(normal_f32(seed_, N * K, 0.0, std).reshape(N, K))

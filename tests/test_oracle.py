@@ -12,7 +12,10 @@
     exact-rational bf16 rounding;
   - int8 activations: quantization invariants, exact ties, sign and power-of-two
     symmetries; the int8 GEMM equals the pinned GEMM where the dequantized
-    activations are exact in bf16, and exact rationals on a small case.
+    activations are exact in bf16, and exact rationals on a small case;
+  - NVFP4: the e2m1 value set, all 256 e4m3 patterns vs torch's float8_e4m3fn,
+    block layout (nibble order, scale index) on hand-built blocks, the GEMM vs
+    numpy on an independent decode and vs exact rationals.
 """
 from fractions import Fraction
 
@@ -418,6 +421,89 @@ def test_gemm_x8_exact_rational(ref, syn):
     for n in range(N):
         exact = sum(Fraction(float(wd[n, k])) * Fraction(float(sc[0, k // 32])) * int(q[0, k]) for k in range(K))
         assert abs(Fraction(float(got[0, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 40) + Fraction(1, 2 ** 60)
+
+
+
+# ------------------------------------------------------------------- NVFP4
+# the e2m1 value set of the FP4 format: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 for
+# codes 0..7, the same negated for codes 8..15
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_values(ref):
+    for c in range(16):
+        v = ref.e2m1_to_f32(c)
+        assert abs(v) == E2M1[c & 7] and (np.signbit(v) == bool(c & 8))
+
+
+def test_e4m3_all_patterns_vs_torch(ref):
+    import torch
+    pats = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = pats.view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    got = np.array([ref.e4m3_to_f32(b) for b in range(256)], dtype=np.float32)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok].view(np.uint32), want[ok].view(np.uint32))
+
+
+def _nvfp4_block(scales, codes) -> np.ndarray:
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[:16] = scales
+    codes = np.asarray(codes, dtype=np.uint8)
+    blk[16:] = codes[0::2] | (codes[1::2] << 4)
+    return blk
+
+
+def test_nvfp4_block_layout(ref):
+    # weight i carries code i % 16 and the scale of group i // 16 (distinct powers of two)
+    scales = np.array([0x38 + 8 * (j % 4) - 8 * (j // 4) for j in range(16)], dtype=np.uint8)  # 2^(j%4 - j//4)
+    codes = np.arange(256) % 16
+    g = 0.75
+    out = ref.nvfp4_dequant_block(_nvfp4_block(scales, codes), g)
+    for i in range(256):
+        j = i // 16
+        sv = 2.0 ** (j % 4 - j // 4)
+        want = np.float32(g * sv * (E2M1[codes[i] & 7] * (-1 if codes[i] & 8 else 1)))
+        assert out[i] == want, i
+    # a subnormal and the largest scale; g rounds the product once
+    blk = _nvfp4_block([0x01] * 8 + [0x7E] * 8, [7] * 256)
+    out = ref.nvfp4_dequant_block(blk, 1.0)
+    assert out[0] == 6 * 2.0 ** -9 and out[255] == 6 * 448.0
+
+
+def _np_nvfp4_decode(w, g, N, K):
+    """Independent decode: the byte layout and the pinned value sets, in numpy."""
+    b = np.asarray(w, np.uint8).reshape(N, K // 256, 144)
+    import torch
+    sc = torch.from_numpy(np.ascontiguousarray(b[:, :, :16])).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    v = b[:, :, 16:]
+    codes = np.stack([v & 15, v >> 4], axis=-1).reshape(N, K // 256, 256)
+    mag = np.array(E2M1)[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+    return (float(g) * np.repeat(sc, 16, axis=2) * mag).reshape(N, K)
+
+
+def test_nvfp4_gemm_vs_numpy(ref, syn):
+    N, K, M = 6, 768, 3
+    w, g = syn.nvfp4_weights(48, N, K)
+    x = syn.normal_bf16(49, M * K).reshape(M, K)
+    want = bf16_bits_to_f64(x) @ _np_nvfp4_decode(w, g, N, K).T
+    got = ref.nvfp4_gemm(w, float(g), N, K, x)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+    # the fp32 dequant is the exact value rounded once
+    wd = ref.nvfp4_dequant(w, float(g), N, K)
+    assert np.array_equal(wd, _np_nvfp4_decode(w, g, N, K).astype(np.float32))
+
+
+def test_nvfp4_gemm_exact_rational(ref, syn):
+    N, K = 2, 256
+    w, g = syn.nvfp4_weights(50, N, K)
+    x = syn.normal_bf16(51, K).reshape(1, K)
+    wd = _np_nvfp4_decode(w, g, N, K)
+    got = ref.nvfp4_gemm(w, float(g), N, K, x)
+    xf = bf16_bits_to_f64(x)[0]
+    for n in range(N):
+        exact = sum(Fraction(float(wd[n, k])) * Fraction(float(xf[k])) for k in range(K))
+        assert abs(Fraction(float(got[0, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 40) + Fraction(1, 2 ** 70)
 
 
 # ------------------------------------------------------------ input module

@@ -40,6 +40,13 @@ MUTANTS = {
     "x8_scale_128": ("const float sc = a / 127.0f;", "const float sc = a / 128.0f;"),
     "x8_signed_max": ("const float v = fabsf(q4k_ref_bf16_to_f32(xb[i]));", "const float v = q4k_ref_bf16_to_f32(xb[i]);"),
     "x8_scale_block": ("(double)s[m * (K / 32) + k / 32]", "(double)s[m * (K / 32) + ((k / 32) ^ 1)]"),
+    "nvfp4_e4m3_bias": ("else v = ldexpf((float)(8 + m), e - 10);", "else v = ldexpf((float)(8 + m), e - 9);"),
+    "nvfp4_e2m1_subnormal": ("e == 0 ? 0.5f * (float)m", "e == 0 ? 1.0f * (float)m"),
+    "nvfp4_scale_group": ("q4k_ref_e4m3_to_f32(blk[i / 16]) * q4k_ref_e2m1_to_f32(code); /* exact */",
+                          "q4k_ref_e4m3_to_f32(blk[i / 32]) * q4k_ref_e2m1_to_f32(code); /* exact */"),
+    "nvfp4_nibble_order": ("(i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);\n        const float sv",
+                           "(i & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4);\n        const float sv"),
+    "nvfp4_gemm_no_global": ("wrow[b * QK + i] = j->g * (double)", "wrow[b * QK + i] = (double)"),
 }
 
 
