@@ -12,8 +12,9 @@ speculative-verify GEMM, K 5120 -> N 17408, --m, default 4), `prefill` (M x K
 `moe` (128 experts, top-8: gate, up and down with the weighted combine, --m
 tokens, default 2048) and `moe_ffn` (the same layer as one routed SwiGLU expert
 feed-forward call: gate, up with the SwiGLU epilogue, down on the bf16 h rows,
-weighted combine), and `decode_x8` (the decode step with int8 activations:
-per-32 quantization of each matrix's input, then the int8 GEMV).
+weighted combine), `decode_x8` (the decode step with int8 activations:
+per-32 quantization of each matrix's input, then the int8 GEMV) and
+`prefill_nvfp4` (the prefill GEMMs with NVFP4 weights, --m tokens).
 
 Timing: W warm-up steps, then exactly K steps between a barrier plus
 cudaDeviceSynchronize on both sides, timed with CUDA events on the launching
@@ -166,6 +167,7 @@ class Workload:
         self.mats = []   # list of (tag, N, K, M, blocks, x) for dense GEMM steps
         self.moe = None
         self.x8 = name == "decode_x8"
+        self.fp4 = {}  # NVFP4 workloads: tag -> tensor scale g
         if name in ("decode", "decode_x8"):
             self.mats = [("gate_up", 17408, 5120, 1, synth.weights(synth.seed(1, 0), 17408, 5120),
                           synth.normal_bf16(synth.seed(1, 1), 5120).reshape(1, 5120)),
@@ -188,6 +190,15 @@ class Workload:
                                                                          10.0, synth.seed(3, 9)),
                           synth.normal_bf16(synth.seed(3, 6), m * 17408).reshape(m, 17408))]
             self.unit, self.config = "TFLOP/s", {"workload": f"prefill GEMM M={m}: K5120->N17408 then K17408->N5120"}
+        elif name == "prefill_nvfp4":
+            mats = []
+            for tag, N, K, sw, sx in (("prefill_up_fp4", 17408, 5120, 0, 1), ("prefill_down_fp4", 5120, 17408, 5, 6)):
+                blocks, g = synth.nvfp4_weights(synth.seed(8, sw), N, K)
+                self.fp4[tag] = float(g)
+                mats.append((tag, N, K, m, blocks, synth.normal_bf16(synth.seed(8, sx), m * K).reshape(m, K)))
+            self.mats = mats
+            self.unit, self.config = "TFLOP/s", {"workload": f"prefill GEMM with NVFP4 weights M={m}: "
+                                                             "K5120->N17408 then K17408->N5120"}
         elif name in ("moe", "moe_ffn"):
             E, topk = 128, 8
             ids, gates = synth.routing(synth.seed(4, 2) + m, synth.seed(4, 3) + m, m, E, topk)
@@ -289,8 +300,10 @@ class GpuRunner:
     def step_one(self, r: int, i: int):
         """Enqueue only matrix i of the step, with weight set r."""
         q4k, wl = self.q4k, self.wl
-        _, N, K, M, _, _ = wl.mats[i]
-        if wl.x8:
+        tag, N, K, M, _, _ = wl.mats[i]
+        if tag in wl.fp4:
+            q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N)
+        elif wl.x8:
             q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N)
         elif M == 1:
             q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i])
@@ -324,10 +337,12 @@ class GpuRunner:
             if mark:
                 mark(1)
             return
-        for i, (_, N, K, M, _, _) in enumerate(wl.mats):
+        for i, (tag, N, K, M, _, _) in enumerate(wl.mats):
             if mark:
                 mark(i)
-            if wl.x8:
+            if tag in wl.fp4:
+                q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N)
+            elif wl.x8:
                 q4k.q4k_quantize_x8(self.x[i], M, K, K, self.q[i], self.sx[i])
                 q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N)
             elif M == 1:
@@ -482,7 +497,8 @@ def run_gpu(args, rank, local_rank, world):
         "metric": METRIC, "value": wl.value(sec_per_step) * world, "unit": wl.unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8 (per-32 fp32 scales) x Q4_K -> fp32" if wl.x8 else "bf16 x Q4_K -> fp32",
+        "dtype": ("int8 (per-32 fp32 scales) x Q4_K -> fp32" if wl.x8 else
+                  "bf16 x NVFP4 -> fp32" if wl.fp4 else "bf16 x Q4_K -> fp32"),
         "data": "synthetic (seeded N(0,0.02^2) weights quantized to Q4_K; N(0,1) bf16 activations)",
         "config": dict(wl.config, l2="rotating %d weight sets, %.0f MB total > 129 MB L2" %
                        (gr.R, gr.R * (wl.weight_bytes() if not wl.moe else sum(
@@ -594,14 +610,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "decode_x8", "verify", "prefill", "moe", "moe_ffn"],
+    ap.add_argument("--workload", choices=["decode", "decode_x8", "verify", "prefill", "prefill_nvfp4", "moe",
+                                           "moe_ffn"],
                     default="decode")
     ap.add_argument("--m", type=int, default=None, help="tokens (verify: 4, prefill: 4096, moe: 2048)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.m is None:
-        args.m = {"decode": 1, "decode_x8": 1, "verify": 4, "prefill": 4096, "moe": 2048,
+        args.m = {"decode": 1, "decode_x8": 1, "verify": 4, "prefill": 4096, "prefill_nvfp4": 4096, "moe": 2048,
                   "moe_ffn": 2048}[args.workload]
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

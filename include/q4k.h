@@ -178,6 +178,28 @@ q4k_status q4k_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
 q4k_status q4k_gemm_x8(const void *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, float *y,
                        int64_t ldy, void *stream);
 
+/* ------------------------------------------------------------- NVFP4 weights --
+ * The pages serve NVFP4 checkpoints as well as GGUF Q4_K (sparkinfer-server
+ * README, "Serve a GGUF instead of NVFP4"); they do not spell the format out.
+ * Reading taken: NVIDIA's NVFP4, w = g * e4m3 * e2m1 - 4-bit e2m1 values
+ * (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 and a sign bit), one e4m3 scale per 16
+ * consecutive weights of a row, one fp32 scale g per tensor.  Byte layout (this
+ * library's): a row is K/256 blocks of 144 bytes (q4k_row_bytes(K)), each 16
+ * e4m3 scale bytes (scale j covers weights 16j..16j+15) followed by 128 bytes
+ * of e2m1 pairs (weight 2i in the low nibble of byte i, 2i+1 in the high one).
+ *
+ * q4k_nvfp4_dequant: out[N][K] fp32 = g * (e4m3 * e2m1), the product exact and
+ * the multiplication by g rounded once: bit-exact.  w and out 16-byte aligned.
+ * q4k_nvfp4_gemm: y[M][ldy] = x[M][ldx] . W^T for any M >= 1, on the tcgen05
+ * tensor cores: each weight enters the MMA as the exact bf16 value e4m3 * e2m1,
+ * the fp32 accumulator is multiplied by g in the epilogue.  x 16-byte aligned,
+ * ldx % 8 == 0; y 4-byte aligned.  Deterministic (no atomics).
+ * Errors: NULL, SHAPE (M or N < 1, K not a positive multiple of 256, ldx < K,
+ * ldy < N), ALIGN, DEVICE, CUDA. */
+q4k_status q4k_nvfp4_dequant(const void *w, float g, int64_t N, int64_t K, float *out, void *stream);
+q4k_status q4k_nvfp4_gemm(const void *w, float g, int64_t N, int64_t K, const uint16_t *x, int64_t M, int64_t ldx,
+                          float *y, int64_t ldy, void *stream);
+
 /* --------------------------------------------------------------------- MoE --
  * Routed-expert layer over E experts, each an N x K Q4_K matrix; the pages' MoE
  * models route each token to its top-k experts and combine the experts' outputs

@@ -28,6 +28,7 @@ EXPORTS = (
     "q4k_set_static_weights", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
     "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_reuse_routing",
     "q4k_moe_grouped_gemm_noalloc", "q4k_moe_ffn_workspace_size", "q4k_moe_ffn", "q4k_quantize_x8", "q4k_gemm_x8",
+    "q4k_nvfp4_dequant", "q4k_nvfp4_gemm",
 )
 
 # fixed scratch capacity of q4k_moe_grouped_gemm_noalloc (Q4K_MOE_NOALLOC_SCRATCH_BYTES)
@@ -75,6 +76,8 @@ def load(path: str | None = None):
         "q4k_moe_ffn": ([P, P, P, i32, i64, i64, P, P, P, i64, i32, P, P, sz, P], st),
         "q4k_quantize_x8": ([P, i64, i64, i64, P, P, P], st),
         "q4k_gemm_x8": ([P, i64, i64, P, P, i64, P, i64, P], st),
+        "q4k_nvfp4_dequant": ([P, ctypes.c_float, i64, i64, P, P], st),
+        "q4k_nvfp4_gemm": ([P, ctypes.c_float, i64, i64, P, i64, i64, P, i64, P], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -217,3 +220,13 @@ def q4k_quantize_x8(x, M: int, K: int, ldx: int, q, s, stream=None) -> None:
 def q4k_gemm_x8(w, N: int, K: int, q, s, M: int, y, ldy: int, stream=None) -> None:
     """y = (s * q) . W^T over int8 activations, M in [1, 16]."""
     _check(load().q4k_gemm_x8(_ptr(w), N, K, _ptr(q), _ptr(s), M, _ptr(y), ldy, _stream(stream)), "q4k_gemm_x8")
+
+
+def q4k_nvfp4_dequant(w, g: float, N: int, K: int, out, stream=None) -> None:
+    """NVFP4 blocks -> fp32 [N][K], w = g * e4m3 * e2m1."""
+    _check(load().q4k_nvfp4_dequant(_ptr(w), g, N, K, _ptr(out), _stream(stream)), "q4k_nvfp4_dequant")
+
+
+def q4k_nvfp4_gemm(w, g: float, N: int, K: int, x, M: int, ldx: int, y, ldy: int, stream=None) -> None:
+    """y = x . W^T with NVFP4 weights (tensor cores, any M >= 1)."""
+    _check(load().q4k_nvfp4_gemm(_ptr(w), g, N, K, _ptr(x), M, ldx, _ptr(y), ldy, _stream(stream)), "q4k_nvfp4_gemm")

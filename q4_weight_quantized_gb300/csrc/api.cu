@@ -304,6 +304,30 @@ q4k_status q4k_gemm_x8(const void *w, int64_t N, int64_t K, const int8_t *q, con
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 
+q4k_status q4k_nvfp4_dequant(const void *w, float g, int64_t N, int64_t K, float *out, void *stream) {
+    if (!w || !out) return Q4K_ERR_NULL;
+    if (N < 1 || !k_ok(K)) return Q4K_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(out, 16)) return Q4K_ERR_ALIGN;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaError_t e = launch_nvfp4_dequant(w, g, N, K, out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
+q4k_status q4k_nvfp4_gemm(const void *w, float g, int64_t N, int64_t K, const uint16_t *x, int64_t M, int64_t ldx,
+                          float *y, int64_t ldy, void *stream) {
+    if (!w || !x || !y) return Q4K_ERR_NULL;
+    if (M < 1 || N < 1 || !k_ok(K) || ldx < K || ldy < N) return Q4K_ERR_SHAPE;
+    if (N > ((int64_t)1 << 31) - 1 || M > ((int64_t)1 << 31) - 1) return Q4K_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(x, 16) || (ldx % 8) != 0 || !aligned(y, 4)) return Q4K_ERR_ALIGN;
+    DeviceInfo di;
+    q4k_status st = check_device(&di);
+    if (st != Q4K_OK) return st;
+    cudaError_t e = launch_gemm_tc_nvfp4(di, w, g, N, K, x, M, ldx, y, ldy, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
+}
+
 q4k_status q4k_gemv(const void *w, int64_t N, int64_t K, const uint16_t *x, float *y, void *stream) {
     return q4k_gemm(w, N, K, x, 1, K, y, N, nullptr, 0, stream);
 }

@@ -1,4 +1,4 @@
-// Standalone Q4_K dequantization (fp32 and bf16 outputs).
+// Standalone Q4_K dequantization (fp32 and bf16 outputs), and NVFP4 (fp32).
 //
 // This is the step a GGUF target repeats on every prefill pass ("dequantizing it
 // into the matrix-multiply operand", sparkinfer-server README, "Serve a GGUF
@@ -112,7 +112,47 @@ cudaError_t launch(const void *w, int64_t N, int64_t K, Store st, cudaStream_t s
                       n_blocks, st);
 }
 
+// NVFP4: one warp per 144-byte block; lane L takes value bytes 4L..4L+3
+// (weights 8L..8L+7, scale L/2).  w = g * (e4m3 * e2m1): the product is exact
+// in fp32, the multiplication by g rounds once.
+__global__ void __launch_bounds__(256) nvfp4_dequant_kernel(const uint8_t *__restrict__ w, float g, int64_t n_blocks,
+                                                            float *__restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t b = warp; b < n_blocks; b += nwarps) {
+        const uint8_t *blk = w + b * kBlockBytes;
+        const float sc = e4m3_to_f32(__ldg(blk + (lane >> 1)));
+        const uint32_t vw = __ldg(reinterpret_cast<const uint32_t *>(blk + 16 + 4 * lane));
+        uint32_t p[4];
+        e2m1x8_to_bf16(vw, p[0], p[1], p[2], p[3]);
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __fmul_rn(g, __fmul_rn(__uint_as_float(p[i] << 16), sc));
+            v[2 * i + 1] = __fmul_rn(g, __fmul_rn(__uint_as_float(p[i] & 0xFFFF0000u), sc));
+        }
+        float *o = out + b * kQK + 8 * lane;
+        *reinterpret_cast<float4 *>(o) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4 *>(o + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_nvfp4_dequant(const void *w, float g, int64_t N, int64_t K, float *out, cudaStream_t s) {
+    const int64_t n_blocks = N * (K / kQK);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t want = (n_blocks + 7) / 8;
+    const int64_t cap = (int64_t)sms * 16;
+    const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+    return launch_pdl(nvfp4_dequant_kernel, dim3(grid), dim3(256), 0, s, dim3(1), static_cast<const uint8_t *>(w), g,
+                      n_blocks, out);
+}
 
 cudaError_t launch_dequant_f32(const void *w, int64_t N, int64_t K, float *out, cudaStream_t s) {
     return launch(w, N, K, StoreF32{out}, s);

@@ -1,4 +1,4 @@
-// Prefill Q4_K GEMM on the tcgen05 tensor cores.
+// Prefill Q4_K (and NVFP4) GEMM on the tcgen05 tensor cores.
 //
 // A GGUF target dequantizes Q4_K "into the matrix-multiply operand on every
 // prefill pass"; that fixed cost dominates at 128 tokens and is amortized by 4k
@@ -73,10 +73,14 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t
     hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
 }
 
-template <int BN>
+// FP4: the weights are NVFP4 blocks (16 e4m3 scales, then 128 bytes of e2m1
+// pairs) instead of Q4_K; each operand element is the exact e2m1 * e4m3 product
+// in bf16, and the epilogue multiplies by the tensor scale gscale.
+template <int BN, bool FP4 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
-                                                              int64_t ldy, int M, int N, int KB, unsigned int *status) {
+                                                              int64_t ldy, int M, int N, int KB, float gscale,
+                                                              unsigned int *status) {
     pdl_wait();  // the activations may come from the previous kernel
     pdl_trigger();
     using C = Cfg<BN>;
@@ -198,6 +202,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 break;
             }
             const uint8_t *rowp = raw + r * kRawBytes + t * kBlockBytes;
+            if constexpr (FP4) {
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const int i = kb * 4 + g4, s = i % NS;
+                    if (i >= NS &&
+                        !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status))) {
+                        ok = false;
+                        break;
+                    }
+                    // stage g4: weights 64*g4 .. +63 of the block, scales 4*g4 .. +3 (16 weights each)
+                    const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(rowp + 4 * g4);
+                    __nv_bfloat162 sv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float f = e4m3_to_f32(sc4 >> (8 * q));
+                        sv[q] = __floats2bfloat162_rn(f, f);  // exact: e4m3 values are bf16 values
+                    }
+                    const uint4 va = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g4);
+                    const uint4 vb = *reinterpret_cast<const uint4 *>(rowp + 32 + 32 * g4);
+                    const uint32_t wds[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                    uint8_t *arow = as + s * kABytes + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {  // chunk j: weights 8j..8j+7 of the stage, scale j / 2
+                        uint32_t p[4];
+                        e2m1x8_to_bf16(wds[j], p[0], p[1], p[2], p[3]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) p[q] = as_u32(__hmul2(as_bf2(p[q]), sv[j >> 1]));  // exact
+                        *reinterpret_cast<uint4 *>(arow + ((j ^ (t & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+                    }
+                    fence_proxy_async_smem();  // make the stores visible to the tensor core
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full0 + 8 * s);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rempty0 + 8 * r);
+                continue;
+            }
             const uint4 h = *reinterpret_cast<const uint4 *>(rowp);
             const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
             const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
@@ -263,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int m = m0 + 32 * cc + j;
-                        if (m < M) y[(int64_t)m * ldy + n] = __uint_as_float(v[j]);
+                        if (m < M) y[(int64_t)m * ldy + n] = FP4 ? gscale * __uint_as_float(v[j]) : __uint_as_float(v[j]);
                     }
                 }
             }
@@ -283,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 float v = 0.0f;
                 for (int qr = 0; qr < S; ++qr) v += ld_shared_cluster_f32(map_shared_rank(off, qr));
                 const int m = m0 + c, n = n0 + rr;
-                if (m < M && n < N) y[(int64_t)m * ldy + n] = v;
+                if (m < M && n < N) y[(int64_t)m * ldy + n] = FP4 ? gscale * v : v;
             }
         }
         cluster_sync();  // keep every partial alive until all ranks have read it
@@ -299,9 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
 }
 
-template <int BN>
+template <int BN, bool FP4>
 cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                      int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
+                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s) {
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
     if (e != cudaSuccess) return e;
@@ -309,7 +349,7 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     if (e != cudaSuccess) return e;
     const int smem = Cfg<BN>::bytes;
     static_assert(Cfg<BN>::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers");
-    e = ensure_smem((const void *)gemm_tc_kernel<BN>, smem);
+    e = ensure_smem((const void *)gemm_tc_kernel<BN, FP4>, smem);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const int64_t tiles = ((N + kTileRows - 1) / kTileRows) * ((M + BN - 1) / BN);
@@ -323,16 +363,22 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
         if (want > 1) S = (int)want;
     }
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
-    return launch_pdl(gemm_tc_kernel<BN>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW, tmX, y,
-                      ldy, (int)M, (int)N, KB, di.status);
+    return launch_pdl(gemm_tc_kernel<BN, FP4>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
+                      tmX, y, ldy, (int)M, (int)N, KB, g, di.status);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
-    if (M <= 128) return launch_bn<128>(di, w, N, K, x, M, ldx, y, ldy, s);
-    return launch_bn<256>(di, w, N, K, x, M, ldx, y, ldy, s);
+    if (M <= 128) return launch_bn<128, false>(di, w, N, K, x, M, ldx, y, ldy, 1.0f, s);
+    return launch_bn<256, false>(di, w, N, K, x, M, ldx, y, ldy, 1.0f, s);
+}
+
+cudaError_t launch_gemm_tc_nvfp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K,
+                                 const uint16_t *x, int64_t M, int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
+    if (M <= 128) return launch_bn<128, true>(di, w, N, K, x, M, ldx, y, ldy, g, s);
+    return launch_bn<256, true>(di, w, N, K, x, M, ldx, y, ldy, g, s);
 }
 
 }  // namespace q4k

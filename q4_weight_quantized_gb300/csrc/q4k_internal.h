@@ -26,6 +26,9 @@ cudaError_t device_info(DeviceInfo *out);
 
 cudaError_t launch_dequant_f32(const void *w, int64_t N, int64_t K, float *out, cudaStream_t s);
 cudaError_t launch_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *out, cudaStream_t s);
+// NVFP4 blocks (16 e4m3 scales, then 128 bytes of e2m1 pairs, per 256 weights)
+// with tensor scale g: w = g * e4m3 * e2m1 in fp32 (dequant.cu)
+cudaError_t launch_nvfp4_dequant(const void *w, float g, int64_t N, int64_t K, float *out, cudaStream_t s);
 
 // M in [1, 16].  early_weights: the first weight blocks may be copied before
 // the kernel has waited on the previous kernel in the stream (static weights).
@@ -56,6 +59,11 @@ struct GluOut {
     uint16_t *h = nullptr;  // null: plain fp32 output
     int h_sorted = 0;
 };
+
+// NVFP4 weights through the same tensor-core kernel: the operand is the exact
+// bf16 e2m1 * e4m3 product, y = g * (x . operand^T) (gemm_tc.cu)
+cudaError_t launch_gemm_tc_nvfp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K,
+                                 const uint16_t *x, int64_t M, int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
 
 // MoE expert GEMM on the tensor cores: a persistent kernel (one CTA per SM,
 // double-buffered tensor-memory accumulators) walking the routing's token tiles

@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -148,6 +149,34 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
+}
+
+// ------------------------------------------------------------------ NVFP4
+// Eight e2m1 codes of one 32-bit value word (weight 2i in the low nibble of byte
+// i) -> four bf16 pairs in natural order, each the exact e2m1 value.  The
+// magnitudes come from two 8-entry byte tables selected by the codes' low three
+// bits (bf16 high bytes 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80
+// C0: 0, 0.5, 1, 1.5, 2, 3, 4, 6); each code's sign bit moves to bit 7 of its
+// high byte.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t &p01, uint32_t &p23, uint32_t &p45,
+                                               uint32_t &p67) {
+    const uint32_t m = w & 0x77777777u;
+    const uint32_t w4 = w << 4;
+    const uint32_t sa = prmt(w4, w, 0x5140u), sb = prmt(w4, w, 0x7362u);  // element k's sign -> bit 7 of byte k
+    const uint32_t hia = prmt(0x3F3F3F00u, 0x40404040u, m) | (sa & 0x80808080u);
+    const uint32_t loa = prmt(0xC0800000u, 0xC0804000u, m);
+    const uint32_t hib = prmt(0x3F3F3F00u, 0x40404040u, m >> 16) | (sb & 0x80808080u);
+    const uint32_t lob = prmt(0xC0800000u, 0xC0804000u, m >> 16);
+    p01 = prmt(loa, hia, 0x5140u);
+    p23 = prmt(loa, hia, 0x7362u);
+    p45 = prmt(lob, hib, 0x5140u);
+    p67 = prmt(lob, hib, 0x7362u);
+}
+
+// e4m3 (finite variant) -> fp32, exact (through the exact e4m3 -> fp16 conversion)
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(b & 0xFFu), __NV_E4M3);
+    return __half2float(__half(h));
 }
 
 // ------------------------------------------------------------- tensor core

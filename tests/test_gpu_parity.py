@@ -6,6 +6,8 @@ within 1e-2; routing is bit-exact.  Full-size workloads are checked on sampled
 output rows (the oracle computes those rows one by one), in the launch
 configuration the benchmark times.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -26,6 +28,9 @@ TOL_FFN_TC = 3 * TOL_TC
 # only the fp32 scaling and the fp32 sum over K/32 terms differ from the oracle's
 # fp64 (at most ~(K/32) * 2^-24 of the sum of |terms|, typically far less)
 TOL_X8 = TOL_SMALL / 10
+# NVFP4: every weight enters the MMA as its exact bf16 value (e2m1 * e4m3), so
+# only the fp32 accumulation order and the final multiplication by g differ
+TOL_FP4 = TOL_SMALL / 10
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -763,3 +768,88 @@ def test_gemm_x8_batch_invariant_and_close_to_bf16(ref):
     yb = ref.gemm(w, N, K, x)
     # |sum w (x - xh)| <= sum |w| * s / 2 per row; checked in aggregate
     assert G.rel_err(ym, yb) <= 2e-2
+
+
+# ------------------------------------------------------------------- NVFP4
+@functools.lru_cache(maxsize=8)
+def fp4_weights(stream: int, N: int, K: int):
+    import synth
+    return synth.nvfp4_weights(synth.seed(7, stream), N, K)
+
+
+def gpu_nvfp4_dequant(w, g, N, K):
+    out = torch.full((N, K), float("nan"), dtype=torch.float32, device="cuda")
+    q4k.q4k_nvfp4_dequant(G.dev(w), g, N, K, out)
+    torch.cuda.synchronize()
+    return G.host(out)
+
+
+def gpu_nvfp4_gemm(w, g, N, K, x, ldx=None, ldy=None, w_dev=None):
+    M = x.shape[0]
+    ldx, ldy = ldx or K, ldy or N
+    xp = np.zeros((M, ldx), np.uint16)
+    xp[:, :K] = x
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    q4k.q4k_nvfp4_gemm(w_dev if w_dev is not None else G.dev(w), g, N, K, G.dev(xp), M, ldx, y, ldy)
+    torch.cuda.synchronize()
+    out = G.host(y)
+    if ldy > N:
+        assert np.all(np.isnan(out[:, N:]))
+    return out[:, :N]
+
+
+def _same_bits(a, b):
+    a, b = np.asarray(a, np.float32), np.asarray(b, np.float32)
+    na, nb = np.isnan(a), np.isnan(b)
+    return np.array_equal(na, nb) and np.array_equal(a[~na].view(np.uint32), b[~nb].view(np.uint32))
+
+
+def test_nvfp4_dequant_bitexact(ref):
+    N, K = 64, 512
+    w, g = fp4_weights(0, N, K)
+    w = w.copy()
+    blk = w.reshape(N, K // 256, 144)
+    blk[0, 0, :16] = [0x01, 0x07, 0x08, 0x38, 0x7E, 0x7F, 0x00, 0x40] * 2   # subnormal, 1, 448, NaN, 0 scales
+    blk[1, 1, 16:] = np.arange(128, dtype=np.uint8) * 2 + 1                   # every code in both nibbles
+    got = gpu_nvfp4_dequant(w, float(g), N, K)
+    assert _same_bits(got, ref.nvfp4_dequant(w, float(g), N, K))
+    rows = G.sample_rows(5120, 48, seed=1)
+    wl, gl = fp4_weights(1, 5120, 17408)
+    got = gpu_nvfp4_dequant(G.rows_of(wl, rows), float(gl), len(rows), 17408)
+    assert _same_bits(got, ref.nvfp4_dequant(G.rows_of(wl, rows), float(gl), len(rows), 17408))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 1024), (17, 200, 768), (128, 384, 2048), (200, 1000, 4096),
+                                   (33, 640, 4096)])
+def test_nvfp4_gemm_parity(ref, M, N, K):
+    # M <= 128: 128-token tiles; (33, 640, 4096): few tiles, so the cluster K split runs
+    w, g = fp4_weights(2, N, K)
+    x = G.activations(7, 3, M, K)
+    y = gpu_nvfp4_gemm(w, float(g), N, K, x, ldx=K + 8, ldy=N + 4)
+    want = ref.nvfp4_gemm(w, float(g), N, K, x, threads=16)
+    err = G.rel_err(y, want)
+    assert err <= TOL_FP4, err
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
+def test_nvfp4_gemm_full_size(ref, N, K):
+    # the prefill shapes at M = 1024, sampled output rows
+    M = 1024
+    w, g = fp4_weights(4, N, K)
+    x = G.activations(7, 5, M, K)
+    y = gpu_nvfp4_gemm(w, float(g), N, K, x)
+    rows = G.sample_rows(N, 32, seed=2)
+    toks = G.sample_rows(M, 64, seed=3)
+    want = ref.nvfp4_gemm(G.rows_of(w, rows), float(g), len(rows), K, x[toks], threads=16)
+    err = G.rel_err(y[np.ix_(toks, rows)], want)
+    assert err <= TOL_FP4, err
+
+
+def test_nvfp4_gemm_deterministic():
+    N, K, M = 640, 4096, 300
+    w, g = fp4_weights(5, N, K)
+    wd = G.dev(w)
+    x = G.activations(7, 6, M, K)
+    a = gpu_nvfp4_gemm(w, float(g), N, K, x, w_dev=wd)
+    b = gpu_nvfp4_gemm(w, float(g), N, K, x, w_dev=wd)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

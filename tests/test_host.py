@@ -116,6 +116,13 @@ A16 = 1 << 20  # a 16-byte aligned fake address; never dereferenced by these cal
     (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 17, A16, 4, None), q4k.Q4K_ERR_SHAPE),
     (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 0, A16, 4, None), q4k.Q4K_ERR_SHAPE),
     (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16 + 4, 1, A16, 4, None), q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_nvfp4_dequant(None, 1.0, 4, 256, A16, None), q4k.Q4K_ERR_NULL),
+    (lambda L: L.q4k_nvfp4_dequant(A16, 1.0, 4, 200, A16, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_nvfp4_dequant(A16 + 4, 1.0, 4, 256, A16, None), q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_nvfp4_gemm(A16, 1.0, 4, 256, None, 2, 256, A16, 4, None), q4k.Q4K_ERR_NULL),
+    (lambda L: L.q4k_nvfp4_gemm(A16, 1.0, 4, 256, A16, 0, 256, A16, 4, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_nvfp4_gemm(A16, 1.0, 4, 256, A16, 2, 128, A16, 4, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_nvfp4_gemm(A16, 1.0, 4, 256, A16 + 8, 2, 256, A16, 4, None), q4k.Q4K_ERR_ALIGN),
 ])
 def test_argument_errors_before_any_device_work(lib, call, status):
     assert call(lib) == status
