@@ -14,7 +14,8 @@ tokens, default 2048) and `moe_ffn` (the same layer as one routed SwiGLU expert
 feed-forward call: gate, up with the SwiGLU epilogue, down on the bf16 h rows,
 weighted combine), `decode_x8` (the decode step with int8 activations:
 per-32 quantization of each matrix's input, then the int8 GEMV) and
-`prefill_nvfp4` (the prefill GEMMs with NVFP4 weights, --m tokens).
+`prefill_nvfp4` / `decode_nvfp4` (the prefill GEMMs and the decode GEMVs
+with NVFP4 weights).
 
 Timing: W warm-up steps, then exactly K steps between a barrier plus
 cudaDeviceSynchronize on both sides, timed with CUDA events on the launching
@@ -190,6 +191,15 @@ class Workload:
                                                                          10.0, synth.seed(3, 9)),
                           synth.normal_bf16(synth.seed(3, 6), m * 17408).reshape(m, 17408))]
             self.unit, self.config = "TFLOP/s", {"workload": f"prefill GEMM M={m}: K5120->N17408 then K17408->N5120"}
+        elif name == "decode_nvfp4":
+            mats = []
+            for tag, N, K, sw, sx in (("gate_up_fp4", 17408, 5120, 10, 11), ("down_fp4", 5120, 17408, 12, 13)):
+                blocks, g = synth.nvfp4_weights(synth.seed(8, sw), N, K)
+                self.fp4[tag] = float(g)
+                mats.append((tag, N, K, 1, blocks, synth.normal_bf16(synth.seed(8, sx), K).reshape(1, K)))
+            self.mats = mats
+            self.unit, self.config = "GB/s", {"workload": "decode GEMV M=1 with NVFP4 weights: K5120->N17408 then "
+                                                          "K17408->N5120"}
         elif name == "prefill_nvfp4":
             mats = []
             for tag, N, K, sw, sx in (("prefill_up_fp4", 17408, 5120, 0, 1), ("prefill_down_fp4", 5120, 17408, 5, 6)):
@@ -610,15 +620,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "decode_x8", "verify", "prefill", "prefill_nvfp4", "moe",
-                                           "moe_ffn"],
+    ap.add_argument("--workload", choices=["decode", "decode_x8", "decode_nvfp4", "verify", "prefill",
+                                           "prefill_nvfp4", "moe", "moe_ffn"],
                     default="decode")
     ap.add_argument("--m", type=int, default=None, help="tokens (verify: 4, prefill: 4096, moe: 2048)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.m is None:
-        args.m = {"decode": 1, "decode_x8": 1, "verify": 4, "prefill": 4096, "prefill_nvfp4": 4096, "moe": 2048,
+        args.m = {"decode": 1, "decode_x8": 1, "decode_nvfp4": 1, "verify": 4, "prefill": 4096, "prefill_nvfp4": 4096, "moe": 2048,
                   "moe_ffn": 2048}[args.workload]
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -324,7 +324,11 @@ q4k_status q4k_nvfp4_gemm(const void *w, float g, int64_t N, int64_t K, const ui
     DeviceInfo di;
     q4k_status st = check_device(&di);
     if (st != Q4K_OK) return st;
-    cudaError_t e = launch_gemm_tc_nvfp4(di, w, g, N, K, x, M, ldx, y, ldy, static_cast<cudaStream_t>(stream));
+    // M <= 16: the small-M kernel in its NVFP4 mode; otherwise the tensor-core kernel
+    cudaError_t e = M <= 16 ? launch_smallm_fp4(di, w, g, N, K, x, M, ldx, y, ldy,
+                                                g_static_weights.load(std::memory_order_relaxed) != 0,
+                                                static_cast<cudaStream_t>(stream))
+                            : launch_gemm_tc_nvfp4(di, w, g, N, K, x, M, ldx, y, ldy, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 

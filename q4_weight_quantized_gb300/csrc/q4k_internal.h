@@ -40,6 +40,11 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
 cudaError_t launch_smallm_x8(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const int8_t *q,
                              const float *sx, int64_t M, float *y, int64_t ldy, bool early_weights, cudaStream_t s);
 
+// M in [1, 16] with NVFP4 weights (same 144-byte block size), y = g * (x . W^T)
+// (smallm.cu, FP4 mode).
+cudaError_t launch_smallm_fp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K, const uint16_t *x,
+                              int64_t M, int64_t ldx, float *y, int64_t ldy, bool early_weights, cudaStream_t s);
+
 // Per-32 int8 quantization of bf16 rows (x8.cu).
 cudaError_t launch_quantize_x8(const DeviceInfo &di, const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q,
                                float *sx, cudaStream_t s);

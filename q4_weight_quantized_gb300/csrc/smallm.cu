@@ -287,6 +287,69 @@ __device__ __forceinline__ void block_mma_x8(const uint8_t *wst, const uint8_t *
     }
 }
 
+// NVFP4 weights (144-byte blocks: 16 e4m3 scales, then 128 bytes of e2m1 pairs,
+// weight 2i in the low nibble of byte i).  Each operand element is the exact
+// bf16 value e4m3 * e2m1, so the MMAs accumulate w . x straight into the fp32
+// accumulators (no per-sub-block scaling; the tensor scale is applied by the
+// epilogue).  The fragment walk of block_mma: per g, a lane holds x for weights
+// 64g + 8c .. +7 (xl) and 64g + 32 + 8c .. +7 (xh); their codes are the value
+// words at bytes 32g + 4c and 32g + 16 + 4c, their scales 4g + c/2 and 4g + 2 + c/2.
+template <int NT, bool ONE, int RT>
+__device__ __forceinline__ void block_mma_fp4(const uint8_t *wst, const uint8_t *xs, const bool (&live)[NT],
+                                              float (&acc)[RT][NT][4], int r, int c) {
+    constexpr int kRowTiles = RT;
+    auto scale2 = [](uint32_t sc4, int i) -> uint32_t {  // e4m3 byte i -> bf16 pair (exact)
+        const float f = e4m3_to_f32(sc4 >> (8 * i));
+        const __nv_bfloat162 v = __floats2bfloat162_rn(f, f);
+        return *reinterpret_cast<const uint32_t *>(&v);
+    };
+    auto mul2 = [](uint32_t a, uint32_t b) -> uint32_t {
+        const __nv_bfloat162 v =
+            __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&a), *reinterpret_cast<const __nv_bfloat162 *>(&b));
+        return *reinterpret_cast<const uint32_t *>(&v);
+    };
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint32_t xl[NT][4], xh[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+            if (live[nt]) {
+                const uint8_t *xp = xs + (nt * 8 + r) * kXBlkBytes + 128 * g + 16 * c;
+                a = *reinterpret_cast<const uint4 *>(xp);
+                b = *reinterpret_cast<const uint4 *>(xp + 64);
+            }
+            xl[nt][0] = a.x; xl[nt][1] = a.y; xl[nt][2] = a.z; xl[nt][3] = a.w;
+            xh[nt][0] = b.x; xh[nt][1] = b.y; xh[nt][2] = b.z; xh[nt][3] = b.w;
+        }
+#pragma unroll
+        for (int rt = 0; rt < kRowTiles; ++rt) {
+            const uint8_t *pa = wst + (rt * 16 + r) * kBlockBytes, *pb = pa + 8 * kBlockBytes;
+            const uint32_t sa = *reinterpret_cast<const uint32_t *>(pa + 4 * g);
+            const uint32_t sb = *reinterpret_cast<const uint32_t *>(pb + 4 * g);
+            const uint32_t sal = scale2(sa, c >> 1), sah = scale2(sa, 2 + (c >> 1));
+            const uint32_t sbl = scale2(sb, c >> 1), sbh = scale2(sb, 2 + (c >> 1));
+            uint32_t a01, a23, a45, a67, b01, b23, b45, b67;
+            uint32_t alo0[4], alo1[4], ahi0[4], ahi1[4];
+            e2m1x8_to_bf16(*reinterpret_cast<const uint32_t *>(pa + 16 + 32 * g + 4 * c), a01, a23, a45, a67);
+            e2m1x8_to_bf16(*reinterpret_cast<const uint32_t *>(pb + 16 + 32 * g + 4 * c), b01, b23, b45, b67);
+            alo0[0] = mul2(a01, sal); alo0[1] = mul2(b01, sbl); alo0[2] = mul2(a23, sal); alo0[3] = mul2(b23, sbl);
+            alo1[0] = mul2(a45, sal); alo1[1] = mul2(b45, sbl); alo1[2] = mul2(a67, sal); alo1[3] = mul2(b67, sbl);
+            e2m1x8_to_bf16(*reinterpret_cast<const uint32_t *>(pa + 32 + 32 * g + 4 * c), a01, a23, a45, a67);
+            e2m1x8_to_bf16(*reinterpret_cast<const uint32_t *>(pb + 32 + 32 * g + 4 * c), b01, b23, b45, b67);
+            ahi0[0] = mul2(a01, sah); ahi0[1] = mul2(b01, sbh); ahi0[2] = mul2(a23, sah); ahi0[3] = mul2(b23, sbh);
+            ahi1[0] = mul2(a45, sah); ahi1[1] = mul2(b45, sbh); ahi1[2] = mul2(a67, sah); ahi1[3] = mul2(b67, sbh);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mma_bf16_16816(acc[rt][nt], alo0, xl[nt][0], xl[nt][1], acc[rt][nt]);
+                mma_bf16_16816(acc[rt][nt], alo1, xl[nt][2], xl[nt][3], acc[rt][nt]);
+                mma_bf16_16816(acc[rt][nt], ahi0, xh[nt][0], xh[nt][1], acc[rt][nt]);
+                mma_bf16_16816(acc[rt][nt], ahi1, xh[nt][2], xh[nt][3], acc[rt][nt]);
+            }
+        }
+    }
+}
+
 
 // Where each token slot of a chunk reads its activation row and writes its
 // output row.  Dense: slot n is token n.  MoE: slot n of a token tile is the
@@ -311,6 +374,7 @@ struct RowArgs {
     const int32_t *ids;
     int E;
     GluOut glu;  // MoE with GLU: h (bf16) receives the SwiGLU of the gate and up projections
+    float gscale;  // FP4: the weights' tensor scale, applied to the outputs
     const float *gates;  // MoE with DC: the combine weights [T][topk]
 };
 
@@ -353,8 +417,10 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // X8 (dense): int8 activations with per-32 fp32 scales (tmX: the int8 rows,
 // tmAux: the scale rows), multiplied through block_mma_x8.
 // tmAux: GLU: the up matrix; X8: the activation scales; otherwise unused.
+// FP4 (dense): NVFP4 weights in the same 144-byte blocks (block_mma_fp4), the
+// outputs multiplied by RowArgs::gscale.
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
-          bool DC = false, bool X8 = false>
+          bool DC = false, bool X8 = false, bool FP4 = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmAux,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
@@ -375,6 +441,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     static_assert(!GLU || MOE, "the fused gate and up projections are a MoE mode");
     static_assert(!DC || (MOE && !RS && !GLU && NT == 1 && ONE), "the in-CTA combine is a one-token MoE mode");
     static_assert(!X8 || !MOE, "int8 activations are a dense mode");
+    static_assert(!FP4 || (!MOE && !X8), "NVFP4 weights are a dense bf16 mode");
     // activation bytes copied per token slot and block: 512 bf16, or 256 int8 + 32 of scales
     constexpr int kXTx = X8 ? 256 + 32 : kXBlkBytes;
     // GLU: the warp pair of matrix `mat` (0 gate, 1 up); wsub = this warp's index in its pair
@@ -529,13 +596,18 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             }
             const uint8_t *wst = region + slot * sbytes;
             const uint8_t *xs = wst + kBlkWBytes;
-            decode_scales<X8>(wst + lane * kBlockBytes, table + lane * (kTableRowBytes / 4));
-            if constexpr (kRows > 32) {
-                if (lane < kRows - 32)
-                    decode_scales<X8>(wst + (lane + 32) * kBlockBytes, table + (lane + 32) * (kTableRowBytes / 4));
+            if constexpr (!FP4) {
+                decode_scales<X8>(wst + lane * kBlockBytes, table + lane * (kTableRowBytes / 4));
+                if constexpr (kRows > 32) {
+                    if (lane < kRows - 32)
+                        decode_scales<X8>(wst + (lane + 32) * kBlockBytes,
+                                          table + (lane + 32) * (kTableRowBytes / 4));
+                }
             }
             __syncwarp();
-            if constexpr (X8)
+            if constexpr (FP4)
+                block_mma_fp4<NT, ONE, kRowTiles>(wst, xs, live, acc, r, c);
+            else if constexpr (X8)
                 block_mma_x8<NT, ONE, kRowTiles>(wst, xs, table, live, nvalid, acc, r, c);
             else
                 block_mma<NT, ONE, kRowTiles>(wst, xs, table, live, acc, r, c);
@@ -690,7 +762,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
                 float v = red[e];
                 for (int q = 1; q < S; ++q) v += ld_shared_cluster_f32(map_shared_rank(base + 4 * e, q));
                 const int tk = e / kRows, rr = e % kRows;
-                if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = v;
+                if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = FP4 ? ra.gscale * v : v;
             }
         }
         cluster_sync();  // keep every CTA's shared memory alive until rank 0 has read it
@@ -698,18 +770,18 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         __syncthreads();
         for (int e = threadIdx.x; e < elems; e += kThreads) {
             const int tk = e / kRows, rr = e % kRows;
-            if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = red[e];
+            if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = FP4 ? ra.gscale * red[e] : red[e];
         }
     }
 }
 
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
-          bool DC = false, bool X8 = false>
+          bool DC = false, bool X8 = false, bool FP4 = false>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status,
                        const CUtensorMap *tmAux = nullptr) {
     const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU, DC, X8>;
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU, DC, X8, FP4>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmAux ? *tmAux : tmW, tmX,
@@ -788,6 +860,41 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
     if (M == 1) return launch_cfg<1, false, true, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
     if (M <= 8) return launch_cfg<1, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
     return launch_cfg<2, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+}
+
+cudaError_t launch_smallm_fp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K, const uint16_t *x,
+                              int64_t M, int64_t ldx, float *y, int64_t ldy, bool early_weights, cudaStream_t s) {
+    const int KB = (int)(K / kQK);
+    const Split sp = split_for(di, N, KB);
+    const int S = sp.S, tiles = (int)((N + sp.rows - 1) / sp.rows);
+    CUtensorMap tmW, tmX;
+    cudaError_t e = make_weight_tmap(&tmW, w, N, K, sp.rows, kBlkWords);
+    if (e != cudaSuccess) return e;
+    e = make_act_tmap(&tmX, x, M, K, ldx, kQK / 4);
+    if (e != cudaSuccess) return e;
+    RowArgs ra = {};
+    ra.y = y; ra.ldy = ldy; ra.M = (int)M;
+    ra.early_w = early_weights ? 1 : 0;
+    ra.gscale = g;
+    const int nx = (int)M, n = (int)N;
+    if (sp.rows == 48) {
+        if (M == 1)
+            return launch_cfg<1, false, true, 2, 48, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX,
+                                                                                          ra, n, KB, di.status);
+        if (M <= 8)
+            return launch_cfg<1, false, false, 2, 48, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW,
+                                                                                           tmX, ra, n, KB, di.status);
+        return launch_cfg<2, false, false, 2, 48, false, 16, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX,
+                                                                                        ra, n, KB, di.status);
+    }
+    if (M == 1)
+        return launch_cfg<1, false, true, 2, 32, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra,
+                                                                                      n, KB, di.status);
+    if (M <= 8)
+        return launch_cfg<1, false, false, 2, 32, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX,
+                                                                                       ra, n, KB, di.status);
+    return launch_cfg<2, false, false, 2, 32, false, 16, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra,
+                                                                                    n, KB, di.status);
 }
 
 cudaError_t launch_smallm_x8(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const int8_t *q,

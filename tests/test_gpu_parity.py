@@ -853,3 +853,32 @@ def test_nvfp4_gemm_deterministic():
     a = gpu_nvfp4_gemm(w, float(g), N, K, x, w_dev=wd)
     b = gpu_nvfp4_gemm(w, float(g), N, K, x, w_dev=wd)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 9, 16])
+def test_nvfp4_small_m_ragged(ref, M):
+    # M <= 16: the small-M kernel's NVFP4 mode (exact bf16 operands, no scale table)
+    N, K = 200, 1024
+    w, g = fp4_weights(6, N, K)
+    x = G.activations(7, 7, M, K)
+    y = gpu_nvfp4_gemm(w, float(g), N, K, x, ldx=K + 16, ldy=N + 8)
+    err = G.rel_err(y, ref.nvfp4_gemm(w, float(g), N, K, x))
+    assert err <= TOL_FP4, err
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)], ids=["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 4])
+def test_nvfp4_decode_full_size(ref, N, K, M):
+    # decode and verify shapes (the down projection splits K over a cluster), sampled rows;
+    # rows of the M-token call equal the 1-token call bit for bit
+    w, g = fp4_weights(8, N, K)
+    wd = G.dev(w)
+    x = G.activations(7, 8, M, K)
+    y = gpu_nvfp4_gemm(w, float(g), N, K, x, w_dev=wd)
+    rows = G.sample_rows(N, 64, seed=M + 7)
+    want = ref.nvfp4_gemm(G.rows_of(w, rows), float(g), len(rows), K, x, threads=16)
+    err = G.rel_err(y[:, rows], want)
+    assert err <= TOL_FP4, err
+    if M > 1:
+        y1 = gpu_nvfp4_gemm(w, float(g), N, K, x[M - 1:M], w_dev=wd)
+        assert np.array_equal(y1[0].view(np.uint32), y[M - 1].view(np.uint32))
