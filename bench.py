@@ -57,6 +57,25 @@ def env_rank():
         int(os.environ.get("WORLD_SIZE", "1"))
 
 
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The maximum of a per-rank time over all ranks (each rank is an independent
+    replica; the job is as slow as its slowest rank).  World size 1: v itself."""
+    if world <= 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(per_step_value: float, world: int) -> float:
+    """Whole-job throughput: every rank processes the same per-step work (weak
+    scaling), so the job's value is the per-rank value at the max-over-ranks time
+    times the number of ranks."""
+    return per_step_value * world
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -460,10 +479,7 @@ def run_gpu(args, rank, local_rank, world):
             torch.cuda.synchronize()
             kernel_ms.append(k0.elapsed_time(k1) / (reps * gr.R))
 
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, device)
 
     # end to end through the public API: activations from pinned host memory,
     # outputs back to pinned host memory, every step
@@ -493,18 +509,15 @@ def run_gpu(args, rank, local_rank, world):
             e1.record(stream)
             torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], dtype=torch.float64, device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": wl.value(ems / 1e3 / e2e_steps) * world, "unit": wl.unit,
+        ems = max_over_ranks(ems, world, device)
+        e2e = {"value": job_value(wl.value(ems / 1e3 / e2e_steps), world), "unit": wl.unit,
                "h2d_bytes_per_step": int(sum(x.nbytes for (*_, x) in wl.mats)),
                "d2h_bytes_per_step": int(sum(y.numel() * 4 for y in gr.y)), "steps": e2e_steps}
 
     hbm, bf16, bf16_s, src = peaks()
     sec_per_step = ms / 1e3 / args.steps
     line = {
-        "metric": METRIC, "value": wl.value(sec_per_step) * world, "unit": wl.unit, "n_gpus": world,
+        "metric": METRIC, "value": job_value(wl.value(sec_per_step), world), "unit": wl.unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("int8 (per-32 fp32 scales) x Q4_K -> fp32" if wl.x8 else
