@@ -515,18 +515,18 @@ def _fma_f32(a: float, b: float, c: float) -> float:
     return best
 
 
-@pytest.mark.parametrize("T", [1, 2])
-def test_moe_combine_in_cta_same_bits(syn, moe_down, T):
+@pytest.mark.parametrize("T,x_mode", [(1, 1), (2, 1), (2, 0)])
+def test_moe_combine_in_cta_same_bits(syn, moe_down, T, x_mode):
     # up to 16 items: the down projection sums the slots in the CTA; the result must be
     # the fp32 fma chain over the per-slot rows in slot order, invalid ids skipped
     N, K = G.MOE_DOWN
     E, topk = G.MOE_E, G.MOE_TOPK
     ids, gates = syn.routing(syn.seed(4, 2) + 50 + T, syn.seed(4, 3) + 50 + T, T, E, topk)
     ids[0, 5] = -1
-    x = G.activations(4, 9, T * topk, K)
+    x = G.activations(4, 9, T * topk if x_mode else T, K)
     w = G.dev(moe_down)
-    y = run_moe(None, E, N, K, x, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_COMBINE, w_dev=w)
-    o = run_moe(None, E, N, K, x, q4k.Q4K_MOE_X_PER_SLOT, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT, w_dev=w)
+    y = run_moe(None, E, N, K, x, x_mode, ids, gates, q4k.Q4K_MOE_Y_COMBINE, w_dev=w)
+    o = run_moe(None, E, N, K, x, x_mode, ids, gates, q4k.Q4K_MOE_Y_PER_SLOT, w_dev=w)
     cols = G.sample_rows(N, 48, seed=T)
     for t in range(T):
         for n in cols:
