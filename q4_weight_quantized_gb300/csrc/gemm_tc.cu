@@ -46,17 +46,23 @@ constexpr int kABytes = kTileRows * kStageK * 2;  // 16 KiB dequantized operand 
 constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K tile per block
 constexpr int kThreads = 192;
 
+// Two stage rings: activations (XS deep) and dequantized weights (NS deep).  The
+// activation copy of stage i can only start once the MMAs of stage i - XS are
+// done, and it crosses L2, so that ring is the deeper one: XS stages of MMA
+// time must cover an L2 round trip under load.
 template <int BN>
 struct Cfg {
-    static constexpr int NS = BN == 256 ? 3 : 4;  // pipeline stages
+    static constexpr int NS = BN == 256 ? 3 : 4;  // dequantized-weight stages
+    static constexpr int XS = BN == 256 ? 4 : 6;  // activation stages
     static constexpr int XB = BN * kStageK * 2;   // activation bytes per stage
     static constexpr int x_off = 0;
-    static constexpr int a_off = NS * XB;
+    static constexpr int a_off = XS * XB;
     static constexpr int raw_off = a_off + NS * kABytes;
     static constexpr int bar_off = raw_off + 2 * kRawBytes;
-    static constexpr int n_bars = 3 * NS + 5;
+    static constexpr int n_bars = 2 * NS + 2 * XS + 5;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;  // + slack to align the base to 1024
+    static_assert(bytes <= 227 * 1024, "dynamic shared memory per CTA");
 };
 
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<__nv_bfloat162 *>(&u); }
@@ -84,18 +90,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     pdl_wait();  // the activations may come from the previous kernel
     pdl_trigger();
     using C = Cfg<BN>;
-    constexpr int NS = C::NS;
+    constexpr int NS = C::NS, XS = C::XS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *xs = base + C::x_off;
     uint8_t *as = base + C::a_off;
     uint8_t *raw = base + C::raw_off;
     const uint32_t bar = smem_u32(base + C::bar_off);
-    // full: the four dequant warps wrote the stage's operand; xfull: its activation
-    // copy landed (tx bytes); empty: the MMAs reading the stage are done; rfull /
-    // rempty: the raw Q4_K tile ring; accfull: all MMAs of the tile are done
-    const uint32_t full0 = bar, empty0 = bar + 8 * NS, xfull0 = bar + 16 * NS, rfull0 = bar + 24 * NS,
-                   rempty0 = rfull0 + 16, accfull = rempty0 + 16;
+    // full: the four dequant warps wrote the stage's operand; empty: the MMAs reading
+    // it are done; xfull: an activation stage's copy landed (tx bytes); xempty: the
+    // MMAs reading it are done; rfull / rempty: the raw tile ring; accfull: all MMAs
+    // of the tile are done
+    const uint32_t full0 = bar, empty0 = bar + 8 * NS, xfull0 = bar + 16 * NS, xempty0 = xfull0 + 8 * XS,
+                   rfull0 = xempty0 + 8 * XS, rempty0 = rfull0 + 16, accfull = rempty0 + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + C::misc_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::misc_off + 4);
 
@@ -111,8 +118,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 4);   // the four dequant warps
-            mbar_init(xfull0 + 8 * s, 1);  // producer (+ tx bytes)
             mbar_init(empty0 + 8 * s, 1);  // tcgen05.commit
+        }
+        for (int s = 0; s < XS; ++s) {
+            mbar_init(xfull0 + 8 * s, 1);   // producer (+ tx bytes)
+            mbar_init(xempty0 + 8 * s, 1);  // tcgen05.commit
         }
         for (int r = 0; r < 2; ++r) {
             mbar_init(rfull0 + 8 * r, 1);
@@ -140,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tma_load_2d(smem_u32(raw), &tmW, kbeg * (kBlockBytes / 4), n0, rfull0);
             int raw_issued = 1, x_issued = 0;
             for (int i = 0; i < total && !*abort_flag; ++i) {
-                const int kb = i >> 2, g = i & 3, s = i % NS;
+                const int kb = i >> 2, g = i & 3, s = i % XS;
                 if (g == 0 && kb + 1 < KBs) {  // raw tile of the next block, one block ahead
                     const int r = (kb + 1) & 1;
                     if (kb + 1 >= 2 && !mbar_wait(rempty0 + 8 * r, (((kb + 1) >> 1) - 1) & 1, status)) {
@@ -152,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                                 rfull0 + 8 * r);
                     ++raw_issued;
                 }
-                if (i >= NS && !mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status)) {
+                if (i >= XS && !mbar_wait(xempty0 + 8 * s, ((i / XS) - 1) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -164,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 // a wait gave up somewhere: wait (bounded) for this CTA's copies still in flight
                 for (int j = raw_issued > 2 ? raw_issued - 2 : 0; j < raw_issued; ++j)
                     (void)mbar_wait(rfull0 + 8 * (j & 1), (j >> 1) & 1, status);
-                for (int j = x_issued > NS ? x_issued - NS : 0; j < x_issued; ++j)
-                    (void)mbar_wait(xfull0 + 8 * (j % NS), (j / NS) & 1, status);
+                for (int j = x_issued > XS ? x_issued - XS : 0; j < x_issued; ++j)
+                    (void)mbar_wait(xfull0 + 8 * (j % XS), (j / XS) & 1, status);
             }
         }
     } else if (warp == 1) {
@@ -173,18 +183,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, BN);
             for (int i = 0; i < total; ++i) {
-                const int s = i % NS;
-                if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status) || !mbar_wait(xfull0 + 8 * s, (i / NS) & 1, status)) {
+                const int s = i % NS, sx = i % XS;
+                if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status) ||
+                    !mbar_wait(xfull0 + 8 * sx, (i / XS) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
                 const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kABytes));
-                const uint64_t bd = umma_desc_sw128(smem_u32(xs + s * C::XB));
+                const uint64_t bd = umma_desc_sw128(smem_u32(xs + sx * C::XB));
 #pragma unroll
                 for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
                     umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
                 umma_commit(empty0 + 8 * s);
+                umma_commit(xempty0 + 8 * sx);
             }
             // completes once every MMA issued above has (also after an abort, so
             // that tensor memory is freed only after the MMAs that write it)
