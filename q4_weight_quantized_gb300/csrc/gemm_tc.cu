@@ -86,8 +86,12 @@ template <int BN, bool FP4 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
                                                               int64_t ldy, int M, int N, int KB, float gscale,
-                                                              unsigned int *status) {
-    pdl_wait();  // the activations may come from the previous kernel
+                                                              int late_wait, unsigned int *status) {
+    // late_wait: this launch is the remainder of a split problem, queued right after
+    // the main launch, which waited for the producers of x and w before letting it
+    // start; it waits for the main launch only before it ends, so that a later
+    // kernel that waits on this one also sees the main launch's outputs
+    if (!late_wait) pdl_wait();  // the activations may come from the previous kernel
     pdl_trigger();
     using C = Cfg<BN>;
     constexpr int NS = C::NS, XS = C::XS;
@@ -349,11 +353,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         tc_fence_after();
         tmem_dealloc(tmem, BN);
     }
+    if (late_wait) pdl_wait();
 }
 
 template <int BN, bool FP4>
 cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s) {
+                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int late_wait = 0) {
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
     if (e != cudaSuccess) return e;
@@ -376,21 +381,46 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     }
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
     return launch_pdl(gemm_tc_kernel<BN, FP4>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
-                      tmX, y, ldy, (int)M, (int)N, KB, g, di.status);
+                      tmX, y, ldy, (int)M, (int)N, KB, g, late_wait, di.status);
+}
+
+// One CTA per SM: when the tiles' last wave would run mostly empty and a row of
+// token tiles is narrow enough for the cluster K split, the last token tiles
+// become a second launch that splits K and fills the idle SMs.  Returns the
+// number of tokens of the main launch (M when nothing is split off).
+int64_t main_part(const DeviceInfo &di, int64_t N, int64_t M) {
+    const int64_t tn = (N + kTileRows - 1) / kTileRows, tm = (M + 255) / 256;
+    const int64_t total = tn * tm, full = total / di.sm_count * di.sm_count, rem = total - full;
+    if (M <= 256 || full == 0 || rem == 0 || 2 * rem > di.sm_count) return M;
+    const int64_t r = (rem + tn - 1) / tn;  // token tiles to peel off
+    if (r >= tm || 2 * r * tn > di.sm_count) return M;  // the remainder must leave room for a K split
+    return (tm - r) * 256;
+}
+
+template <bool FP4>
+cudaError_t launch_split(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
+                         int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s) {
+    if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s);
+    const int64_t m1 = main_part(di, N, M);
+    cudaError_t e = launch_bn<256, FP4>(di, w, N, K, x, m1, ldx, y, ldy, g, s);
+    if (e != cudaSuccess || m1 == M) return e;
+    const int64_t m2 = M - m1;
+    const uint16_t *x2 = x + m1 * ldx;
+    float *y2 = y + m1 * ldy;
+    return m2 <= 128 ? launch_bn<128, FP4>(di, w, N, K, x2, m2, ldx, y2, ldy, g, s, 1)
+                     : launch_bn<256, FP4>(di, w, N, K, x2, m2, ldx, y2, ldy, g, s, 1);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                            int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
-    if (M <= 128) return launch_bn<128, false>(di, w, N, K, x, M, ldx, y, ldy, 1.0f, s);
-    return launch_bn<256, false>(di, w, N, K, x, M, ldx, y, ldy, 1.0f, s);
+    return launch_split<false>(di, w, N, K, x, M, ldx, y, ldy, 1.0f, s);
 }
 
 cudaError_t launch_gemm_tc_nvfp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K,
                                  const uint16_t *x, int64_t M, int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
-    if (M <= 128) return launch_bn<128, true>(di, w, N, K, x, M, ldx, y, ldy, g, s);
-    return launch_bn<256, true>(di, w, N, K, x, M, ldx, y, ldy, g, s);
+    return launch_split<true>(di, w, N, K, x, M, ldx, y, ldy, g, s);
 }
 
 }  // namespace q4k

@@ -274,6 +274,18 @@ def test_prefill_split_k_ragged(ref, M, N, K):
     assert G.rel_err(gpu_gemm(b, N, K, x), ref.gemm(b, N, K, x, threads=16)) <= TOL_TC
 
 
+def test_prefill_last_wave_split(ref):
+    # 160 tiles of 128 x 256 on 152 SMs: the last token tile (ragged, 232 tokens) becomes
+    # a second launch with a cluster K split, which finishes after the main launch
+    M, N, K = 1000, 5120, 2048
+    b = G.weights(3, 7, N, K, outliers=True)
+    x = G.activations(3, 8, M, K)
+    y = gpu_gemm(b, N, K, x)
+    rows = np.unique(np.concatenate([G.sample_rows(N, 24, seed=7), np.arange(N - 8, N)]))
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=16)
+    assert G.rel_err(y[:, rows], want) <= TOL_TC
+
+
 def test_prefill_many_tiles_ragged(ref):
     # more 128 x 256 tiles than SMs, ragged in M (600 = 2*256 + 88) and N (6600 = 51*128 + 72)
     M, N, K = 600, 6600, 1024
