@@ -450,7 +450,9 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const CUtensorMap *tw = mat ? &tmAux : &tmW;
     const int row0 = blockIdx.y * kRows * (RS ? kNw : 1);
     const int wrow0 = row0 + (RS ? wsub * kRows : 0);  // this warp's first row
-    const int kb0 = (int)((int64_t)KB * split / S), kb1 = (int)((int64_t)KB * (split + 1) / S);
+    // the cluster splits K, except in DC mode, where its ranks split the token's slots
+    const int kS = DC ? 1 : S, ksplit = DC ? 0 : split;
+    const int kb0 = (int)((int64_t)KB * ksplit / kS), kb1 = (int)((int64_t)KB * (ksplit + 1) / kS);
     // this warp's blocks: all of them (row split), or blocks wsub, wsub+kNw, ... of the split
     const int nblk = RS || DC ? kb1 - kb0 : (kb1 - kb0 > wsub ? (kb1 - kb0 - wsub + kNw - 1) / kNw : 0);
     const int kb_first = RS || DC ? kb0 : kb0 + wsub, kb_step = RS || DC ? 1 : kNw;
@@ -461,9 +463,10 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     // its chunks are the valid ones, in order
     unsigned dc_mask = 0;
     if constexpr (DC) {
-        const int j = warp + kWarps * lane;
+        // warp w of cluster rank q takes slots q*4 + w + 4*S*i
+        const int j = split * kWarps + warp + kWarps * S * lane;
         bool v = false;
-        if (lane < 4 && j < ra.topk) {
+        if (lane < 16 && j < ra.topk) {
             const int e = __ldg(ra.ids + (int)blockIdx.z * ra.topk + j);
             v = e >= 0 && e < ra.E;
         }
@@ -506,7 +509,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     auto dc_slot = [&](int ch) {
         unsigned m = dc_mask;
         for (int i = 0; i < ch; ++i) m &= m - 1;  // drop the ch lowest valid slots
-        return warp + kWarps * (__ffs(m) - 1);
+        return split * kWarps + warp + kWarps * S * (__ffs(m) - 1);
     };
 
     const int sbytes = G::slot_bytes(nx);
@@ -711,19 +714,28 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     }
     if (aborted) drain_ring<SLOTS>(bar0, it, min(total, it + SLOTS), status);
     if constexpr (DC) {
-        // the weighted combine of token t over its slots, in slot order
-        __syncthreads();
+        // the weighted combine of token t over its slots, in slot order; slot j's
+        // rows were staged at index j by the cluster rank that owns it ((j / 4) % S),
+        // and rank 0 reads the other ranks' over distributed shared memory
+        if (S > 1) cluster_sync();
+        else __syncthreads();
         const int t = blockIdx.z;
-        if (!*(volatile int *)&abort_flag && threadIdx.x < kRows && row0 + (int)threadIdx.x < N) {
-            const float *o = reinterpret_cast<const float *>(smem + G::red_off(nx, SLOTS));
+        if (split == 0 && !*(volatile int *)&abort_flag && threadIdx.x < kRows && row0 + (int)threadIdx.x < N) {
+            const uint32_t o = smem_u32(smem + G::red_off(nx, SLOTS)) + 4u * threadIdx.x;
             float v = 0.0f;
             for (int j = 0; j < ra.topk; ++j) {
                 const int e = __ldg(ra.ids + t * ra.topk + j);
                 if (e < 0 || e >= ra.E) continue;
-                v = fmaf(__ldg(ra.gates + t * ra.topk + j), o[j * kRows + threadIdx.x], v);
+                const uint32_t a = o + 4u * (uint32_t)(j * kRows);
+                const int owner = (j / kWarps) % S;
+                const float oj = owner == 0 ? *reinterpret_cast<const float *>(smem + G::red_off(nx, SLOTS) +
+                                                                                4 * (j * kRows + threadIdx.x))
+                                            : ld_shared_cluster_f32(map_shared_rank(a, owner));
+                v = fmaf(__ldg(ra.gates + t * ra.topk + j), oj, v);
             }
             ra.y[(long long)t * ra.ldy + row0 + threadIdx.x] = v;
         }
+        if (S > 1) cluster_sync();  // keep every rank's stage alive until rank 0 has read it
         return;
     }
     if constexpr (MOE) return;
@@ -1013,11 +1025,12 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
     const int layers = ra.direct ? (int)items : (int)moe_max_tiles(E, items) + (zero_invalid ? 1 : 0);
     const int nx1 = ra.direct ? 1 : 0;  // a direct layer has one token: one activation row per slot
     if (ra.direct && gates && !fused) {
-        // the weighted combine in the CTA: one grid layer per token, 32-row CTAs
+        // the weighted combine in the CTA: one grid layer per token, 32-row CTAs in
+        // clusters of two that split the token's slots
         ra.gates = gates;
         ra.zero_invalid = 0;
         const int t32 = (int)((N + kRows - 1) / kRows);
-        return launch_cfg<1, true, true, 3, 32, false, 8, false, true>(1, t32, (int)T, 1, s, tmW, tmX, ra, (int)N,
+        return launch_cfg<1, true, true, 3, 32, false, 8, false, true>(2, t32, (int)T, 1, s, tmW, tmX, ra, (int)N,
                                                                         KB, di.status);
     }
     const bool deep = rs_ctas <= di.sm_count;
