@@ -264,7 +264,7 @@ class Workload:
         return self.weight_bytes() / seconds_per_step / 1e9
 
 
-class GpuRunner:
+class DeviceRunner:
     """Device buffers (R rotating weight sets) and per-step launch functions."""
 
     def __init__(self, wl: Workload, device):
@@ -402,7 +402,7 @@ def run_gpu(args, rank, local_rank, world):
         dist.init_process_group("nccl", device_id=device)
 
     wl = Workload(args.workload, args.m)
-    gr = GpuRunner(wl, device)
+    gr = DeviceRunner(wl, device)
     stream = torch.cuda.Stream(device)
 
     # warm the host-side state (descriptors, attributes) before capture
