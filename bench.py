@@ -271,6 +271,7 @@ class DeviceRunner:
         import torch
         import q4_weight_quantized_gb300 as q4k
         self.torch, self.q4k, self.wl, self.dev = torch, q4k, wl, device
+        self.sh = None  # the stream handle every call is enqueued on (None: torch's current stream)
         np = wl.np
 
         def d(a):
@@ -303,9 +304,20 @@ class DeviceRunner:
             for r in range(self.R):
                 self.sets.append(base if r == 0 else [t.clone() for t in base])
             self.q, self.sx = [], []
-            for (_, N, K, M, _, x) in wl.mats:
-                self.x.append(d(x))
-                self.y.append(torch.empty((M, N), dtype=torch.float32, device=device))
+            # a step's activations and outputs each live in one buffer (matrix i's rows
+            # are a view into it), so that end to end a step is one copy in and one out
+            nx = [M * K for (_, N, K, M, _, _) in wl.mats]
+            ny = [M * N for (_, N, K, M, _, _) in wl.mats]
+            self.x_all = torch.empty(sum(nx), dtype=torch.int16, device=device)
+            self.y_all = torch.empty(sum(ny), dtype=torch.float32, device=device)
+            ox = oy = 0
+            for i, (_, N, K, M, _, x) in enumerate(wl.mats):
+                xv = self.x_all[ox:ox + nx[i]].view(M, K)
+                xv.copy_(d(x))
+                self.x.append(xv)
+                self.y.append(self.y_all[oy:oy + ny[i]].view(M, N))
+                ox += nx[i]
+                oy += ny[i]
                 if wl.x8:
                     self.q.append(torch.empty((M, K), dtype=torch.int8, device=device))
                     self.sx.append(torch.empty((M, K // 32), dtype=torch.float32, device=device))
@@ -331,14 +343,14 @@ class DeviceRunner:
         q4k, wl = self.q4k, self.wl
         tag, N, K, M, _, _ = wl.mats[i]
         if tag in wl.fp4:
-            q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N)
+            q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N, stream=self.sh)
         elif wl.x8:
-            q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N)
+            q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N, stream=self.sh)
         elif M == 1:
-            q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i])
+            q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i], stream=self.sh)
         else:
             ws, wsb = self.ws[i]
-            q4k.q4k_gemm(self.sets[r][i], N, K, self.x[i], M, K, self.y[i], N, ws if wsb else None, wsb)
+            q4k.q4k_gemm(self.sets[r][i], N, K, self.x[i], M, K, self.y[i], N, ws if wsb else None, wsb, stream=self.sh)
 
     def step(self, r: int, mark=None):
         """Enqueue one step using weight set r.  mark(i) is called before
@@ -351,18 +363,18 @@ class DeviceRunner:
                 mark(0)
             if mo["ffn"]:
                 q4k.q4k_moe_ffn(s["gate"], s["up"], s["down"], E, 768, 2048, self.xg, self.ids, self.gates, T, topk,
-                                self.y_down, self.moe_ws, self.moe_wsb)
+                                self.y_down, self.moe_ws, self.moe_wsb, stream=self.sh)
                 if mark:
                     mark(1)
                 return
             # the layer's three projections share one routing: the first call sorts
             # the items, the other two reuse the sort left in the workspace
             q4k.q4k_moe_grouped_gemm(s["gate"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk, self.y_gate,
-                                     0, self.moe_ws, self.moe_wsb)
+                                     0, self.moe_ws, self.moe_wsb, stream=self.sh)
             q4k.q4k_moe_grouped_gemm_reuse_routing(s["up"], E, 768, 2048, self.xg, 0, self.ids, self.gates, T, topk,
-                                                   self.y_up, 0, self.moe_ws, self.moe_wsb)
+                                                   self.y_up, 0, self.moe_ws, self.moe_wsb, stream=self.sh)
             q4k.q4k_moe_grouped_gemm_reuse_routing(s["down"], E, 2048, 768, self.xd, 1, self.ids, self.gates, T, topk,
-                                                   self.y_down, 1, self.moe_ws, self.moe_wsb)
+                                                   self.y_down, 1, self.moe_ws, self.moe_wsb, stream=self.sh)
             if mark:
                 mark(1)
             return
@@ -370,15 +382,15 @@ class DeviceRunner:
             if mark:
                 mark(i)
             if tag in wl.fp4:
-                q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N)
+                q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N, stream=self.sh)
             elif wl.x8:
-                q4k.q4k_quantize_x8(self.x[i], M, K, K, self.q[i], self.sx[i])
-                q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N)
+                q4k.q4k_quantize_x8(self.x[i], M, K, K, self.q[i], self.sx[i], stream=self.sh)
+                q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N, stream=self.sh)
             elif M == 1:
-                q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i])
+                q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i], stream=self.sh)
             else:
                 ws, wsb = self.ws[i]
-                q4k.q4k_gemm(self.sets[r][i], N, K, self.x[i], M, K, self.y[i], N, ws if wsb else None, wsb)
+                q4k.q4k_gemm(self.sets[r][i], N, K, self.x[i], M, K, self.y[i], N, ws if wsb else None, wsb, stream=self.sh)
         if mark:
             mark(len(wl.mats))
 
@@ -404,6 +416,7 @@ def run_gpu(args, rank, local_rank, world):
     wl = Workload(args.workload, args.m)
     gr = DeviceRunner(wl, device)
     stream = torch.cuda.Stream(device)
+    gr.sh = stream.cuda_stream  # every call names its stream, as a serving loop would
 
     # warm the host-side state (descriptors, attributes) before capture
     with torch.cuda.stream(stream):
@@ -485,34 +498,31 @@ def run_gpu(args, rank, local_rank, world):
     # outputs back to pinned host memory, every step
     e2e = None
     if not wl.moe:
-        hx = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory() for (*_, x) in wl.mats]
-        hy = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in gr.y]
+        hx = torch.from_numpy(np.concatenate([np.ascontiguousarray(x).view(np.int16).reshape(-1)
+                                              for (*_, x) in wl.mats])).pin_memory()
+        hy = torch.empty(gr.y_all.shape, dtype=torch.float32).pin_memory()
         e2e_steps = min(args.steps, 2000)
         with torch.cuda.stream(stream):
             for i in range(10):
-                for j in range(len(wl.mats)):
-                    gr.x[j].copy_(hx[j], non_blocking=True)
+                gr.x_all.copy_(hx, non_blocking=True)
                 gr.step(i % gr.R)
-                for j in range(len(wl.mats)):
-                    hy[j].copy_(gr.y[j], non_blocking=True)
+                hy.copy_(gr.y_all, non_blocking=True)
             torch.cuda.synchronize()
             if world > 1:
                 dist.barrier()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for i in range(e2e_steps):
-                for j in range(len(wl.mats)):
-                    gr.x[j].copy_(hx[j], non_blocking=True)
+                gr.x_all.copy_(hx, non_blocking=True)  # the step's activations, pinned host -> device
                 gr.step(i % gr.R)
-                for j in range(len(wl.mats)):
-                    hy[j].copy_(gr.y[j], non_blocking=True)
+                hy.copy_(gr.y_all, non_blocking=True)  # the step's outputs, device -> pinned host
             e1.record(stream)
             torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
         ems = max_over_ranks(ems, world, device)
         e2e = {"value": job_value(wl.value(ems / 1e3 / e2e_steps), world), "unit": wl.unit,
-               "h2d_bytes_per_step": int(sum(x.nbytes for (*_, x) in wl.mats)),
-               "d2h_bytes_per_step": int(sum(y.numel() * 4 for y in gr.y)), "steps": e2e_steps}
+               "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hy.numel() * 4),
+               "steps": e2e_steps}
 
     hbm, bf16, bf16_s, src = peaks()
     sec_per_step = ms / 1e3 / args.steps
