@@ -298,8 +298,10 @@ def test_prefill_many_tiles_ragged(ref):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (128, 5120, 17408), (1024, 5120, 17408),
-                                   (4096, 17408, 5120)])
+                                   (4096, 17408, 5120), (4096, 5120, 17408)])
 def test_prefill_full_size(ref, M, N, K):
+    # (4096, 5120, 17408) runs as the benchmark's two launches: 15 token tiles, then
+    # the last one with the cluster K split
     b = G.weights(3, 0, N, K, outliers=True)
     x = G.activations(3, 1, M, K)
     y = gpu_gemm(b, N, K, x)
@@ -843,10 +845,10 @@ def test_nvfp4_gemm_parity(ref, M, N, K):
     assert err <= TOL_FP4, err
 
 
+@pytest.mark.parametrize("M", [1024, 4096])
 @pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
-def test_nvfp4_gemm_full_size(ref, N, K):
-    # the prefill shapes at M = 1024, sampled output rows
-    M = 1024
+def test_nvfp4_gemm_full_size(ref, N, K, M):
+    # the prefill shapes, sampled output rows and tokens (M = 4096 is the benchmark's size)
     w, g = fp4_weights(4, N, K)
     x = G.activations(7, 5, M, K)
     y = gpu_nvfp4_gemm(w, float(g), N, K, x)
