@@ -189,14 +189,15 @@ class Workload:
         self.x8 = name == "decode_x8"
         self.fp4 = {}  # NVFP4 workloads: tag -> tensor scale g
         if name in ("decode", "decode_x8"):
-            self.mats = [("gate_up", 17408, 5120, 1, synth.weights(synth.seed(1, 0), 17408, 5120),
-                          synth.normal_bf16(synth.seed(1, 1), 5120).reshape(1, 5120)),
-                         ("down", 5120, 17408, 1, synth.weights(synth.seed(1, 5), 5120, 17408),
-                          synth.normal_bf16(synth.seed(1, 6), 17408).reshape(1, 17408))]
+            mt = m if self.x8 else 1  # the int8 variant also runs at verify sizes (--m up to 16)
+            self.mats = [("gate_up", 17408, 5120, mt, synth.weights(synth.seed(1, 0), 17408, 5120),
+                          synth.normal_bf16(synth.seed(1, 1), mt * 5120).reshape(mt, 5120)),
+                         ("down", 5120, 17408, mt, synth.weights(synth.seed(1, 5), 5120, 17408),
+                          synth.normal_bf16(synth.seed(1, 6), mt * 17408).reshape(mt, 17408))]
             self.unit, self.config = "GB/s", {"workload": "decode GEMV M=1: K5120->N17408 then K17408->N5120"}
             if self.x8:
-                self.config = {"workload": "decode GEMV M=1 with int8 activations (per-32 scales, quantized in "
-                                           "the step): K5120->N17408 then K17408->N5120"}
+                self.config = {"workload": f"decode GEMV M={mt} with int8 activations (per-32 scales, quantized "
+                                           "in the step): K5120->N17408 then K17408->N5120"}
                 self.mats = [(tag + "_x8",) + tuple(rest) for (tag, *rest) in self.mats]
         elif name == "verify":
             self.mats = [("verify", 17408, 5120, m, synth.weights(synth.seed(2, 0), 17408, 5120),
@@ -215,10 +216,10 @@ class Workload:
             for tag, N, K, sw, sx in (("gate_up_fp4", 17408, 5120, 10, 11), ("down_fp4", 5120, 17408, 12, 13)):
                 blocks, g = synth.nvfp4_weights(synth.seed(8, sw), N, K)
                 self.fp4[tag] = float(g)
-                mats.append((tag, N, K, 1, blocks, synth.normal_bf16(synth.seed(8, sx), K).reshape(1, K)))
+                mats.append((tag, N, K, m, blocks, synth.normal_bf16(synth.seed(8, sx), m * K).reshape(m, K)))
             self.mats = mats
-            self.unit, self.config = "GB/s", {"workload": "decode GEMV M=1 with NVFP4 weights: K5120->N17408 then "
-                                                          "K17408->N5120"}
+            self.unit, self.config = "GB/s", {"workload": f"decode GEMV M={m} with NVFP4 weights: K5120->N17408 "
+                                                          "then K17408->N5120"}
         elif name == "prefill_nvfp4":
             mats = []
             for tag, N, K, sw, sx in (("prefill_up_fp4", 17408, 5120, 0, 1), ("prefill_down_fp4", 5120, 17408, 5, 6)):
