@@ -184,6 +184,36 @@ def test_batch_invariance_and_determinism():
         assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
 
 
+@pytest.mark.parametrize("KB", [1, 2, 3, 6, 7, 9, 11, 13])
+def test_smallm_uneven_warp_blocks(ref, KB):
+    # K blocks per split not divisible by the 4 warps (some warps take one block
+    # more, or none), N 5120 over a cluster K split; batch invariance on the same shapes
+    N, K = 5120, 256 * KB
+    b = G.weights(2, 5, N, K, outliers=True)
+    x = G.activations(2, 6, 16, K)
+    w = G.dev(b)
+    y16 = gpu_gemm(b, N, K, x, w_dev=w)
+    rows = G.sample_rows(N, 256)
+    assert G.rel_err(y16[:, rows], ref.gemm(G.rows_of(b, rows), len(rows), K, x)) <= TOL_SMALL
+    for m in (0, 9):
+        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+
+
+def test_batch_invariance_down_shape():
+    # K 17408 over a 4-way cluster split: 17 blocks per CTA, so one warp takes 5 of them
+    cfg, N, K = G.DECODE_DOWN
+    b = G.weights(cfg, 0, N, K)
+    w = G.dev(b)
+    x = G.activations(cfg, 7, 16, K)
+    y16 = gpu_gemm(b, N, K, x, w_dev=w)
+    y4 = gpu_gemm(b, N, K, x[:4], w_dev=w)
+    assert np.array_equal(y4.view(np.uint32), y16[:4].view(np.uint32))
+    for m in (0, 7, 15):
+        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+
+
 @pytest.mark.parametrize("shape", [G.DECODE_UP, G.DECODE_DOWN], ids=["gate_up", "down"])
 def test_decode_gemv_full_size(ref, shape):
     cfg, N, K = shape
