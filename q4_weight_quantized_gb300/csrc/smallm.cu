@@ -40,6 +40,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "q4k_internal.h"
 #include "q4k_ptx.cuh"
 
@@ -420,7 +422,7 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // FP4 (dense): NVFP4 weights in the same 144-byte blocks (block_mma_fp4), the
 // outputs multiplied by RowArgs::gscale.
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
-          bool DC = false, bool X8 = false, bool FP4 = false>
+          bool DC = false, bool X8 = false, bool FP4 = false, bool PUSH = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmAux,
                                                           const __grid_constant__ CUtensorMap tmX, RowArgs ra, int N,
@@ -516,7 +518,12 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     uint8_t *region = smem + warp * G::warp_bytes(nx, SLOTS);
     float *table = reinterpret_cast<float *>(region + SLOTS * sbytes);
     const uint32_t bar0 = smem_u32(smem + G::bars_off(nx, SLOTS)) + warp * SLOTS * 8;
+    // PUSH (dense K split): rank 0's landing barrier for the other ranks' partials
+    const uint32_t lbar = smem_u32(smem + G::bars_off(nx, SLOTS)) + kWarps * SLOTS * 8;
     if (threadIdx.x == 0) abort_flag = 0;
+    if constexpr (PUSH && !MOE) {
+        if (threadIdx.x == 0) mbar_init(lbar, (S - 1) * kThreads);
+    }
     if (lane == 0) {
         for (int i = 0; i < SLOTS; ++i) mbar_init(bar0 + 8 * i, 1);
         fence_mbar_init();
@@ -537,6 +544,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     if constexpr (!MOE) pdl_wait();  // x may come from the previous kernel
     pdl_trigger();
     __syncthreads();
+    if constexpr (PUSH && !MOE) cluster_arrive();  // waited on before the partials are pushed
 
     // issue the copies of iteration `it` (chunk it / nblk, block it % nblk) into
     // its slot; `weights` false: the weight copy (and the transaction count) went out already
@@ -766,7 +774,27 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         for (int w = 1; w < kWarps; ++w) v += red_w[w * 16 * kRows + e];
         red[e] = v;
     }
-    if (S > 1) {
+    if constexpr (PUSH) {
+        // ranks 1.. push their partial into rank 0's landing buffer [S-1][elems] (apart
+        // from the rings, which rank 0 may still be reading) and arrive on its landing
+        // barrier, then leave; rank 0 adds them in rank order, as the pull below does
+        __syncthreads();  // red is complete
+        cluster_wait();   // the prologue's arrive: rank 0's landing barrier is initialised
+        float *land = reinterpret_cast<float *>(smem + G::red_off(nx, SLOTS));
+        if (split != 0) {
+            const uint32_t dst = map_shared_rank(smem_u32(land + (split - 1) * elems), 0);
+            for (int e = threadIdx.x; e < elems; e += kThreads) st_shared_cluster_f32(dst + 4u * e, red[e]);
+            mbar_arrive_cluster(map_shared_rank(lbar, 0));
+        } else if (mbar_wait_cluster(lbar, 0, status, (SLOTS + 2) * 4 * kWaitLimitNs)) {
+            // (the limit outlasts every bounded wait a pushing rank can make first)
+            for (int e = threadIdx.x; e < elems; e += kThreads) {
+                float v = red[e];
+                for (int q = 1; q < S; ++q) v += land[(q - 1) * elems + e];
+                const int tk = e / kRows, rr = e % kRows;
+                if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = FP4 ? ra.gscale * v : v;
+            }
+        }
+    } else if (S > 1) {
         cluster_sync();  // every split's partial is in its shared memory
         if (split == 0) {
             const uint32_t base = smem_u32(red);
@@ -788,12 +816,13 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
 }
 
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
-          bool DC = false, bool X8 = false, bool FP4 = false>
+          bool DC = false, bool X8 = false, bool FP4 = false, bool PUSH = false>
 cudaError_t launch_cfg(int S, int tiles, int E, int nx, cudaStream_t s, const CUtensorMap &tmW,
                        const CUtensorMap &tmX, const RowArgs &ra, int N, int KB, unsigned int *status,
                        const CUtensorMap *tmAux = nullptr) {
-    const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS);
-    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU, DC, X8, FP4>;
+    // PUSH: rank 0's landing buffer for the other ranks' partials
+    const int smem = Geo<ROWS>::smem_total(nx, SLOTS, MOE && !RS) + (PUSH ? (S - 1) * nx * ROWS * 4 : 0);
+    auto kern = smallm_kernel<NT, MOE, ONE, SLOTS, ROWS, RS, CH, GLU, DC, X8, FP4, PUSH>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(S, tiles, E), dim3(kThreads), (size_t)smem, s, dim3(S), tmW, tmAux ? *tmAux : tmW, tmX,
@@ -864,14 +893,30 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
     ra.y = y; ra.ldy = ldy; ra.M = (int)M;
     ra.early_w = early_weights ? 1 : 0;
     const int nx = (int)M, n = (int)N;
-    if (sp.rows == 48) {
-        if (M == 1) return launch_cfg<1, false, true, 2, 48>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
-        if (M <= 8) return launch_cfg<1, false, false, 2, 48>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
-        return launch_cfg<2, false, false, 2, 48>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
-    }
-    if (M == 1) return launch_cfg<1, false, true, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
-    if (M <= 8) return launch_cfg<1, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
-    return launch_cfg<2, false, false, 2, 32>(S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+    // a K split reduces by pushing the partials to rank 0 (PUSH); without one the
+    // kernel has no cluster work at all
+    auto go = [&](auto push) -> cudaError_t {
+        constexpr bool P = decltype(push)::value;
+        if (sp.rows == 48) {
+            if (M == 1)
+                return launch_cfg<1, false, true, 2, 48, false, 8, false, false, false, false, P>(
+                    S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+            if (M <= 8)
+                return launch_cfg<1, false, false, 2, 48, false, 8, false, false, false, false, P>(
+                    S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+            return launch_cfg<2, false, false, 2, 48, false, 16, false, false, false, false, P>(
+                S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+        }
+        if (M == 1)
+            return launch_cfg<1, false, true, 2, 32, false, 8, false, false, false, false, P>(
+                S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+        if (M <= 8)
+            return launch_cfg<1, false, false, 2, 32, false, 8, false, false, false, false, P>(
+                S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+        return launch_cfg<2, false, false, 2, 32, false, 16, false, false, false, false, P>(
+            S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+    };
+    return S > 1 ? go(std::true_type{}) : go(std::false_type{});
 }
 
 cudaError_t launch_smallm_fp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K, const uint16_t *x,

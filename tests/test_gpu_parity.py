@@ -889,6 +889,48 @@ def test_nvfp4_gemm_full_size(ref, N, K, M):
     assert err <= TOL_FP4, err
 
 
+@pytest.mark.parametrize("N,K,M,fp4", [(5120, 17408, 1, False), (2000, 5120, 4, False), (5120, 17408, 1, True)],
+                         ids=["split_k_m1", "ragged_m4", "nvfp4_split_k"])
+def test_static_weights_activations_from_the_previous_kernel(ref, N, K, M, fp4):
+    # static weights on: the first activation blocks are read by plain loads right
+    # after the wait on the previous kernel - here the dequantization that writes them,
+    # alternating between two sources, with no host synchronization in between
+    srcs = [G.weights(2, 20 + i, M, K) for i in range(2)]
+    src_d = [G.dev(s) for s in srcs]
+    xs = [ref.dequant_bf16(s, M, K).reshape(M, K) for s in srcs]
+    if fp4:
+        b, g = fp4_weights(6, N, K)
+    else:
+        b = G.weights(2, 22, N, K)
+    w = G.dev(b)
+    xd = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    outs = torch.empty((6, M, N), dtype=torch.float32, device="cuda")
+    prev = q4k.q4k_set_static_weights(True)
+    try:
+        for i in range(6):
+            q4k.q4k_dequant_bf16(src_d[i % 2], M, K, xd)
+            if fp4:
+                q4k.q4k_nvfp4_gemm(w, float(g), N, K, xd, M, K, y, N)
+            else:
+                q4k.q4k_gemm(w, N, K, xd, M, K, y, N, None, 0)
+            outs[i].copy_(y)
+        torch.cuda.synchronize()
+    finally:
+        q4k.q4k_set_static_weights(prev)
+    got = G.host(outs)
+    rows = np.unique(np.concatenate([G.sample_rows(N, 48, seed=4), np.arange(N - 8, N)]))
+    for j in range(2):
+        if fp4:
+            want = ref.nvfp4_gemm(G.rows_of(b, rows), float(g), len(rows), K, xs[j], threads=16)
+            tol = TOL_FP4
+        else:
+            want = ref.gemm(G.rows_of(b, rows), len(rows), K, xs[j], threads=8)
+            tol = TOL_SMALL
+        for i in range(j, 6, 2):
+            assert G.rel_err(got[i][:, rows], want) <= tol, (i, j)
+
+
 def test_nvfp4_gemm_deterministic():
     N, K, M = 640, 4096, 300
     w, g = fp4_weights(5, N, K)
