@@ -173,15 +173,29 @@ __global__ void combine_kernel(const float *__restrict__ out, const float *__res
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = q / n4, c = (q % n4) * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < topk; ++j) {
-            const int e = __ldg(ids + t * topk + j);
-            if (e < 0 || e >= E) continue;
-            const float g = __ldg(gates + t * topk + j);
-            const float4 o = __ldg(reinterpret_cast<const float4 *>(out + (t * topk + j) * N + c));
-            acc.x = fmaf(g, o.x, acc.x);
-            acc.y = fmaf(g, o.y, acc.y);
-            acc.z = fmaf(g, o.z, acc.z);
-            acc.w = fmaf(g, o.w, acc.w);
+        // up to 8 slots' loads in flight at once, then their FMAs in increasing j
+        for (int j0 = 0; j0 < topk; j0 += 8) {
+            float4 o[8];
+            float g[8];
+            bool v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                const int e = j < topk ? __ldg(ids + t * topk + j) : -1;
+                v[u] = e >= 0 && e < E;
+                if (v[u]) {
+                    g[u] = __ldg(gates + t * topk + j);
+                    o[u] = __ldg(reinterpret_cast<const float4 *>(out + (t * topk + j) * N + c));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (!v[u]) continue;
+                acc.x = fmaf(g[u], o[u].x, acc.x);
+                acc.y = fmaf(g[u], o[u].y, acc.y);
+                acc.z = fmaf(g[u], o[u].z, acc.z);
+                acc.w = fmaf(g[u], o[u].w, acc.w);
+            }
         }
         *reinterpret_cast<float4 *>(y + t * N + c) = acc;
     }
