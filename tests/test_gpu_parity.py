@@ -200,6 +200,21 @@ def test_smallm_uneven_warp_blocks(ref, KB):
         assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
 
 
+@pytest.mark.parametrize("N,K", [(600, 16384), (1000, 17408)])
+def test_smallm_cluster_split_of_eight(ref, N, K):
+    # few row tiles and long K: clusters of 8 split K, so ranks 1..7 push their
+    # partials (16 tokens: the largest landing buffer) into rank 0
+    b = G.weights(2, 8, N, K)
+    x = G.activations(2, 9, 16, K)
+    w = G.dev(b)
+    y16 = gpu_gemm(b, N, K, x, w_dev=w)
+    rows = np.unique(np.concatenate([G.sample_rows(N, 96, seed=5), np.arange(N - 8, N)]))
+    assert G.rel_err(y16[:, rows], ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=8)) <= TOL_SMALL
+    for m in (0, 13):
+        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+
+
 def test_batch_invariance_down_shape():
     # K 17408 over a 4-way cluster split: 17 blocks per CTA, so one warp takes 5 of them
     cfg, N, K = G.DECODE_DOWN
