@@ -517,9 +517,12 @@ q4k_status q4k_moe_ffn(const void *w_gate, const void *w_up, const void *w_down,
                                   false, s, glu, w_up);
         // very few items: the down projection combines in the CTA, straight into y
         const bool dcomb = moe_direct(n);
+        // (its ids were waited for by the gate and up kernel just before: with static
+        // weights its first expert weight blocks go out before its own wait)
         if (e == cudaSuccess)
             e = launch_moe_smallm(di, w_down, E, D, H, h, 1, perm, offsets, tiles, n_tiles, topk_ids, T, topk,
-                                  dcomb ? y : o, false, s, GluOut(), nullptr, dcomb ? gates : nullptr);
+                                  dcomb ? y : o, false, s, GluOut(), nullptr, dcomb ? gates : nullptr,
+                                  dcomb && g_static_weights.load(std::memory_order_relaxed) != 0);
         if (e == cudaSuccess && !dcomb) e = launch_moe_combine(di, o, gates, topk_ids, E, T, topk, D, y, s);
         return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
     }

@@ -88,12 +88,15 @@ cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, i
 // With zero_invalid, the per-slot rows of the items with an invalid id
 // (perm[offsets[E] .. T*topk)) are zeroed.  With very few items (moe_direct),
 // no routing is read: each item is its own grid layer, its expert ids[item].
+// ids_early (with gates, very few items): the ids and the first expert weight
+// blocks are read before waiting on the previous kernel - only for a call whose
+// previous kernel itself waited for the ids' writer, and with static weights.
 inline bool moe_direct(int64_t n_items) { return n_items <= 16; }
 cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E, int64_t N, int64_t K,
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
                               float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu = GluOut(),
-                              const void *w_up = nullptr, const float *gates = nullptr);
+                              const void *w_up = nullptr, const float *gates = nullptr, bool ids_early = false);
 
 // Stable counting sort of items by expert (E <= 1024).  Items with an id
 // outside [0, E) are left out of offsets; with invalid_tail they follow the

@@ -378,6 +378,10 @@ struct RowArgs {
     GluOut glu;  // MoE with GLU: h (bf16) receives the SwiGLU of the gate and up projections
     float gscale;  // FP4: the weights' tensor scale, applied to the outputs
     const float *gates;  // MoE with DC: the combine weights [T][topk]
+    // MoE with DC: the ids may be read, and the first slots' (static) expert weights
+    // copied, before waiting on the previous kernel - the expert FFN's down
+    // projection, whose previous kernel (gate and up) waited for the ids' writer
+    int ids_early;
 };
 
 // The (token, k-slot) item at position p of the expert-sorted order (MoE).
@@ -459,7 +463,10 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     const int nblk = RS || DC ? kb1 - kb0 : (kb1 - kb0 > wsub ? (kb1 - kb0 - wsub + kNw - 1) / kNw : 0);
     const int kb_first = RS || DC ? kb0 : kb0 + wsub, kb_step = RS || DC ? 1 : kNw;
 
-    if constexpr (MOE) pdl_wait();  // the routing comes from the previous kernel
+    // the routing comes from the previous kernel (DC with ids_early: wait below)
+    if constexpr (MOE) {
+        if (!DC || !ra.ids_early) pdl_wait();
+    }
     int off0 = 0, cnt = ra.M, tma_row = wrow0;
     // DC: bit j of dc_mask marks this warp's j-th slot (slot warp + 4j) as valid;
     // its chunks are the valid ones, in order
@@ -540,8 +547,22 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
                                 tma_row, bar);
                 }
         }
+        if constexpr (DC) {
+            // the same for the first slots' expert weights (one token slot each)
+            if (ra.ids_early)
+                for (int it = 0; it < SLOTS && it < total; ++it) {
+                    const uint32_t bar = bar0 + 8 * (it % SLOTS);
+                    const int item = (int)blockIdx.z * ra.topk + dc_slot(it / nblk);
+                    mbar_arrive_expect_tx(bar, kBlkWBytes + kXTx);
+                    tma_load_2d(smem_u32(region + (it % SLOTS) * sbytes), tw, (kb_first + kb_step * (it % nblk)) *
+                                kBlkWords, __ldg(ra.ids + item) * N + wrow0, bar);
+                }
+        }
     }
     if constexpr (!MOE) pdl_wait();  // x may come from the previous kernel
+    if constexpr (DC) {
+        if (ra.ids_early) pdl_wait();  // h comes from the previous kernel
+    }
     pdl_trigger();
     __syncthreads();
     if constexpr (PUSH && !MOE) cluster_arrive();  // waited on before the partials are pushed
@@ -579,7 +600,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
         }
     };
 
-    const bool early = !MOE && ra.early_w;
+    const bool early = (!MOE && ra.early_w) || (DC && ra.ids_early);
     for (int it = 0; it < SLOTS && it < total; ++it) issue(it, !early);
 
     float acc[kRowTiles][NT][4];
@@ -1034,7 +1055,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
                               const uint16_t *x, int x_per_slot, const int32_t *perm, const int32_t *offsets,
                               const int4 *tok_tiles, const int *n_tiles, const int32_t *ids, int64_t T, int topk,
                               float *out, bool zero_invalid, cudaStream_t s, const GluOut &glu,
-                              const void *w_up, const float *gates) {
+                              const void *w_up, const float *gates, bool ids_early) {
     CUtensorMap tmW, tmAux, tmX;
     // all experts stacked: E*N rows of the same pitch
     constexpr int kRows = 32;
@@ -1074,6 +1095,7 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
         // clusters of two that split the token's slots
         ra.gates = gates;
         ra.zero_invalid = 0;
+        ra.ids_early = ids_early ? 1 : 0;
         const int t32 = (int)((N + kRows - 1) / kRows);
         return launch_cfg<1, true, true, 3, 32, false, 8, false, true>(2, t32, (int)T, 1, s, tmW, tmX, ra, (int)N,
                                                                         KB, di.status);

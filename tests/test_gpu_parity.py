@@ -667,6 +667,45 @@ def test_moe_ffn_layer(ref, syn, ffn_layer, T):
     assert G.rel_err(y, want) <= TOL_SMALL
 
 
+@pytest.mark.parametrize("T", [1, 2])
+def test_moe_ffn_static_weights_ids_from_the_previous_kernel(ref, syn, ffn_layer, T):
+    # static weights on: the down projection of the fused small layer reads the ids
+    # and copies its first expert weight blocks before its own wait.  The ids
+    # alternate between two routings, each written by a device copy right before the
+    # call, with no host synchronization in between; results match the oracle and
+    # the bits of the default mode
+    wg, wu, wd, devs = ffn_layer
+    (H, D), E, topk = G.MOE_UP, G.MOE_E, G.MOE_TOPK
+    routes = [syn.routing(310 + T + 7 * i, 311 + T + 7 * i, T, E, topk) for i in range(2)]
+    routes[1][0][0, 2] = -1
+    x = G.activations(4, 46, T, D)
+    xd = G.dev(x)
+    ids_src = [G.dev(r[0]) for r in routes]
+    gates_d = [G.dev(r[1]) for r in routes]
+    ids_d = torch.empty_like(ids_src[0])
+    ws_bytes = q4k.q4k_moe_ffn_workspace_size(E, H, D, T, topk)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    y = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    outs = torch.empty((6, T, D), dtype=torch.float32, device="cuda")
+    prev = q4k.q4k_set_static_weights(True)
+    try:
+        for i in range(6):
+            ids_d.copy_(ids_src[i % 2])
+            q4k.q4k_moe_ffn(*devs, E, H, D, xd, ids_d, gates_d[i % 2], T, topk, y, ws, ws_bytes)
+            outs[i].copy_(y)
+        torch.cuda.synchronize()
+    finally:
+        q4k.q4k_set_static_weights(prev)
+    got = G.host(outs)
+    for j in range(2):
+        ids, gates = routes[j]
+        want = ref.moe_ffn(wg, wu, wd, E, H, D, x, ids, gates, threads=16)
+        off = run_ffn(wg, wu, wd, E, H, D, x, ids, gates, devs)
+        for i in range(j, 6, 2):
+            assert G.rel_err(got[i], want) <= TOL_SMALL, (i, j)
+            assert np.array_equal(got[i].view(np.uint32), off.view(np.uint32)), (i, j)
+
+
 def test_moe_ffn_t2048_sampled(ref, syn, ffn_layer):
     # the prefill-sized layer (tensor-core path, h stored expert-sorted), in the
     # configuration the benchmark times; the oracle computes sampled tokens
