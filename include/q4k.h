@@ -89,14 +89,17 @@ int q4k_version(void);
  * Q4K_ERR_CUDA if the synchronization itself failed. */
 q4k_status q4k_check_device(void *stream);
 
-/* Declares whether the weight matrices read by the small-M calls (q4k_gemv, and
- * q4k_gemm with M <= 16) are static: never written by the kernel enqueued on the
- * same stream immediately before the call.  Every kernel of the library is
+/* Declares whether the weight matrices read by the small-M calls (q4k_gemv,
+ * q4k_gemm with M <= 16, q4k_gemm_x8, q4k_nvfp4_gemm with M <= 16, and the down
+ * projection of q4k_moe_ffn with at most 16 items) are static: never written by
+ * the kernel enqueued on the same stream immediately before the call.  Every kernel of the library is
  * launched so that it may start while the previous kernel on its stream drains,
  * and it waits for that kernel to finish before it touches memory.  With static
  * weights on, the small-M kernels already copy their first weight blocks into
  * shared memory during that wait, which hides part of each call's start-up
- * (about 1.5 us on a 50 MB GEMV).  That is the usual inference setting: weights
+ * (about 1.5 us on a 50 MB GEMV).  In q4k_moe_ffn the down projection then also
+ * reads topk_ids early; its gate/up kernel has already waited for the ids' writer
+ * by then.  That is the usual inference setting: weights
  * are uploaded once, by copies, and only read afterwards.  Keep it off (the
  * default) when a kernel may write a weight buffer right before a q4k call reads
  * it, for example a fill or an on-device quantization kernel: the early copies
