@@ -114,7 +114,7 @@ class ClockSampler:
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
 
     def __init__(self, cuda_index: int):
-        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.samples, self.reasons, self.max_mhz, self.power_mw = [], 0, None, []
         self._stop = threading.Event()
         self._nvml = None
         try:
@@ -153,6 +153,8 @@ class ClockSampler:
                 self.samples.append(c.value)
             if get_reasons(h, ctypes.byref(r)) == 0:
                 self.reasons |= r.value
+            if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(c)) == 0:
+                self.power_mw.append(c.value)
             time.sleep(0.005)
 
     def __enter__(self):
@@ -169,9 +171,12 @@ class ClockSampler:
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b and n != "gpu_idle"],
-                "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+               "reasons": [n for b, n in self.REASONS.items() if self.reasons & b and n != "gpu_idle"],
+               "samples": len(self.samples)}
+        if self.power_mw:
+            out["power_w"] = statistics.median(self.power_mw) / 1e3
+        return out
 
 
 # --------------------------------------------------------------- workloads
@@ -471,6 +476,21 @@ def run_gpu(args, rank, local_rank, world):
     ms = t0.elapsed_time(t1)
     q4k.q4k_check_device(stream)
 
+    # spread: a separate pass of graph replays, each bracketed by events, so that the
+    # events do not touch the timed region above
+    spread = None
+    n_rep = max(3, min(200, args.steps // gr.R))
+    with torch.cuda.stream(stream):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+        evs[0].record(stream)
+        for i in range(n_rep):
+            g_full.replay()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = sorted(evs[i].elapsed_time(evs[i + 1]) / gr.R for i in range(n_rep))
+    spread = {"replays": n_rep, "steps_per_replay": gr.R, "median_ms_per_step": statistics.median(per),
+              "best_ms_per_step": per[0], "worst_ms_per_step": per[-1]}
+
     # per-kernel durations: each kernel of the step alone, R launches over the R
     # weight sets per graph, replayed back to back and timed with CUDA events on
     # the launching stream (average launch duration, launch gaps included)
@@ -560,6 +580,8 @@ def run_gpu(args, rank, local_rank, world):
                                 "peak_source": src, "frac_of_nominal_8tbs": ach / 8000.0}
         line["kernels_us"] = {wl.mats[i][0]: kernel_ms[i] * 1e3 for i in range(len(kernel_ms))}
     line["clocks"] = clocks.summary()
+    if spread:
+        line["spread"] = spread
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and args.workload == "decode" and not args.no_cpu:
