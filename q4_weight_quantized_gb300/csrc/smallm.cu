@@ -425,6 +425,10 @@ __device__ __forceinline__ void slot_rows(const RowArgs &ra, int off0, int cnt, 
 // tmAux: GLU: the up matrix; X8: the activation scales; otherwise unused.
 // FP4 (dense): NVFP4 weights in the same 144-byte blocks (block_mma_fp4), the
 // outputs multiplied by RowArgs::gscale.
+// PUSH (dense, K split over a cluster): ranks 1.. store their CTA partial into a
+// landing buffer in rank 0's shared memory and arrive on its barrier, then exit;
+// rank 0 adds the partials in rank order.  Without it the K split's ranks meet at
+// cluster barriers and rank 0 reads the others' partials (same order, same bits).
 template <int NT, bool MOE, bool ONE, int SLOTS, int ROWS, bool RS = false, int CH = 8 * NT, bool GLU = false,
           bool DC = false, bool X8 = false, bool FP4 = false, bool PUSH = false>
 __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant__ CUtensorMap tmW,
