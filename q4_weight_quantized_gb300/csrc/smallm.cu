@@ -959,24 +959,29 @@ cudaError_t launch_smallm_fp4(const DeviceInfo &di, const void *w, float g, int6
     ra.early_w = early_weights ? 1 : 0;
     ra.gscale = g;
     const int nx = (int)M, n = (int)N;
-    if (sp.rows == 48) {
+    // a K split reduces by pushing the partials to rank 0 (PUSH), as in launch_smallm
+    auto go = [&](auto push) -> cudaError_t {
+        constexpr bool P = decltype(push)::value;
+        if (sp.rows == 48) {
+            if (M == 1)
+                return launch_cfg<1, false, true, 2, 48, false, 8, false, false, false, true, P>(
+                    S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+            if (M <= 8)
+                return launch_cfg<1, false, false, 2, 48, false, 8, false, false, false, true, P>(
+                    S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+            return launch_cfg<2, false, false, 2, 48, false, 16, false, false, false, true, P>(
+                S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+        }
         if (M == 1)
-            return launch_cfg<1, false, true, 2, 48, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX,
-                                                                                          ra, n, KB, di.status);
+            return launch_cfg<1, false, true, 2, 32, false, 8, false, false, false, true, P>(
+                S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
         if (M <= 8)
-            return launch_cfg<1, false, false, 2, 48, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW,
-                                                                                           tmX, ra, n, KB, di.status);
-        return launch_cfg<2, false, false, 2, 48, false, 16, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX,
-                                                                                        ra, n, KB, di.status);
-    }
-    if (M == 1)
-        return launch_cfg<1, false, true, 2, 32, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra,
-                                                                                      n, KB, di.status);
-    if (M <= 8)
-        return launch_cfg<1, false, false, 2, 32, false, 8, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX,
-                                                                                       ra, n, KB, di.status);
-    return launch_cfg<2, false, false, 2, 32, false, 16, false, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra,
-                                                                                    n, KB, di.status);
+            return launch_cfg<1, false, false, 2, 32, false, 8, false, false, false, true, P>(
+                S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+        return launch_cfg<2, false, false, 2, 32, false, 16, false, false, false, true, P>(
+            S, tiles, 1, nx, s, tmW, tmX, ra, n, KB, di.status);
+    };
+    return S > 1 ? go(std::true_type{}) : go(std::false_type{});
 }
 
 cudaError_t launch_smallm_x8(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const int8_t *q,
@@ -995,6 +1000,8 @@ cudaError_t launch_smallm_x8(const DeviceInfo &di, const void *w, int64_t N, int
     ra.y = y; ra.ldy = ldy; ra.M = (int)M;
     ra.early_w = early_weights ? 1 : 0;
     const int nx = (int)M, n = (int)N;
+    // the K split keeps the pull reduction: with the push form the int8 decode step was
+    // measured no faster (its steps varied 40-50 us, against 39-40 us with the pull)
     if (sp.rows == 48) {
         if (M == 1)
             return launch_cfg<1, false, true, 2, 48, false, 8, false, false, true>(S, tiles, 1, nx, s, tmW, tmX, ra, n,
