@@ -181,6 +181,10 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workloads
 
+# the expert weights do not depend on the token count: generated once per process
+_MOE_WEIGHTS = {}
+
+
 class Workload:
     """Holds the host inputs of one workload and knows how to run one step."""
 
@@ -237,8 +241,8 @@ class Workload:
         elif name in ("moe", "moe_ffn"):
             E, topk = 128, 8
             ids, gates = synth.routing(synth.seed(4, 2) + m, synth.seed(4, 3) + m, m, E, topk)
-            mk = lambda s, N, K: np.concatenate(  # noqa: E731
-                [synth.weights(synth.seed(4, s) + 1000 * (e + 1), N, K) for e in range(E)])
+            mk = lambda s, N, K: _MOE_WEIGHTS.setdefault((s, N, K), np.concatenate(  # noqa: E731
+                [synth.weights(synth.seed(4, s) + 1000 * (e + 1), N, K) for e in range(E)]))
             self.moe = dict(E=E, topk=topk, T=m, ids=ids, gates=gates, ffn=name == "moe_ffn",
                             gate=mk(0, 768, 2048), up=mk(7, 768, 2048), down=mk(5, 2048, 768),
                             x=synth.normal_bf16(synth.seed(4, 1), m * 2048).reshape(m, 2048),
@@ -358,6 +362,37 @@ class DeviceRunner:
             ws, wsb = self.ws[i]
             q4k.q4k_gemm(self.sets[r][i], N, K, self.x[i], M, K, self.y[i], N, ws if wsb else None, wsb, stream=self.sh)
 
+    def kernel_calls(self):
+        """(tag, enqueue(r)) for each separately timed kernel of the step.  Dense:
+        each matrix's GEMM.  MoE: the up projection call on the routing the step left
+        in the workspace (the expert GEMM; on the tensor-core path, from 32 items per
+        expert, the activation gather it starts with is inside the call too)."""
+        if self.wl.moe:
+            mo, q4k = self.wl.moe, self.q4k
+            E, T, topk = mo["E"], mo["T"], mo["topk"]
+
+            def up(r):
+                q4k.q4k_moe_grouped_gemm_reuse_routing(self.sets[r]["up"], E, 768, 2048, self.xg, 0, self.ids,
+                                                       self.gates, T, topk, self.y_up, 0, self.moe_ws, self.moe_wsb,
+                                                       stream=self.sh)
+            return [("moe_up", up)]
+        return [(tag, (lambda r, i=i: self.step_one(r, i))) for i, (tag, *_) in enumerate(self.wl.mats)]
+
+    def kernel_roofline(self, tag: str):
+        """Algorithmic work of one launch of kernel `tag`: ("hbm", bytes) or ("tensor", flops)."""
+        wl = self.wl
+        if wl.moe:
+            mo = wl.moe
+            items = mo["T"] * mo["topk"]
+            if items >= 32 * mo["E"]:
+                return "tensor", 2.0 * items * 768 * 2048
+            touched = len(set(mo["ids"].reshape(-1).tolist()))
+            return "hbm", touched * 768 * 2048 * 144 / 256 + mo["T"] * 2048 * 2 + items * 768 * 4
+        _, N, K, M, *_ = next(m for m in wl.mats if m[0] == tag)
+        if wl.unit == "TFLOP/s":
+            return "tensor", 2.0 * M * N * K
+        return "hbm", N * K * 144 / 256 + (M * K + M * K // 32 * 4 if wl.x8 else M * K * 2) + M * N * 4
+
     def step(self, r: int, mark=None):
         """Enqueue one step using weight set r.  mark(i) is called before
         matrix i and after the last one (to record events)."""
@@ -401,27 +436,17 @@ class DeviceRunner:
             mark(len(wl.mats))
 
 
-def run_gpu(args, rank, local_rank, world):
+def measure(wl, args, steps, warmup, stream, device, world, e2e=True):
+    """Times `steps` steps of workload `wl` on `stream` (after `warmup` untimed
+    steps); returns the record for the JSON line: value, time per step, the
+    dominant kernel's roofline, per-kernel times, clocks, spread and (e2e) the
+    end-to-end figure through the public API."""
     import numpy as np
     import torch
     import torch.distributed as dist
-    from q4_weight_quantized_gb300.build import build_library
     import q4_weight_quantized_gb300 as q4k
 
-    build_library()
-    q4k.load()
-    # weights are uploaded once and only read afterwards, as in serving: the
-    # small-M kernels may copy their first weight blocks while the previous
-    # kernel drains (include/q4k.h, q4k_set_static_weights)
-    q4k.q4k_set_static_weights(True)
-    torch.cuda.set_device(local_rank)
-    device = torch.device("cuda", local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=device)
-
-    wl = Workload(args.workload, args.m)
     gr = DeviceRunner(wl, device)
-    stream = torch.cuda.Stream(device)
     gr.sh = stream.cuda_stream  # every call names its stream, as a serving loop would
 
     # warm the host-side state (descriptors, attributes) before capture
@@ -445,8 +470,8 @@ def run_gpu(args, rank, local_rank, world):
         return g
 
     g_full = capture(gr.R)
-    g_rem = capture(args.steps % gr.R)
-    g_wrem = capture(args.warmup % gr.R)
+    g_rem = capture(steps % gr.R)
+    g_wrem = capture(warmup % gr.R)
 
     def run_steps(n, rem):
         for _ in range(n // gr.R):
@@ -456,19 +481,19 @@ def run_gpu(args, rank, local_rank, world):
 
     # warm-up steps
     with torch.cuda.stream(stream):
-        run_steps(args.warmup, g_wrem)
+        run_steps(warmup, g_wrem)
     torch.cuda.synchronize()
 
     # timed region
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(device.index)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with clocks:
         with torch.cuda.stream(stream):
             t0.record(stream)
-            run_steps(args.steps, g_rem)
+            run_steps(steps, g_rem)
             t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -478,8 +503,7 @@ def run_gpu(args, rank, local_rank, world):
 
     # spread: a separate pass of graph replays, each bracketed by events, so that the
     # events do not touch the timed region above
-    spread = None
-    n_rep = max(3, min(200, args.steps // gr.R))
+    n_rep = max(3, min(200, steps // gr.R))
     with torch.cuda.stream(stream):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
         evs[0].record(stream)
@@ -494,35 +518,34 @@ def run_gpu(args, rank, local_rank, world):
     # per-kernel durations: each kernel of the step alone, R launches over the R
     # weight sets per graph, replayed back to back and timed with CUDA events on
     # the launching stream (average launch duration, launch gaps included)
-    kernel_ms = None
-    if not wl.moe:
-        kernel_ms = []
-        for i in range(len(wl.mats)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for r in range(gr.R):
-                    gr.step_one(r, i)
-            reps = max(3, min(200, args.steps // gr.R))
-            with torch.cuda.stream(stream):
+    kernel_ms = {}
+    for tag, call in gr.kernel_calls():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(gr.R):
+                call(r)
+        reps = max(3, min(200, steps // gr.R))
+        with torch.cuda.stream(stream):
+            g.replay()
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            for _ in range(reps):
                 g.replay()
-                k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                k0.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                k1.record(stream)
-            torch.cuda.synchronize()
-            kernel_ms.append(k0.elapsed_time(k1) / (reps * gr.R))
+            k1.record(stream)
+        torch.cuda.synchronize()
+        kernel_ms[tag] = k0.elapsed_time(k1) / (reps * gr.R)
+    q4k.q4k_check_device(stream)
 
     ms = max_over_ranks(ms, world, device)
 
     # end to end through the public API: activations from pinned host memory,
     # outputs back to pinned host memory, every step
-    e2e = None
-    if not wl.moe:
+    e2e_rec = None
+    if e2e and not wl.moe:
         hx = torch.from_numpy(np.concatenate([np.ascontiguousarray(x).view(np.int16).reshape(-1)
                                               for (*_, x) in wl.mats])).pin_memory()
         hy = torch.empty(gr.y_all.shape, dtype=torch.float32).pin_memory()
-        e2e_steps = min(args.steps, 2000)
+        e2e_steps = min(steps, 2000)
         with torch.cuda.stream(stream):
             for i in range(10):
                 gr.x_all.copy_(hx, non_blocking=True)
@@ -541,51 +564,100 @@ def run_gpu(args, rank, local_rank, world):
             torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
         ems = max_over_ranks(ems, world, device)
-        e2e = {"value": job_value(wl.value(ems / 1e3 / e2e_steps), world), "unit": wl.unit,
-               "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hy.numel() * 4),
-               "steps": e2e_steps}
+        e2e_rec = {"value": job_value(wl.value(ems / 1e3 / e2e_steps), world), "unit": wl.unit,
+                   "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hy.numel() * 4),
+                   "steps": e2e_steps}
 
     hbm, bf16, bf16_s, src = peaks()
-    sec_per_step = ms / 1e3 / args.steps
-    line = {
-        "metric": METRIC, "value": job_value(wl.value(sec_per_step), world), "unit": wl.unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("int8 (per-32 fp32 scales) x Q4_K -> fp32" if wl.x8 else
-                  "bf16 x NVFP4 -> fp32" if wl.fp4 else "bf16 x Q4_K -> fp32"),
-        "data": "synthetic (seeded N(0,0.02^2) weights quantized to Q4_K; N(0,1) bf16 activations)",
+    sec_per_step = ms / 1e3 / steps
+    rec = {
+        "value": job_value(wl.value(sec_per_step), world), "unit": wl.unit, "steps": steps, "warmup": warmup,
+        "ms_per_step": ms / steps,
         "config": dict(wl.config, l2="rotating %d weight sets, %.0f MB total > 129 MB L2" %
                        (gr.R, gr.R * (wl.weight_bytes() if not wl.moe else sum(
                            wl.moe[k].nbytes for k in ("gate", "up", "down"))) / 1e6),
                        parallelism="replicas x%d" % world, static_weights=True,
                        timing="CUDA graphs of %d steps, CUDA events; kernel times from per-kernel graphs" % gr.R),
-        "gpu_launches": gr.launches_per_step() * args.steps,
+        "gpu_launches": gr.launches_per_step() * steps,
     }
-    # roofline of the dominant kernel
-    if kernel_ms is not None and not wl.moe:
-        i_dom = int(np.argmax(kernel_ms))
-        tag, N, K, M, *_ = wl.mats[i_dom]
-        if wl.unit == "TFLOP/s":
-            algo = 2.0 * M * N * K
-            ach = algo / (kernel_ms[i_dom] / 1e3) / 1e12
-            line["roofline"] = {"bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
-                                "frac": ach / bf16, "traffic": profiled_traffic(tag), "kernel": tag,
-                                "kernel_us": kernel_ms[i_dom] * 1e3, "peak_source": src + " (burst)"}
-        else:
-            algo = N * K * 144 / 256 + (M * K + M * K // 32 * 4 if wl.x8 else M * K * 2) + M * N * 4
-            ach = algo / (kernel_ms[i_dom] / 1e3) / 1e9
-            line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                                "traffic": profiled_traffic(tag), "kernel": tag,
-                                "kernel_us": kernel_ms[i_dom] * 1e3, "algorithmic_bytes": algo,
-                                "peak_source": src, "frac_of_nominal_8tbs": ach / 8000.0}
-        line["kernels_us"] = {wl.mats[i][0]: kernel_ms[i] * 1e3 for i in range(len(kernel_ms))}
-    line["clocks"] = clocks.summary()
-    if spread:
-        line["spread"] = spread
-    if e2e:
-        line["e2e"] = e2e
-    if rank == 0 and args.workload == "decode" and not args.no_cpu:
+    # roofline of the dominant (slowest) kernel
+    tag = max(kernel_ms, key=kernel_ms.get)
+    bound, algo = gr.kernel_roofline(tag)
+    sec = kernel_ms[tag] / 1e3
+    if bound == "tensor":
+        ach = algo / sec / 1e12
+        rec["roofline"] = {"bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s", "frac": ach / bf16,
+                           "traffic": profiled_traffic(tag), "kernel": tag, "kernel_us": kernel_ms[tag] * 1e3,
+                           "algorithmic_flops": algo, "peak_source": src + " (burst)"}
+    else:
+        ach = algo / sec / 1e9
+        rec["roofline"] = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                           "traffic": profiled_traffic(tag), "kernel": tag, "kernel_us": kernel_ms[tag] * 1e3,
+                           "algorithmic_bytes": algo, "peak_source": src, "frac_of_nominal_8tbs": ach / 8000.0}
+    rec["kernels_us"] = {k: v * 1e3 for k, v in kernel_ms.items()}
+    rec["clocks"] = clocks.summary()
+    rec["spread"] = spread
+    if e2e_rec:
+        rec["e2e"] = e2e_rec
+    del gr
+    torch.cuda.empty_cache()
+    return rec
+
+
+# the other configurations, measured in the default run beside the decode
+# headline: (key, workload, tokens)
+SUB_WORKLOADS = (("verify_m4", "verify", 4), ("prefill_m4096", "prefill", 4096), ("prefill_m128", "prefill", 128),
+                 ("moe_t16", "moe", 16), ("moe_t2048", "moe", 2048))
+
+
+def run_gpu(args, rank, local_rank, world):
+    import torch
+    import torch.distributed as dist
+    from q4_weight_quantized_gb300.build import build_library
+    import q4_weight_quantized_gb300 as q4k
+
+    build_library()
+    q4k.load()
+    # weights are uploaded once and only read afterwards, as in serving: the
+    # small-M kernels may copy their first weight blocks while the previous
+    # kernel drains (include/q4k.h, q4k_set_static_weights)
+    q4k.q4k_set_static_weights(True)
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    stream = torch.cuda.Stream(device)
+
+    wl = Workload(args.workload, args.m)
+    rec = measure(wl, args, args.steps, args.warmup, stream, device, world, e2e=True)
+    line = {"metric": METRIC, "value": rec["value"], "unit": rec["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": ("int8 (per-32 fp32 scales) x Q4_K -> fp32" if wl.x8 else
+                      "bf16 x NVFP4 -> fp32" if wl.fp4 else "bf16 x Q4_K -> fp32"),
+            "data": "synthetic (seeded N(0,0.02^2) weights quantized to Q4_K; N(0,1) bf16 activations)"}
+    for k in ("config", "gpu_launches", "roofline", "kernels_us", "clocks", "spread", "e2e"):
+        if k in rec:
+            line[k] = rec[k]
+    if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+
+    # every other configuration, each timed the same way with its own step count
+    # (about half a second of timed work, at most --steps)
+    if args.workload == "decode" and not args.no_workloads:
+        subs = {}
+        for key, name, m in SUB_WORKLOADS:
+            swl = Workload(name, m)
+            est = swl.flops() / 1.0e15 if swl.unit == "TFLOP/s" else swl.weight_bytes() / 4.0e12
+            if swl.moe:
+                est = max(est, 2.0 * swl.flops() / 1.0e15)
+            n = int(max(2 * args.warmup, min(args.steps, 0.5 / max(est, 1e-6))))
+            r = measure(swl, args, n, args.warmup, stream, device, world, e2e=False)
+            r["config"] = dict(r["config"])
+            if rank == 0 and not args.no_cpu:
+                r["cpu_baseline"] = cpu_baseline(swl, budget_s=max(2.0, args.cpu_seconds / 3))
+            subs[key] = r
+        line["workloads"] = subs
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -595,24 +667,64 @@ def run_gpu(args, rank, local_rank, world):
 
 # ------------------------------------------------------------ oracle (CPU)
 
-def cpu_baseline(wl: Workload, budget_s: float = 12.0, rows_fraction: float = 1.0):
-    """Times the oracle (as it stands) on the host cores over the same inputs."""
+def cpu_baseline(wl: Workload, budget_s: float = 8.0):
+    """Times the oracle (as it stands) on the host cores over the same inputs, for
+    about `budget_s` seconds, in the workload's own unit.  Dense workloads run the
+    whole step while that fits the budget, else a sample of each matrix's rows
+    (every token); the MoE layer runs whole, or on a sample of its tokens.  A
+    sampled figure is the work done divided by the time taken, which is what the
+    full workload would give at the same rate."""
     import oracle
     oracle.build()
     np = wl.np
     threads = os.cpu_count() or 1
-    done_bytes, t_total, reps = 0.0, 0.0, 0
-    while t_total < budget_s:
-        for (_, N, K, M, blocks, x) in wl.mats:
-            n = max(1, int(N * rows_fraction))
-            sub = blocks if n == N else np.ascontiguousarray(blocks[:n])
+    if wl.moe:
+        mo = wl.moe
+        E, T, topk = mo["E"], mo["T"], mo["topk"]
+        def layer(n):  # the layer's three projections over the first n tokens
+            ids, gates = mo["ids"][:n], mo["gates"][:n]
+            x, xd = mo["x"][:n], mo["xd"][:n * topk]
             t = time.perf_counter()
-            oracle.gemm(sub, n, K, x, threads=threads)
+            oracle.moe(mo["gate"], E, 768, 2048, x, False, ids, threads=threads)
+            oracle.moe(mo["up"], E, 768, 2048, x, False, ids, threads=threads)
+            oracle.moe(mo["down"], E, 2048, 768, xd, True, ids, gates, threads=threads)
+            return time.perf_counter() - t
+
+        n0 = min(T, 4)
+        per_token = layer(n0) / n0  # calibration, not counted
+        t_sample = int(max(1, min(T, budget_s / 3 / max(per_token, 1e-9))))
+        done_tokens, t_total, reps = 0, 0.0, 0
+        while t_total < budget_s:
+            t_total += layer(t_sample)
+            done_tokens += t_sample
+            reps += 1
+        sec_per_layer = t_total / done_tokens * T
+        sample = (f"{reps} layer passes over {t_sample} of the {T} tokens, {t_total:.1f} s, time per layer "
+                  f"projected from the time per token; plain C, fp64 accumulate, {threads} pthreads")
+        value = wl.value(sec_per_layer)
+        return {"value": value, "unit": wl.unit, "cores": threads, "kind": "oracle", "sample": sample}
+    # dense: rows per matrix so that one pass over all matrices takes about a third
+    # of the budget (all rows when that fits)
+    t = time.perf_counter()
+    for (_, N, K, M, blocks, x) in wl.mats:
+        oracle.gemm(np.ascontiguousarray(blocks[:16]), 16, K, x, threads=threads)
+    per_row = (time.perf_counter() - t) / 16
+    rows = [max(1, min(N, int(budget_s / 3 / max(per_row, 1e-9) / len(wl.mats)))) for (_, N, *_) in wl.mats]
+    subs = [(np.ascontiguousarray(b[:n]) if n < N else b, n, K, M, x)
+            for (n, (_, N, K, M, b, x)) in zip(rows, wl.mats)]
+    done, t_total, reps = 0.0, 0.0, 0
+    while t_total < budget_s:
+        for (b, n, K, M, x) in subs:
+            t = time.perf_counter()
+            oracle.gemm(b, n, K, x, threads=threads)
             t_total += time.perf_counter() - t
-            done_bytes += n * K * 144 / 256
+            done += 2.0 * M * n * K if wl.unit == "TFLOP/s" else n * K * 144 / 256
         reps += 1
-    return {"value": done_bytes / t_total / 1e9, "unit": wl.unit, "cores": threads, "kind": "oracle",
-            "sample": f"{reps} full decode steps (both matrices, all rows), {t_total:.1f} s, plain C, "
+    value = done / t_total / (1e12 if wl.unit == "TFLOP/s" else 1e9)
+    full = all(n == N for n, (_, N, *_) in zip(rows, wl.mats))
+    what = "all rows" if full else "rows " + " and ".join(f"{n} of {N}" for n, (_, N, *_) in zip(rows, wl.mats))
+    return {"value": value, "unit": wl.unit, "cores": threads, "kind": "oracle",
+            "sample": f"{reps} passes over {what} of each matrix, every token, {t_total:.1f} s, plain C, "
                       f"fp64 accumulate, rows split over {threads} pthreads"}
 
 
@@ -670,8 +782,10 @@ def main():
                                            "prefill_nvfp4", "moe", "moe_ffn"],
                     default="decode")
     ap.add_argument("--m", type=int, default=None, help="tokens (verify: 4, prefill: 4096, moe: 2048)")
-    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline legs")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="decode: skip the other configurations' records (verify, prefill, MoE)")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     args = ap.parse_args()
     if args.m is None:
         args.m = {"decode": 1, "decode_x8": 1, "decode_nvfp4": 1, "verify": 4, "prefill": 4096, "prefill_nvfp4": 4096, "moe": 2048,

@@ -68,7 +68,8 @@ typedef enum {
     Q4K_ERR_WORKSPACE = 4,
     Q4K_ERR_DEVICE = 5,
     Q4K_ERR_CUDA = 6,
-    Q4K_ERR_TIMEOUT = 7
+    Q4K_ERR_TIMEOUT = 7,
+    Q4K_ERR_ROUTING = 8
 } q4k_status;
 
 /* Static English text for a status code; never NULL. */
@@ -85,8 +86,10 @@ size_t q4k_row_bytes(int64_t K);
 int q4k_version(void);
 
 /* Synchronizes `stream`, then reads and clears the device status word that the
- * kernels set when a bounded wait gives up.  Returns Q4K_OK, Q4K_ERR_TIMEOUT, or
- * Q4K_ERR_CUDA if the synchronization itself failed. */
+ * kernels set when a bounded wait gives up (Q4K_ERR_TIMEOUT) or when a call of
+ * q4k_moe_grouped_gemm_reuse_routing found no routing for its shape in its
+ * workspace (Q4K_ERR_ROUTING; a timeout is reported first).  Returns Q4K_OK,
+ * one of those two, or Q4K_ERR_CUDA if the synchronization itself failed. */
 q4k_status q4k_check_device(void *stream);
 
 /* Declares whether the weight matrices read by the small-M calls (q4k_gemv,
@@ -248,7 +251,9 @@ typedef enum {
  *              per-slot fp32 rows; contents need not be initialized
  * Errors: NULL, SHAPE (as q4k_moe_route, plus N < 1, bad K, E*N >= 2^31, an
  * unknown mode, N % 4 != 0 with Q4K_MOE_Y_COMBINE), ALIGN, WORKSPACE, DEVICE,
- * CUDA.  q4k_moe_workspace_size returns 0 for arguments that would give SHAPE. */
+ * CUDA.  q4k_moe_workspace_size returns 0 for arguments that would give SHAPE.
+ * It takes the output mode as well as the shape (an addition to the plain
+ * shape query): only Q4K_MOE_Y_COMBINE needs room for the per-slot rows. */
 size_t q4k_moe_workspace_size(int32_t n_experts, int64_t N, int64_t K, int64_t T, int32_t topk, int y_mode);
 q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_t N, int64_t K, const uint16_t *x,
                                 int x_mode, const int32_t *topk_ids, const float *gates, int64_t T, int32_t topk,
@@ -260,16 +265,21 @@ q4k_status q4k_moe_grouped_gemm(const void *w_experts, int32_t n_experts, int64_
  * routing), so after one q4k_moe_grouped_gemm call has sorted the items into
  * `ws`, the layer's other projections can use that sort instead of repeating it.
  * Same arguments, results and errors as q4k_moe_grouped_gemm (same bits), under
- * these conditions, which cannot be checked:
+ * these conditions:
  *   - `ws` holds the routing written by the last q4k_moe_grouped_gemm call that
  *     used it (calls to this function leave it unchanged, so any number of them
  *     may follow one routing call), ordered before this call on the GPU;
- *   - that call had the same n_experts, T and topk, and topk_ids has not changed
- *     since.
- * N, K, x, x_mode, gates, y and y_mode may differ from that call; ws_bytes must
- * cover this call (q4k_moe_workspace_size), and the routing part of the
- * workspace depends only on (n_experts, T, topk).  A stale routing gives wrong
- * results, not an error. */
+ *   - that call had the same n_experts and the same number of items T*topk, and
+ *     topk_ids has not changed since.
+ * The routing records the (n_experts, T*topk) it was made for, and the kernels
+ * check it on the GPU before reading any of it: a workspace holding a routing
+ * for another shape, or none, makes the call write nothing, and the next
+ * q4k_check_device reports Q4K_ERR_ROUTING.  (With at most 16 items no routing
+ * is used at all.)  That topk_ids is unchanged is not checked: changed ids give
+ * wrong results, not an error.  N, K, x, x_mode, gates, y and y_mode may differ
+ * from the routing call; ws_bytes must cover this call
+ * (q4k_moe_workspace_size), and the routing part of the workspace depends only
+ * on (n_experts, T, topk). */
 q4k_status q4k_moe_grouped_gemm_reuse_routing(const void *w_experts, int32_t n_experts, int64_t N, int64_t K,
                                               const uint16_t *x, int x_mode, const int32_t *topk_ids,
                                               const float *gates, int64_t T, int32_t topk, float *y, int y_mode,
@@ -321,8 +331,10 @@ q4k_status q4k_moe_ffn(const void *w_gate, const void *w_up, const void *w_down,
  * library, which every GPU that loads the library keeps allocated until the
  * process exits.  It allocates nothing itself.
  *   - The first call on a device looks up that device's scratch address
- *     (cudaGetSymbolAddress, with the device current).  Make that first call
- *     before capturing a stream into a CUDA graph.
+ *     (cudaGetSymbolAddress, with the device current), and so does the first
+ *     call in a context of that device created since (cudaDeviceReset destroys
+ *     the context the address belonged to).  Make that first call before
+ *     capturing a stream into a CUDA graph.
  *   - Every call on a device shares the one array.  Calls whose kernels can
  *     overlap on the GPU (different streams without ordering between them) race
  *     on it and give wrong results; order them on one stream.

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libq4k.so")
 
 Q4K_OK, Q4K_ERR_NULL, Q4K_ERR_SHAPE, Q4K_ERR_ALIGN = 0, 1, 2, 3
-Q4K_ERR_WORKSPACE, Q4K_ERR_DEVICE, Q4K_ERR_CUDA, Q4K_ERR_TIMEOUT = 4, 5, 6, 7
+Q4K_ERR_WORKSPACE, Q4K_ERR_DEVICE, Q4K_ERR_CUDA, Q4K_ERR_TIMEOUT, Q4K_ERR_ROUTING = 4, 5, 6, 7, 8
 Q4K_MOE_X_PER_TOKEN, Q4K_MOE_X_PER_SLOT = 0, 1
 Q4K_MOE_Y_PER_SLOT, Q4K_MOE_Y_COMBINE = 0, 1
 

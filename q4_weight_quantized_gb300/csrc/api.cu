@@ -10,6 +10,7 @@
 
 #include "q4k.h"
 #include "q4k_internal.h"
+#include "q4k_ptx.cuh"
 
 namespace q4k {
 
@@ -30,10 +31,15 @@ q4k_status cuda_fail(cudaError_t e) {
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
 bool g_dev_ready[kMaxDevices];
+unsigned long long g_dev_ctx[kMaxDevices];  // context the cached entry was made in
 DeviceInfo g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -41,13 +47,35 @@ bool k_ok(int64_t K) { return K > 0 && K % kQK == 0 && K <= (int64_t)1 << 30; }
 
 }  // namespace
 
+unsigned long long context_id() {
+    std::call_once(g_ctx_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!g_ctx_current || !g_ctx_id || g_ctx_current(&c) != CUDA_SUCCESS || !c || g_ctx_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 cudaError_t device_info(DeviceInfo *out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    // the status word's address belongs to the device's current context: a context
+    // made since the entry was cached (after cudaDeviceReset, say) is looked up anew
+    unsigned long long ctx = context_id();
     std::lock_guard<std::mutex> lock(g_dev_mutex);
-    if (!g_dev_ready[dev]) {
+    if (!g_dev_ready[dev] || ctx == 0 || ctx != g_dev_ctx[dev]) {
         DeviceInfo di = {};
         di.device = dev;
         if ((e = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -63,14 +91,17 @@ cudaError_t device_info(DeviceInfo *out) {
         }
         g_dev[dev] = di;
         g_dev_ready[dev] = true;
+        g_dev_ctx[dev] = context_id();  // the symbol lookup above made the context current
     }
     *out = g_dev[dev];
     return cudaSuccess;
 }
 
 cudaError_t ensure_smem(const void *kern, int bytes) {
+    // keyed by context as well: a re-created context starts from the default limit
     struct Entry {
         const void *kern;
+        unsigned long long ctx;
         int device, bytes;
     };
     static std::mutex mu;
@@ -79,16 +110,18 @@ cudaError_t ensure_smem(const void *kern, int bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const unsigned long long ctx = context_id();
     std::lock_guard<std::mutex> lock(mu);
     int i = 0;
     while (i < used && !(table[i].kern == kern && table[i].device == dev)) ++i;
-    if (i < used && table[i].bytes >= bytes) return cudaSuccess;
+    if (i < used && ctx != 0 && table[i].ctx == ctx && table[i].bytes >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     if (i < used) {
-        table[i].bytes = bytes;
+        if (table[i].ctx != ctx || table[i].bytes < bytes) table[i].bytes = bytes;
+        table[i].ctx = ctx;
     } else if (used < 256) {
-        table[used++] = {kern, dev, bytes};
+        table[used++] = {kern, ctx, dev, bytes};
     }
     return cudaSuccess;
 }
@@ -202,6 +235,7 @@ const char *q4k_status_string(int status) {
         case Q4K_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
         case Q4K_ERR_CUDA: return "a CUDA runtime call failed";
         case Q4K_ERR_TIMEOUT: return "a kernel gave up waiting on a barrier";
+        case Q4K_ERR_ROUTING: return "a call reusing a routing found one made for another shape";
         default: return "unknown status";
     }
 }
@@ -225,7 +259,7 @@ q4k_status q4k_check_device(void *stream) {
     if (v != 0) {
         const unsigned int zero = 0;
         if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(e);
-        return Q4K_ERR_TIMEOUT;
+        return (v & kDevTimeout) ? Q4K_ERR_TIMEOUT : Q4K_ERR_ROUTING;
     }
     return Q4K_OK;
 }
@@ -416,7 +450,7 @@ static q4k_status moe_common(const void *w_experts, int32_t n_experts, int64_t N
         e = launch_moe_route(topk_ids, T * topk, n_experts, offsets, perm, true, tiles, n_tiles, s);
     if (e == cudaSuccess && tc)
         e = launch_moe_gather(di, x, x_mode, topk, perm, offsets, n_experts, T * topk, K, x_sorted,
-                              per_slot ? y : nullptr, N, s);
+                              per_slot ? y : nullptr, N, n_tiles, s);
     // with very few items the small-M kernel combines in the CTA, straight into y
     const bool dcomb = !tc && !per_slot && moe_direct(T * topk);
     if (e == cudaSuccess)
@@ -503,7 +537,7 @@ q4k_status q4k_moe_ffn(const void *w_gate, const void *w_up, const void *w_down,
         glu.h = h;
         glu.h_sorted = 1;
         if (e == cudaSuccess)
-            e = launch_moe_gather(di, x, 0, topk, perm, offsets, E, n, D, x_sorted, nullptr, H, s);
+            e = launch_moe_gather(di, x, 0, topk, perm, offsets, E, n, D, x_sorted, nullptr, H, n_tiles, s);
         if (e == cudaSuccess) e = launch_moe_tcp(di, w_gate, E, H, D, x_sorted, n, perm, tiles, n_tiles, g, s);
         if (e == cudaSuccess)
             e = launch_moe_tcp(di, w_up, E, H, D, x_sorted, n, perm, tiles, n_tiles, nullptr, s, glu);

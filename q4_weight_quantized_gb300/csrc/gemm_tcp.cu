@@ -61,7 +61,8 @@ struct Params {
     int tiles_n;           // 128-row weight tiles per expert
     const int32_t *perm;   // routing permutation
     const int4 *tiles;     // MoE: (expert, first item, count, -)
-    const int *n_tiles;    // number of token tiles
+    const int *n_tiles;    // number of token tiles; then the routing's (E, items, stamp)
+    int E, n_items;        // this call's shape, checked against the routing's
     unsigned int *status;
     GluOut glu;            // SwiGLU epilogue (up projection of an expert FFN)
 };
@@ -115,6 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
     unsigned int *status = p.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a routing made for another shape: leave before any barrier or allocation
+    if (!routing_matches(p.n_tiles, p.E, p.n_items, status)) return;
     const int tiles_m = __ldg(p.n_tiles);
     const int total_tiles = p.tiles_n * tiles_m;
     const int my_tiles =
@@ -408,6 +411,8 @@ cudaError_t launch_moe_tcp(const DeviceInfo &di, const void *w_experts, int E, i
     p.perm = perm;
     p.tiles = tiles;
     p.n_tiles = n_tiles;
+    p.E = E;
+    p.n_items = (int)n_items;
     p.status = di.status;
     p.glu = glu;
     return launch(tmW, tmX, p, di.sm_count, s);

@@ -143,7 +143,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t *__r
             tiles[f0 + k] = make_int4(e0, x0 + k * kMoeTileItems, min(kMoeTileItems, total[e0] - k * kMoeTileItems), 0);
         for (int k = 0; k < nt1; ++k)
             tiles[f1 + k] = make_int4(e1, x1 + k * kMoeTileItems, min(kMoeTileItems, total[e1] - k * kMoeTileItems), 0);
-        if (tid == 0) *n_tiles = nt;
+        if (tid == 0) {
+            n_tiles[0] = nt;
+            n_tiles[1] = E;  // the shape this routing was made for (checked on reuse)
+            n_tiles[2] = n_items;
+            n_tiles[3] = kRoutingStamp;
+        }
     }
     __syncthreads();
     // 3. stable scatter: each warp walks its run in item order
@@ -208,9 +213,10 @@ __global__ void combine_kernel(const float *__restrict__ out, const float *__res
 __global__ void gather_kernel(const uint16_t *__restrict__ x, int x_per_slot, int topk,
                               const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets, int E,
                               int64_t K, uint16_t *__restrict__ x_sorted, float *__restrict__ zero_y, int64_t N,
-                              int n_items) {
+                              int n_items, const int *__restrict__ hdr, unsigned int *status) {
     pdl_wait();
     pdl_trigger();
+    if (!routing_matches(hdr, E, n_items, status)) return;  // not this call's routing: read none of it
     const int n_valid = __ldg(offsets + E);
     const int lane = threadIdx.x & 31;
     const int64_t chunks = K / 8;  // 16-byte chunks per row
@@ -233,13 +239,13 @@ __global__ void gather_kernel(const uint16_t *__restrict__ x, int x_per_slot, in
 
 cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per_slot, int topk, const int32_t *perm,
                               const int32_t *offsets, int E, int64_t n_items, int64_t K, uint16_t *x_sorted,
-                              float *zero_y, int64_t N, cudaStream_t s) {
+                              float *zero_y, int64_t N, const int *hdr, cudaStream_t s) {
     int64_t blocks = (n_items + 7) / 8;
     const int64_t cap = (int64_t)di.sm_count * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return launch_pdl(gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, dim3(1), x, x_per_slot, topk, perm, offsets,
-                      E, K, x_sorted, zero_y, N, (int)n_items);
+                      E, K, x_sorted, zero_y, N, (int)n_items, hdr, di.status);
 }
 
 size_t route_smem_bytes(int E) { return (size_t)(E + 1) * (2 + kWhStride) * 4; }

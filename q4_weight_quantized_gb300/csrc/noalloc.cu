@@ -14,13 +14,16 @@
 // The array is a file-scope __device__ object, so every GPU that loads this
 // library holds Q4K_MOE_NOALLOC_SCRATCH_BYTES of device memory for it until the
 // process exits.  In host code its name is only a stand-in: the device address
-// is looked up with cudaGetSymbolAddress, once per device, with that device
-// current, the first time the entry point runs on it.
+// is looked up with cudaGetSymbolAddress, with the device current, the first
+// time the entry point runs on a device - and again the first time it runs in a
+// context of that device made since (cudaDeviceReset destroys the context the
+// address belonged to; the array may land elsewhere in the next one).
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "q4k.h"
+#include "q4k_internal.h"
 
 namespace {
 
@@ -28,18 +31,22 @@ static __device__ __align__(256) unsigned char g_moe_scratch[Q4K_MOE_NOALLOC_SCR
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices];  // device address of g_moe_scratch, per device
+void *g_scratch_ptr[kMaxDevices];              // device address of g_moe_scratch, per device
+unsigned long long g_scratch_ctx[kMaxDevices];  // the context that address belongs to
 
-// Device address of the scratch array on the current device (set up on first use).
+// Device address of the scratch array in the current device's current context
+// (looked up on first use there).
 q4k_status scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return Q4K_ERR_DEVICE;
+    const unsigned long long ctx = q4k::context_id();  // 0: no context current yet
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_moe_scratch);
         if (e != cudaSuccess || !p) return e == cudaErrorNoDevice ? Q4K_ERR_DEVICE : Q4K_ERR_CUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = q4k::context_id();  // the lookup made the context current
     }
     *out = g_scratch_ptr[dev];
     return Q4K_OK;

@@ -21,8 +21,14 @@ struct DeviceInfo {
     unsigned int *status;  // device address of the status word
 };
 
-// Current device's cached properties (first call per device queries them).
+// Current device's cached properties (first call per device, and per context
+// of that device, queries them).
 cudaError_t device_info(DeviceInfo *out);
+
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), 0 if no
+// context is current.  Caches of device addresses are keyed on it, so that a
+// context re-created after cudaDeviceReset never sees a stale address.
+unsigned long long context_id();
 
 cudaError_t launch_dequant_f32(const void *w, int64_t N, int64_t K, float *out, cudaStream_t s);
 cudaError_t launch_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *out, cudaStream_t s);
@@ -102,7 +108,8 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
 // outside [0, E) are left out of offsets; with invalid_tail they follow the
 // valid items in perm (item order), otherwise that tail of perm is -1.  When
 // tiles is given, it also lists every (expert, first item, item count) token
-// tile of at most kMoeTileItems items, and *n_tiles receives their number.
+// tile of at most kMoeTileItems items, and n_tiles[0..3] receives their number,
+// E, n_items and kRoutingStamp.
 constexpr int kMoeTileItems = 256;
 size_t route_smem_bytes(int E);
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
@@ -119,9 +126,12 @@ inline int64_t moe_max_tiles(int E, int64_t n_items) {
 // (x[item / topk]) or per-slot rows (x[item]), K bf16 each.  With zero_y, the N
 // floats of zero_y's row of every invalid item (perm[offsets[E] .. n_items)) are
 // zeroed.
+// hdr: the routing header (tile count, E, items, stamp) written by the routing
+// kernel; a header made for another (E, n_items) makes the kernel record
+// kDevRouting and leave (so do the expert kernels).
 cudaError_t launch_moe_gather(const DeviceInfo &di, const uint16_t *x, int x_per_slot, int topk, const int32_t *perm,
                               const int32_t *offsets, int E, int64_t n_items, int64_t K, uint16_t *x_sorted,
-                              float *zero_y, int64_t N, cudaStream_t s);
+                              float *zero_y, int64_t N, const int *hdr, cudaStream_t s);
 
 // y[t] = sum_j gates[t][j] * out[t*topk+j] in slot order (N % 4 == 0)
 cudaError_t launch_moe_combine(const DeviceInfo &di, const float *out, const float *gates, const int32_t *ids, int E,

@@ -13,6 +13,10 @@
 namespace q4k {
 
 constexpr unsigned int kDevTimeout = 1u;         // status bit: a bounded wait gave up
+constexpr unsigned int kDevRouting = 2u;         // status bit: a reused routing was made for another call shape
+// Written by the routing kernel after the tile count, with (E, item count): a
+// call that reuses the routing checks that it was made for its own shape.
+constexpr int kRoutingStamp = 0x5134524B;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -90,6 +94,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
             return false;
         }
     }
+}
+
+// Whether the routing header hdr = {tile count, E, items, stamp} in the workspace
+// was written for E experts and n_items items; if not, thread 0 of CTA 0 records
+// kDevRouting in *status (the caller then leaves before touching the routing).
+__device__ __forceinline__ bool routing_matches(const int *hdr, int E, int n_items, unsigned int *status) {
+    const bool ok = __ldg(hdr + 1) == E && __ldg(hdr + 2) == n_items && __ldg(hdr + 3) == kRoutingStamp;
+    if (!ok && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(status, kDevRouting);
+    return ok;
 }
 
 // ---------------------------------------------------------------------- TMA

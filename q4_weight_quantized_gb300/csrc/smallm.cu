@@ -501,7 +501,9 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
     }
     if constexpr (MOE && !DC) if (!ra.direct) {
         // grid layer z = token tile z of the routing (only tiles of experts that have items);
-        // the layer right after the last tile zeroes the invalid items' rows of this row tile
+        // the layer right after the last tile zeroes the invalid items' rows of this row tile.
+        // A routing made for another shape: leave before any barrier, reading none of it
+        if (!routing_matches(ra.n_tiles, ra.E, ra.n_items, status)) return;
         const int n_tl = __ldg(ra.n_tiles);
         if ((int)blockIdx.z >= n_tl) {  // leave before any barrier
             if ((int)blockIdx.z == n_tl && ra.zero_invalid)
@@ -810,14 +812,24 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             const uint32_t dst = map_shared_rank(smem_u32(land + (split - 1) * elems), 0);
             for (int e = threadIdx.x; e < elems; e += kThreads) st_shared_cluster_f32(dst + 4u * e, red[e]);
             mbar_arrive_cluster(map_shared_rank(lbar, 0));
-        } else if (mbar_wait_cluster(lbar, 0, status, (SLOTS + 2) * 4 * kWaitLimitNs)) {
+            // second cluster-barrier phase: this rank's stores into rank 0 are done; it
+            // arrives and leaves without waiting
+            cluster_arrive();
+        } else {
             // (the limit outlasts every bounded wait a pushing rank can make first)
-            for (int e = threadIdx.x; e < elems; e += kThreads) {
-                float v = red[e];
-                for (int q = 1; q < S; ++q) v += land[(q - 1) * elems + e];
-                const int tk = e / kRows, rr = e % kRows;
-                if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = FP4 ? ra.gscale * v : v;
+            if (mbar_wait_cluster(lbar, 0, status, (SLOTS + 2) * 4 * kWaitLimitNs)) {
+                for (int e = threadIdx.x; e < elems; e += kThreads) {
+                    float v = red[e];
+                    for (int q = 1; q < S; ++q) v += land[(q - 1) * elems + e];
+                    const int tk = e / kRows, rr = e % kRows;
+                    if (row0 + rr < N) ra.y[yoff_s[tk] + row0 + rr] = FP4 ? ra.gscale * v : v;
+                }
             }
+            // rank 0 leaves only after every other rank has arrived on the second phase,
+            // that is after its last store into this CTA's shared memory - also when the
+            // landing wait above gave up (the other ranks' own waits are bounded)
+            cluster_arrive();
+            cluster_wait();
         }
     } else if (S > 1) {
         cluster_sync();  // every split's partial is in its shared memory

@@ -542,6 +542,45 @@ def test_moe_reuse_routing_same_bits(syn, moe_up, moe_down, T):
 
 
 
+@pytest.mark.parametrize("T,T2", [(16, 20), (600, 601)])
+def test_moe_reuse_routing_checks_the_shape(syn, moe_up, T, T2):
+    # a routing made for T tokens reused by a call with T2: the kernels find the
+    # workspace's routing stamped with another item count, write nothing, and
+    # q4k_check_device reports it; a workspace that never held a routing is
+    # refused the same way; the next ordinary call is unaffected
+    E, topk = G.MOE_E, G.MOE_TOPK
+    N, K = G.MOE_UP
+    P = q4k.Q4K_MOE_Y_PER_SLOT
+    wu = G.dev(moe_up)
+    size = max(q4k.q4k_moe_workspace_size(E, N, K, t, topk, P) for t in (T, T2))
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    ids, gates = syn.routing(70 + T, 71 + T, T2, E, topk)
+    idd, gd = G.dev(ids), G.dev(gates)
+    x = G.dev(G.activations(4, 22, T2, K))
+
+    def call(fn, t):
+        y = torch.full((t, topk, N), float("nan"), dtype=torch.float32, device="cuda")
+        fn(wu, E, N, K, x, q4k.Q4K_MOE_X_PER_TOKEN, idd, gd, t, topk, y, P, ws, size)
+        return y
+
+    y = call(q4k.q4k_moe_grouped_gemm_reuse_routing, T2)  # nothing routed yet
+    with pytest.raises(q4k.Q4KError) as err:
+        q4k.q4k_check_device()
+    assert err.value.status == q4k.Q4K_ERR_ROUTING
+    assert np.isnan(G.host(y)).all()
+    call(q4k.q4k_moe_grouped_gemm, T)  # a routing for the first T tokens
+    y = call(q4k.q4k_moe_grouped_gemm_reuse_routing, T2)
+    with pytest.raises(q4k.Q4KError) as err:
+        q4k.q4k_check_device()
+    assert err.value.status == q4k.Q4K_ERR_ROUTING
+    assert np.isnan(G.host(y)).all()
+    good = call(q4k.q4k_moe_grouped_gemm, T2)
+    again = call(q4k.q4k_moe_grouped_gemm_reuse_routing, T2)
+    q4k.q4k_check_device()
+    a, b = G.host(good), G.host(again)
+    assert not np.isnan(a).any() and np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
 @pytest.mark.parametrize("K", [768, 2048])
 def test_moe_few_items_direct(ref, syn, K):
     # up to 16 items: every item is its own grid layer, its expert read from the ids

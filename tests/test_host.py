@@ -40,8 +40,13 @@ def test_row_bytes_and_strings(lib):
     assert q4k.q4k_row_bytes(5120) == 20 * 144
     assert q4k.q4k_row_bytes(17408) == 68 * 144
     assert q4k.q4k_row_bytes(100) == 0 and q4k.q4k_row_bytes(0) == 0 and q4k.q4k_row_bytes(-256) == 0
-    for s in range(0, 9):
+    for s in range(0, 10):
         assert isinstance(q4k.status_string(s), str) and q4k.status_string(s)
+    # every status the header declares has its own text (9: unknown)
+    texts = [q4k.status_string(s) for s in range(0, 9)]
+    assert len(set(texts)) == 9 and q4k.status_string(9) == "unknown status"
+    src = open(os.path.join(ROOT, "include", "q4k.h")).read()
+    assert "Q4K_ERR_ROUTING = 8" in src and q4k.Q4K_ERR_ROUTING == 8
     assert q4k.q4k_version() >= 100
 
 
