@@ -111,6 +111,22 @@ q4k_status q4k_check_device(void *stream);
  * previous setting (0 or 1). */
 int q4k_set_static_weights(int enable);
 
+/* Batch-invariant mode.  The pages' serving engines pick their decode kernels by
+ * the step's token count, so a token's logits can change with how many tokens
+ * share the step; their deterministic mode removes that for a small cost
+ * (sparkinfer-server README, "Determinism").  Here every call is run-to-run
+ * deterministic in either mode; this switch is about batch invariance:
+ *   off (default): M = 1 runs the decode GEMV kernel (sub-blocks in the MMA
+ *       columns: the fastest one-token form), whose rounding differs from the
+ *       2..16-token kernel's (both within the small-M bar).  Rows of calls with
+ *       2 <= M <= 16 tokens equal each other bit for bit.
+ *   on: M = 1 runs the 2..16-token kernel as well, so row m of any call with
+ *       M <= 16 equals the one-token call on row m bit for bit.
+ * Calls with M > 16 take the tensor-core path either way (different bits from the
+ * small-M path).  Process-wide; applies to calls enqueued after it returns.
+ * Returns the previous setting (0 or 1). */
+int q4k_set_batch_invariant(int enable);
+
 /* ----------------------------------------------------------------- dequant --
  * Standalone dequantization of an N x K Q4_K matrix:
  *     out[n][k] = d*sc_s*q - dmin*m_s   (fp32, computed as fp32 multiplies and one
@@ -128,7 +144,9 @@ q4k_status q4k_dequant_bf16(const void *w, int64_t N, int64_t K, uint16_t *out, 
  * Decode projection, one token:  y[n] = sum_k x[k] * w[n][k]   (n < N, k < K)
  * Same as q4k_gemm with M = 1 and the same bits.  The decode path of the pages
  * carries no floating-point atomics (sparkinfer-server README, "Determinism");
- * neither does this one.
+ * neither does this one.  Activations must be finite and below 2^63 in
+ * magnitude (the kernel scales them by 2^64 inside its tensor-core operands);
+ * magnitudes below 2^-56 lose relative precision there.
  *   w  device Q4_K blocks, 16-byte aligned;  x  device bf16[K], 16-byte aligned;
  *   y  device fp32[N], 4-byte aligned.
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA. */
@@ -139,8 +157,9 @@ q4k_status q4k_gemv(const void *w, int64_t N, int64_t K, const uint16_t *x, floa
  *   M <= 16 : the small-M path (decode and speculative verification, 1 + drafts
  *             tokens per lane; ninfer serving docs "Determinism"): exact integer
  *             tensor-core products per 32-weight sub-block, fp32 scaling and
- *             accumulation.  Row m of the result does not depend on M (the same
- *             bits as q4k_gemv on row m alone).
+ *             accumulation.  M = 1 is the decode GEMV (q4k_gemv).  For 2 <= M <=
+ *             16, row m of the result does not depend on M; with
+ *             q4k_set_batch_invariant(1) that holds for M = 1 too.
  *   M >  16 : the prefill path (sparkinfer-server README, "Serve a GGUF instead of
  *             NVFP4"): each weight tile is dequantized to bf16 in shared memory and
  *             multiplied on the tcgen05 tensor cores with fp32 accumulation in

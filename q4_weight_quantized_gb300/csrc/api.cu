@@ -18,6 +18,8 @@ __device__ unsigned int g_status_word;  // kernels OR Q4K_DEV_* bits here
 
 // q4k_set_static_weights (process-wide, default off)
 static std::atomic<int> g_static_weights{0};
+// q4k_set_batch_invariant (process-wide, default off)
+static std::atomic<int> g_batch_invariant{0};
 
 namespace {
 
@@ -248,6 +250,8 @@ int q4k_version(void) { return 100; }
 
 int q4k_set_static_weights(int enable) { return g_static_weights.exchange(enable ? 1 : 0); }
 
+int q4k_set_batch_invariant(int enable) { return g_batch_invariant.exchange(enable ? 1 : 0); }
+
 q4k_status q4k_check_device(void *stream) {
     DeviceInfo di;
     q4k_status st = check_device(&di);
@@ -305,10 +309,15 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
     q4k_status st = check_device(&di);
     if (st != Q4K_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // M <= 16: small-M kernel; otherwise the tensor-core kernel, one CTA per
-    // output tile (with a cluster K split when the tiles leave the GPU half idle)
+    // M = 1: the decode GEMV kernel, unless batch invariance is asked for (then the
+    // small-M kernel, whose rows do not depend on M); M <= 16: small-M kernel;
+    // otherwise the tensor-core kernel, one CTA per output tile (with a cluster K
+    // split when the tiles leave the GPU half idle)
+    const bool early = g_static_weights.load(std::memory_order_relaxed) != 0;
+    const bool invariant = g_batch_invariant.load(std::memory_order_relaxed) != 0;
     cudaError_t e;
-    if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, g_static_weights.load(std::memory_order_relaxed) != 0, s);
+    if (M == 1 && !invariant) e = launch_gemv(di, w, N, K, x, y, early, s);
+    else if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, early, s);
     else e = launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }

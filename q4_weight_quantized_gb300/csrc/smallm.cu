@@ -812,9 +812,9 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             const uint32_t dst = map_shared_rank(smem_u32(land + (split - 1) * elems), 0);
             for (int e = threadIdx.x; e < elems; e += kThreads) st_shared_cluster_f32(dst + 4u * e, red[e]);
             mbar_arrive_cluster(map_shared_rank(lbar, 0));
-            // second cluster-barrier phase: this rank's stores into rank 0 are done; it
-            // arrives and leaves without waiting
-            cluster_arrive();
+            // second cluster-barrier phase: this rank's stores into rank 0 are done (the
+            // arrive above released them); it arrives and leaves without waiting
+            cluster_arrive_relaxed();
         } else {
             // (the limit outlasts every bounded wait a pushing rank can make first)
             if (mbar_wait_cluster(lbar, 0, status, (SLOTS + 2) * 4 * kWaitLimitNs)) {
@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(kThreads) smallm_kernel(const __grid_constant_
             // rank 0 leaves only after every other rank has arrived on the second phase,
             // that is after its last store into this CTA's shared memory - also when the
             // landing wait above gave up (the other ranks' own waits are bounded)
-            cluster_arrive();
+            cluster_arrive_relaxed();
             cluster_wait();
         }
     } else if (S > 1) {

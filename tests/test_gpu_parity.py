@@ -43,6 +43,18 @@ def _lib():
     q4k.q4k_check_device()
 
 
+class batch_invariant:
+    """q4k_set_batch_invariant(1) for the duration of a with-block (one-token calls
+    then run the 2..16-token kernel)."""
+
+    def __enter__(self):
+        self.prev = q4k.q4k_set_batch_invariant(True)
+        return self
+
+    def __exit__(self, *a):
+        q4k.q4k_set_batch_invariant(self.prev)
+
+
 def gpu_dequant(blocks, N, K, bf16=False):
     w = G.dev(blocks)
     out = torch.empty((N, K), dtype=torch.int16 if bf16 else torch.float32, device="cuda")
@@ -179,9 +191,12 @@ def test_batch_invariance_and_determinism():
     assert np.array_equal(y16.view(np.uint32), y16b.view(np.uint32)), "not run-to-run deterministic"
     y4 = gpu_gemm(b, N, K, x[:4], w_dev=w)
     assert np.array_equal(y4.view(np.uint32), y16[:4].view(np.uint32))
-    for m in (0, 5, 15):
-        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
-        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+    y2 = gpu_gemm(b, N, K, x[5:7], w_dev=w)
+    assert np.array_equal(y2.view(np.uint32), y16[5:7].view(np.uint32))
+    with batch_invariant():
+        for m in (0, 5, 15):
+            y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+            assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
 
 
 @pytest.mark.parametrize("KB", [1, 2, 3, 6, 7, 9, 11, 13])
@@ -194,10 +209,15 @@ def test_smallm_uneven_warp_blocks(ref, KB):
     w = G.dev(b)
     y16 = gpu_gemm(b, N, K, x, w_dev=w)
     rows = G.sample_rows(N, 256)
-    assert G.rel_err(y16[:, rows], ref.gemm(G.rows_of(b, rows), len(rows), K, x)) <= TOL_SMALL
-    for m in (0, 9):
-        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
-        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x)
+    assert G.rel_err(y16[:, rows], want) <= TOL_SMALL
+    with batch_invariant():
+        for m in (0, 9):
+            y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+            assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+    # the decode GEMV kernel on the same uneven splits
+    y1 = gpu_gemm(b, N, K, x[9:10], w_dev=w)
+    assert G.rel_err(y1[:, rows], want[9:10]) <= TOL_SMALL
 
 
 @pytest.mark.parametrize("N,K", [(600, 16384), (1000, 17408)])
@@ -209,10 +229,15 @@ def test_smallm_cluster_split_of_eight(ref, N, K):
     w = G.dev(b)
     y16 = gpu_gemm(b, N, K, x, w_dev=w)
     rows = np.unique(np.concatenate([G.sample_rows(N, 96, seed=5), np.arange(N - 8, N)]))
-    assert G.rel_err(y16[:, rows], ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=8)) <= TOL_SMALL
-    for m in (0, 13):
-        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
-        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=8)
+    assert G.rel_err(y16[:, rows], want) <= TOL_SMALL
+    with batch_invariant():
+        for m in (0, 13):
+            y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+            assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+    # the decode GEMV kernel: clusters of 8 as well (its landing buffer: one token)
+    y1 = gpu_gemm(b, N, K, x[13:14], w_dev=w)
+    assert G.rel_err(y1[:, rows], want[13:14]) <= TOL_SMALL
 
 
 def test_batch_invariance_down_shape():
@@ -224,9 +249,47 @@ def test_batch_invariance_down_shape():
     y16 = gpu_gemm(b, N, K, x, w_dev=w)
     y4 = gpu_gemm(b, N, K, x[:4], w_dev=w)
     assert np.array_equal(y4.view(np.uint32), y16[:4].view(np.uint32))
-    for m in (0, 7, 15):
-        y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
-        assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+    with batch_invariant():
+        for m in (0, 7, 15):
+            y1 = gpu_gemm(b, N, K, x[m:m + 1], w_dev=w)
+            assert np.array_equal(y1[0].view(np.uint32), y16[m].view(np.uint32)), m
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (3, 512), (200, 1280), (33, 2304), (1000, 3328), (5120, 17408),
+                                 (600, 16384), (17408, 5120)])
+def test_decode_gemv_kernel(ref, N, K):
+    # the one-token kernel on ragged row tiles, K of 1..68 blocks (warps with no
+    # block, uneven warps, cluster K splits of 2..8): against the oracle, run to
+    # run, and against the small-M kernel (batch-invariant mode) within the bar
+    b = G.weights(2, 11, N, K, outliers=True)
+    x = G.activations(2, 12, 1, K)
+    w = G.dev(b)
+    y = gpu_gemm(b, N, K, x, w_dev=w)
+    y2 = gpu_gemm(b, N, K, x, w_dev=w)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32)), "not run-to-run deterministic"
+    rows = np.unique(np.concatenate([G.sample_rows(N, min(N, 128), seed=4), np.arange(max(0, N - 40), N)]))
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x, threads=8)
+    assert G.rel_err(y[:, rows], want) <= TOL_SMALL
+    with batch_invariant():
+        yi = gpu_gemm(b, N, K, x, w_dev=w)
+    assert G.rel_err(y, yi.astype(np.float64)) <= TOL_SMALL
+
+
+def test_decode_gemv_activation_scale_exact():
+    # the kernel scales the activations by a power of two inside its operands; so
+    # does this test: 2^k x gives exactly 2^k y wherever no intermediate leaves the
+    # normal range (|x| from 2^-56 to 2^63)
+    N, K = 5120, 17408
+    b = G.weights(2, 13, N, K)
+    w = G.dev(b)
+    x = G.activations(2, 14, 1, K)
+    y = gpu_gemm(b, N, K, x, w_dev=w)
+    for k in (-20, -7, 9, 40):
+        xs = (x.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** k)
+        xk = (xs.view(np.uint32) >> 16).astype(np.uint16)
+        assert np.array_equal(((xk.astype(np.uint32) << 16).view(np.float32)), xs)  # exact in bf16
+        yk = gpu_gemm(b, N, K, xk, w_dev=w)
+        assert np.array_equal(yk.view(np.uint32), (y * np.float32(2.0 ** k)).view(np.uint32)), k
 
 
 @pytest.mark.parametrize("shape", [G.DECODE_UP, G.DECODE_DOWN], ids=["gate_up", "down"])
