@@ -405,8 +405,8 @@ def test_prefill_many_tiles_ragged(ref):
     assert G.rel_err(y[:, rows], want) <= TOL_TC
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (128, 5120, 17408), (1024, 5120, 17408),
-                                   (4096, 17408, 5120), (4096, 5120, 17408)])
+@pytest.mark.parametrize("M,N,K", [(128, 17408, 5120), (128, 5120, 17408), (1024, 17408, 5120),
+                                   (1024, 5120, 17408), (4096, 17408, 5120), (4096, 5120, 17408)])
 def test_prefill_full_size(ref, M, N, K):
     # (4096, 5120, 17408) runs as the benchmark's two launches: 15 token tiles, then
     # the last one with the cluster K split
