@@ -318,7 +318,7 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
     cudaError_t e;
     if (M == 1 && !invariant) e = launch_gemv(di, w, N, K, x, y, early, s);
     else if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, early, s);
-    else e = launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, s);
+    else e = launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, invariant, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 
@@ -371,7 +371,9 @@ q4k_status q4k_nvfp4_gemm(const void *w, float g, int64_t N, int64_t K, const ui
     cudaError_t e = M <= 16 ? launch_smallm_fp4(di, w, g, N, K, x, M, ldx, y, ldy,
                                                 g_static_weights.load(std::memory_order_relaxed) != 0,
                                                 static_cast<cudaStream_t>(stream))
-                            : launch_gemm_tc_nvfp4(di, w, g, N, K, x, M, ldx, y, ldy, static_cast<cudaStream_t>(stream));
+                            : launch_gemm_tc_nvfp4(di, w, g, N, K, x, M, ldx, y, ldy,
+                                                   g_batch_invariant.load(std::memory_order_relaxed) != 0,
+                                                   static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 

@@ -356,9 +356,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (late_wait) pdl_wait();
 }
 
+// The cluster K split of an N x K problem with `tiles` output tiles: when the
+// tiles leave more than half of the SMs idle (one CTA per SM), split K over up to
+// 8 CTAs, at least four K blocks each.
+int k_split(const DeviceInfo &di, int64_t tiles, int KB) {
+    int S = 1;
+    if (2 * tiles <= di.sm_count) {
+        int64_t want = di.sm_count / tiles;
+        if (want > 8) want = 8;
+        if (want > KB / 4) want = KB / 4;
+        if (want > 1) S = (int)want;
+    }
+    return S;
+}
+
+// S: the cluster K split (1: none).
 template <int BN, bool FP4>
 cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int late_wait = 0) {
+                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int S, int late_wait = 0) {
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
     if (e != cudaSuccess) return e;
@@ -369,16 +384,6 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     e = ensure_smem((const void *)gemm_tc_kernel<BN, FP4>, smem);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
-    const int64_t tiles = ((N + kTileRows - 1) / kTileRows) * ((M + BN - 1) / BN);
-    // Split K over a cluster when the output tiles leave more than half of the
-    // SMs idle (one CTA per SM); at least four K blocks per split.
-    int S = 1;
-    if (2 * tiles <= di.sm_count) {
-        int64_t want = di.sm_count / tiles;
-        if (want > 8) want = 8;
-        if (want > KB / 4) want = KB / 4;
-        if (want > 1) S = (int)want;
-    }
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
     return launch_pdl(gemm_tc_kernel<BN, FP4>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
                       tmX, y, ldy, (int)M, (int)N, KB, g, late_wait, di.status);
@@ -397,30 +402,44 @@ int64_t main_part(const DeviceInfo &di, int64_t N, int64_t M) {
     return (tm - r) * 256;
 }
 
+// Default: the K split follows the tile count (so it depends on M), and a mostly
+// empty last wave becomes a second, K-split launch.  Batch-invariant: the K split
+// is the one the weight rows alone would get (one token tile), for every M, and
+// nothing is split off; each output element is then summed over the same K
+// ranges in the same order whatever M is.
 template <bool FP4>
 cudaError_t launch_split(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                         int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s) {
-    if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s);
+                         int64_t ldx, float *y, int64_t ldy, float g, bool invariant, cudaStream_t s) {
+    const int KB = (int)(K / kQK);
+    const int64_t tn = (N + kTileRows - 1) / kTileRows;
+    if (invariant) {
+        const int S = k_split(di, tn, KB);
+        return M <= 128 ? launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S)
+                        : launch_bn<256, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
+    }
+    if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, k_split(di, tn, KB));
     const int64_t m1 = main_part(di, N, M);
-    cudaError_t e = launch_bn<256, FP4>(di, w, N, K, x, m1, ldx, y, ldy, g, s);
+    cudaError_t e = launch_bn<256, FP4>(di, w, N, K, x, m1, ldx, y, ldy, g, s, k_split(di, tn * ((m1 + 255) / 256), KB));
     if (e != cudaSuccess || m1 == M) return e;
     const int64_t m2 = M - m1;
     const uint16_t *x2 = x + m1 * ldx;
     float *y2 = y + m1 * ldy;
-    return m2 <= 128 ? launch_bn<128, FP4>(di, w, N, K, x2, m2, ldx, y2, ldy, g, s, 1)
-                     : launch_bn<256, FP4>(di, w, N, K, x2, m2, ldx, y2, ldy, g, s, 1);
+    return m2 <= 128 ? launch_bn<128, FP4>(di, w, N, K, x2, m2, ldx, y2, ldy, g, s, k_split(di, tn, KB), 1)
+                     : launch_bn<256, FP4>(di, w, N, K, x2, m2, ldx, y2, ldy, g, s,
+                                           k_split(di, tn * ((m2 + 255) / 256), KB), 1);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                           int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
-    return launch_split<false>(di, w, N, K, x, M, ldx, y, ldy, 1.0f, s);
+                           int64_t ldx, float *y, int64_t ldy, bool invariant, cudaStream_t s) {
+    return launch_split<false>(di, w, N, K, x, M, ldx, y, ldy, 1.0f, invariant, s);
 }
 
 cudaError_t launch_gemm_tc_nvfp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K,
-                                 const uint16_t *x, int64_t M, int64_t ldx, float *y, int64_t ldy, cudaStream_t s) {
-    return launch_split<true>(di, w, N, K, x, M, ldx, y, ldy, g, s);
+                                 const uint16_t *x, int64_t M, int64_t ldx, float *y, int64_t ldy, bool invariant,
+                                 cudaStream_t s) {
+    return launch_split<true>(di, w, N, K, x, M, ldx, y, ldy, g, invariant, s);
 }
 
 }  // namespace q4k

@@ -61,9 +61,10 @@ cudaError_t launch_smallm_fp4(const DeviceInfo &di, const void *w, float g, int6
 cudaError_t launch_quantize_x8(const DeviceInfo &di, const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q,
                                float *sx, cudaStream_t s);
 
-// M > 16: per-tile dequantization into shared memory + tcgen05 MMA (gemm_tc.cu)
+// M > 16: per-tile dequantization into shared memory + tcgen05 MMA (gemm_tc.cu).
+// invariant: the K split depends on (N, K, SM count) only, never on M.
 cudaError_t launch_gemm_tc(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                           int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
+                           int64_t ldx, float *y, int64_t ldy, bool invariant, cudaStream_t s);
 
 // SwiGLU epilogue of a routed expert's up projection: instead of its fp32
 // output u, the kernel stores h = swiglu_bf16(g, u), g being the gate
@@ -80,7 +81,8 @@ struct GluOut {
 // NVFP4 weights through the same tensor-core kernel: the operand is the exact
 // bf16 e2m1 * e4m3 product, y = g * (x . operand^T) (gemm_tc.cu)
 cudaError_t launch_gemm_tc_nvfp4(const DeviceInfo &di, const void *w, float g, int64_t N, int64_t K,
-                                 const uint16_t *x, int64_t M, int64_t ldx, float *y, int64_t ldy, cudaStream_t s);
+                                 const uint16_t *x, int64_t M, int64_t ldx, float *y, int64_t ldy, bool invariant,
+                                 cudaStream_t s);
 
 // MoE expert GEMM on the tensor cores: a persistent kernel (one CTA per SM,
 // double-buffered tensor-memory accumulators) walking the routing's token tiles

@@ -418,6 +418,26 @@ def test_prefill_full_size(ref, M, N, K):
     assert G.rel_err(y[:, rows], want) <= TOL_TC
 
 
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)], ids=["up", "down"])
+def test_prefill_batch_invariant_mode(ref, N, K):
+    # q4k_set_batch_invariant(1) on the tensor-core path (M > 16): the K split is
+    # chosen from the weight shape alone and no last-wave launch is split off, so a
+    # token's output row has the same bits in calls of 17 to 4096 tokens at any
+    # offset in the batch (the down projection's shape runs the cluster K split)
+    b = G.weights(3, 0, N, K, outliers=True)
+    w = G.dev(b)
+    x = G.activations(3, 1, 4096, K)
+    with batch_invariant():
+        yfull = gpu_gemm(b, N, K, x, w_dev=w)
+        for m0, M in ((0, 128), (0, 1000), (1000, 17), (2900, 1000), (4096 - 300, 300), (77, 129)):
+            y = gpu_gemm(b, N, K, x[m0:m0 + M], w_dev=w)
+            assert np.array_equal(y.view(np.uint32), yfull[m0:m0 + M].view(np.uint32)), (m0, M)
+    rows = G.sample_rows(N, 16)
+    toks = G.sample_rows(4096, 24, seed=5)
+    want = ref.gemm(G.rows_of(b, rows), len(rows), K, x[toks], threads=16)
+    assert G.rel_err(yfull[np.ix_(toks, rows)], want) <= TOL_TC
+
+
 # ---------------------------------------------------------------------- MoE
 
 def test_moe_route_bitexact(ref, syn):
@@ -1085,6 +1105,20 @@ def test_static_weights_activations_from_the_previous_kernel(ref, N, K, M, fp4):
             tol = TOL_SMALL
         for i in range(j, 6, 2):
             assert G.rel_err(got[i][:, rows], want) <= tol, (i, j)
+
+
+def test_nvfp4_batch_invariant_mode(ref):
+    # the NVFP4 tensor-core path in batch-invariant mode: rows independent of M
+    N, K = 1000, 4096   # 8 row tiles: the cluster K split runs
+    w, g = fp4_weights(2, N, K)
+    x = G.activations(7, 9, 700, K)
+    with batch_invariant():
+        yfull = gpu_nvfp4_gemm(w, float(g), N, K, x)
+        for m0, M in ((0, 40), (300, 300), (699 - 130, 130)):
+            y = gpu_nvfp4_gemm(w, float(g), N, K, x[m0:m0 + M])
+            assert np.array_equal(y.view(np.uint32), yfull[m0:m0 + M].view(np.uint32)), (m0, M)
+    want = ref.nvfp4_gemm(w, float(g), N, K, x[:32], threads=16)
+    assert G.rel_err(yfull[:32], want) <= TOL_FP4
 
 
 def test_nvfp4_gemm_deterministic():
