@@ -136,6 +136,20 @@ int q4k_set_static_weights(int enable);
  * setting (0 or 1). */
 int q4k_set_batch_invariant(int enable);
 
+/* Failure-detection test hook (no counterpart on the pages).  Every wait inside
+ * the kernels is bounded (2 s); a wait that runs out makes its kernel abandon
+ * its work, wait for its own copies in flight, reach all of its barriers and
+ * set a device status word that q4k_check_device reports as Q4K_ERR_TIMEOUT.
+ * This sets the limit of the decode GEMV's main-loop waits (q4k_gemv, and
+ * q4k_gemm with M = 1 outside batch-invariant mode) to `ns`, so that a test can
+ * make that path run out without faulting or hanging anything; 0 restores the
+ * standard limit.  Under 1000 ns a wait tests its copy once, without blocking,
+ * and gives up at once if it has not landed.  A GEMV whose wait ran out leaves
+ * its output undefined.
+ * Process-wide; applies to calls enqueued after it returns.  Returns the
+ * previous setting (0 = standard). */
+unsigned long long q4k_set_gemv_wait_limit_ns(unsigned long long ns);
+
 /* ----------------------------------------------------------------- dequant --
  * Standalone dequantization of an N x K Q4_K matrix:
  *     out[n][k] = d*sc_s*q - dmin*m_s   (fp32, computed as fp32 multiplies and one

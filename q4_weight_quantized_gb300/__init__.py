@@ -25,7 +25,7 @@ QK = 256
 # every symbol include/q4k.h declares
 EXPORTS = (
     "q4k_status_string", "q4k_last_cuda_error", "q4k_row_bytes", "q4k_version", "q4k_check_device",
-    "q4k_set_static_weights", "q4k_set_batch_invariant", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
+    "q4k_set_static_weights", "q4k_set_batch_invariant", "q4k_set_gemv_wait_limit_ns", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
     "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_reuse_routing",
     "q4k_moe_grouped_gemm_noalloc", "q4k_moe_ffn_workspace_size", "q4k_moe_ffn", "q4k_quantize_x8", "q4k_gemm_x8",
     "q4k_nvfp4_dequant", "q4k_nvfp4_gemm",
@@ -63,6 +63,7 @@ def load(path: str | None = None):
         "q4k_check_device": ([P], st),
         "q4k_set_static_weights": ([ctypes.c_int], ctypes.c_int),
         "q4k_set_batch_invariant": ([ctypes.c_int], ctypes.c_int),
+        "q4k_set_gemv_wait_limit_ns": ([ctypes.c_ulonglong], ctypes.c_ulonglong),
         "q4k_dequant": ([P, i64, i64, P, P], st),
         "q4k_dequant_bf16": ([P, i64, i64, P, P], st),
         "q4k_gemv": ([P, i64, i64, P, P, P], st),
@@ -140,6 +141,12 @@ def q4k_set_static_weights(enable: bool) -> bool:
     kernel enqueued just before a call on the same stream); returns the previous
     setting.  See include/q4k.h."""
     return bool(load().q4k_set_static_weights(1 if enable else 0))
+
+
+def q4k_set_gemv_wait_limit_ns(ns: int) -> int:
+    """Test hook: the limit of the decode GEMV's main-loop waits in nanoseconds (0:
+    the standard 2 s); returns the previous setting.  See include/q4k.h."""
+    return int(load().q4k_set_gemv_wait_limit_ns(int(ns)))
 
 
 def q4k_set_batch_invariant(enable: bool) -> bool:

@@ -20,6 +20,8 @@ __device__ unsigned int g_status_word;  // kernels OR Q4K_DEV_* bits here
 static std::atomic<int> g_static_weights{0};
 // q4k_set_batch_invariant (process-wide, default off)
 static std::atomic<int> g_batch_invariant{0};
+// q4k_set_gemv_wait_limit_ns (process-wide, 0 = the standard limit)
+static std::atomic<unsigned long long> g_gemv_wait_ns{0};
 
 namespace {
 
@@ -252,6 +254,8 @@ int q4k_set_static_weights(int enable) { return g_static_weights.exchange(enable
 
 int q4k_set_batch_invariant(int enable) { return g_batch_invariant.exchange(enable ? 1 : 0); }
 
+unsigned long long q4k_set_gemv_wait_limit_ns(unsigned long long ns) { return g_gemv_wait_ns.exchange(ns); }
+
 q4k_status q4k_check_device(void *stream) {
     DeviceInfo di;
     q4k_status st = check_device(&di);
@@ -316,7 +320,10 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
     const bool early = g_static_weights.load(std::memory_order_relaxed) != 0;
     const bool invariant = g_batch_invariant.load(std::memory_order_relaxed) != 0;
     cudaError_t e;
-    if (M == 1 && !invariant) e = launch_gemv(di, w, N, K, x, y, early, s);
+    if (M == 1 && !invariant) {
+        const unsigned long long lim = g_gemv_wait_ns.load(std::memory_order_relaxed);
+        e = launch_gemv(di, w, N, K, x, y, early, lim ? lim : kWaitLimitNs, s);
+    }
     else if (M <= 16) e = launch_smallm(di, w, N, K, x, M, ldx, y, ldy, early, s);
     else e = launch_gemm_tc(di, w, N, K, x, M, ldx, y, ldy, invariant, s);
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);

@@ -177,7 +177,8 @@ __device__ __forceinline__ void stage_x(const uint4 v, uint8_t *xs, float *sums,
 template <class C, bool PUSH>
 __global__ void __launch_bounds__(C::kThreadsG, C::kCtasPerSm) gemv_kernel(const __grid_constant__ CUtensorMap tmW,
                                                          const uint16_t *__restrict__ x, float *__restrict__ y,
-                                                         int N, int KB, int early_w, unsigned int *status) {
+                                                         int N, int KB, int early_w, unsigned int *status,
+                                                         unsigned long long wait_ns) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int abort_flag;
     using G = C;
@@ -310,7 +311,10 @@ __global__ void __launch_bounds__(C::kThreadsG, C::kCtasPerSm) gemv_kernel(const
         sv[0] = s0.x, sv[1] = s0.y, sv[2] = s0.z, sv[3] = s0.w, sv[4] = s1.x, sv[5] = s1.y, sv[6] = s1.z, sv[7] = s1.w;
     };
     // every lane observes the copy's completion; the decision to go on is warp-uniform
-    auto wait_slot = [&](int sl, uint32_t ph) { return __all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * sl, ph, status)); };
+    // (main-loop waits take wait_ns; the drain after a give-up keeps the full limit)
+    auto wait_slot = [&](int sl, uint32_t ph) {
+        return __all_sync(0xFFFFFFFFu, mbar_wait_limit(bar0 + 8 * sl, ph, status, wait_ns));
+    };
 
     bool aborted = false;
     int it = 0, slot = 0;
@@ -483,19 +487,19 @@ cudaError_t gemv_split(const DeviceInfo &di, int64_t N, int KB, int *out) {
 
 template <class C, bool PUSH>
 cudaError_t gemv_launch(const DeviceInfo &di, const CUtensorMap &tmW, const uint16_t *x, float *y, int N, int KB,
-                        int S, bool early_weights, cudaStream_t s) {
+                        int S, bool early_weights, unsigned long long wait_ns, cudaStream_t s) {
     const int smem = C::kSmem;
     auto kern = gemv_kernel<C, PUSH>;
     cudaError_t e = ensure_smem((const void *)kern, smem);
     if (e != cudaSuccess) return e;
     const int tiles = (N + C::kRowsG - 1) / C::kRowsG;
     return launch_pdl(kern, dim3(S, tiles, 1), dim3(C::kThreadsG), (size_t)smem, s, dim3(S), tmW, x, y, N, KB,
-                      early_weights ? 1 : 0, di.status);
+                      early_weights ? 1 : 0, di.status, wait_ns);
 }
 
 template <class C>
 cudaError_t launch_cfg(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, float *y,
-                       bool early_weights, cudaStream_t s) {
+                       bool early_weights, unsigned long long wait_ns, cudaStream_t s) {
     const int KB = (int)(K / kQK);
     int S = 1;
     cudaError_t e = gemv_split<C>(di, N, KB, &S);
@@ -504,8 +508,8 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *w, int64_t N, int64_t K
     e = make_weight_tmap(&tmW, w, N, K, C::kRowsW, kBlkWordsG);
     if (e != cudaSuccess) return e;
     const int n = (int)N;
-    return S > 1 ? gemv_launch<C, true>(di, tmW, x, y, n, KB, S, early_weights, s)
-                 : gemv_launch<C, false>(di, tmW, x, y, n, KB, 1, early_weights, s);
+    return S > 1 ? gemv_launch<C, true>(di, tmW, x, y, n, KB, S, early_weights, wait_ns, s)
+                 : gemv_launch<C, false>(di, tmW, x, y, n, KB, 1, early_weights, wait_ns, s);
 }
 
 }  // namespace
@@ -513,10 +517,10 @@ cudaError_t launch_cfg(const DeviceInfo &di, const void *w, int64_t N, int64_t K
 // The wide shape when the 64-row tiles alone give every SM a CTA, else the
 // K-split shape.  Depends on (N, SM count) only.
 cudaError_t launch_gemv(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, float *y,
-                        bool early_weights, cudaStream_t s) {
+                        bool early_weights, unsigned long long wait_ns, cudaStream_t s) {
     const int64_t tiles = (N + CfgWide::kRowsG - 1) / CfgWide::kRowsG;
-    return tiles >= di.sm_count ? launch_cfg<CfgWide>(di, w, N, K, x, y, early_weights, s)
-                                : launch_cfg<CfgSplit>(di, w, N, K, x, y, early_weights, s);
+    return tiles >= di.sm_count ? launch_cfg<CfgWide>(di, w, N, K, x, y, early_weights, wait_ns, s)
+                                : launch_cfg<CfgSplit>(di, w, N, K, x, y, early_weights, wait_ns, s);
 }
 
 }  // namespace q4k

@@ -44,8 +44,9 @@ cudaError_t launch_smallm(const DeviceInfo &di, const void *w, int64_t N, int64_
 // M = 1: the decode GEMV kernel (gemv.cu): sub-blocks in the MMA columns, codes as
 // bare bf16 bit patterns, activations staged once per warp.  Deterministic; its
 // rounding differs from launch_smallm's at M = 1.
+// wait_ns: the limit of the main-loop waits (kWaitLimitNs unless a test shortens it)
 cudaError_t launch_gemv(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, float *y,
-                        bool early_weights, cudaStream_t s);
+                        bool early_weights, unsigned long long wait_ns, cudaStream_t s);
 
 // M in [1, 16] with int8 activations: q [M][K] int8 and sx [M][K/32] fp32 scales,
 // both dense and 16-byte aligned (smallm.cu, int8 mode).

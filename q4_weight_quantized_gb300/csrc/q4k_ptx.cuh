@@ -82,18 +82,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, sets the timeout bit in *status and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *status) {
+// limit_ns, sets the timeout bit in *status and returns false.  A limit under
+// 1 us (a test of the give-up path) tests the phase once, without blocking, and
+// gives up at once if it has not completed; limits under 100 us are checked on
+// every retry.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, unsigned int *status,
+                                                unsigned long long limit_ns) {
+    if (limit_ns < 1000ull) {
+        if (mbar_test_wait(bar, parity)) return true;
+        atomicOr(status, kDevTimeout);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint32_t every = limit_ns < 100000ull ? 0u : 63u;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((i & every) == 0 && global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, kDevTimeout);
             return false;
         }
     }
+}
+
+// mbar_wait_limit with the standard limit, kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *status) {
+    return mbar_wait_limit(bar, parity, status, kWaitLimitNs);
 }
 
 // Whether the routing header hdr = {tile count, E, items, stamp} in the workspace
