@@ -355,7 +355,7 @@ class DeviceRunner:
         if tag in wl.fp4:
             q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N, stream=self.sh)
         elif wl.x8:
-            q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N, stream=self.sh)
+            q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N, None, 0, stream=self.sh)
         elif M == 1:
             q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i], stream=self.sh)
         else:
@@ -426,7 +426,8 @@ class DeviceRunner:
                 q4k.q4k_nvfp4_gemm(self.sets[r][i], wl.fp4[tag], N, K, self.x[i], M, K, self.y[i], N, stream=self.sh)
             elif wl.x8:
                 q4k.q4k_quantize_x8(self.x[i], M, K, K, self.q[i], self.sx[i], stream=self.sh)
-                q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N, stream=self.sh)
+                q4k.q4k_gemm_x8(self.sets[r][i], N, K, self.q[i], self.sx[i], M, self.y[i], N, None, 0,
+                                stream=self.sh)
             elif M == 1:
                 q4k.q4k_gemv(self.sets[r][i], N, K, self.x[i], self.y[i], stream=self.sh)
             else:

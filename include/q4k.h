@@ -216,15 +216,26 @@ q4k_status q4k_gemm(const void *w, int64_t N, int64_t K, const uint16_t *x, int6
  * ldx < K), ALIGN, DEVICE, CUDA. */
 q4k_status q4k_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q, float *s, void *stream);
 
-/* q4k_gemm_x8: y = xh . W^T for M in [1, 16] tokens, where xh[m][k] =
- * s[m][k/32] * q[m][k] are the int8 activations (layouts as q4k_quantize_x8).
- * The integer dot products of each 32-weight sub-block are exact; the scaling
- * and accumulation are fp32.  y: fp32 [M][ldy], ldy >= N, 4-byte aligned.
- * Batch-invariant like q4k_gemm: row m of the result does not depend on M.
- * Errors: NULL, SHAPE (M outside [1, 16], N < 1, bad K, ldy < N), ALIGN,
- * DEVICE, CUDA. */
+/* q4k_gemm_x8: y = xh . W^T, where xh[m][k] = s[m][k/32] * q[m][k] are the
+ * int8 activations (layouts as q4k_quantize_x8).
+ *   M <= 16: the integer dot products of each 32-weight sub-block are exact; the
+ *            scaling and accumulation are fp32.  Row m of the result does not
+ *            depend on M.  No workspace.
+ *   M >  16 (prefill, where the pages requantize the next layer's input): the
+ *            activation scale changes every 32 elements of K, which an MMA
+ *            accumulating over K cannot apply, so a pre-pass writes
+ *            bf16(s * q) (the fp32 product rounded to nearest-even bf16) into
+ *            the workspace and the tcgen05 prefill GEMM multiplies it like bf16
+ *            activations (within the tensor-core bar, 1e-2).
+ *   y   fp32 [M][ldy], ldy >= N; 4-byte aligned for M <= 16, 16-byte aligned with
+ *       ldy % 4 == 0 for M > 16
+ *   ws  device scratch of at least q4k_gemm_x8_workspace_size(M, K) bytes (M*K*2
+ *       for M > 16, else 0), 256-byte aligned; garbage afterwards
+ * Errors: NULL, SHAPE (M < 1, N < 1, bad K, ldy < N), ALIGN, WORKSPACE, DEVICE,
+ * CUDA. */
+size_t q4k_gemm_x8_workspace_size(int64_t M, int64_t K);
 q4k_status q4k_gemm_x8(const void *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, float *y,
-                       int64_t ldy, void *stream);
+                       int64_t ldy, void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------- NVFP4 weights --
  * The pages serve NVFP4 checkpoints as well as GGUF Q4_K (sparkinfer-server

@@ -27,7 +27,7 @@ EXPORTS = (
     "q4k_status_string", "q4k_last_cuda_error", "q4k_row_bytes", "q4k_version", "q4k_check_device",
     "q4k_set_static_weights", "q4k_set_batch_invariant", "q4k_set_gemv_wait_limit_ns", "q4k_dequant", "q4k_dequant_bf16", "q4k_gemv", "q4k_gemm_workspace_size", "q4k_gemm",
     "q4k_moe_route", "q4k_moe_workspace_size", "q4k_moe_grouped_gemm", "q4k_moe_grouped_gemm_reuse_routing",
-    "q4k_moe_grouped_gemm_noalloc", "q4k_moe_ffn_workspace_size", "q4k_moe_ffn", "q4k_quantize_x8", "q4k_gemm_x8",
+    "q4k_moe_grouped_gemm_noalloc", "q4k_moe_ffn_workspace_size", "q4k_moe_ffn", "q4k_quantize_x8", "q4k_gemm_x8_workspace_size", "q4k_gemm_x8",
     "q4k_nvfp4_dequant", "q4k_nvfp4_gemm",
 )
 
@@ -77,7 +77,8 @@ def load(path: str | None = None):
         "q4k_moe_ffn_workspace_size": ([i32, i64, i64, i64, i32], sz),
         "q4k_moe_ffn": ([P, P, P, i32, i64, i64, P, P, P, i64, i32, P, P, sz, P], st),
         "q4k_quantize_x8": ([P, i64, i64, i64, P, P, P], st),
-        "q4k_gemm_x8": ([P, i64, i64, P, P, i64, P, i64, P], st),
+        "q4k_gemm_x8_workspace_size": ([i64, i64], sz),
+        "q4k_gemm_x8": ([P, i64, i64, P, P, i64, P, i64, P, sz, P], st),
         "q4k_nvfp4_dequant": ([P, ctypes.c_float, i64, i64, P, P], st),
         "q4k_nvfp4_gemm": ([P, ctypes.c_float, i64, i64, P, i64, i64, P, i64, P], st),
     }
@@ -232,9 +233,15 @@ def q4k_quantize_x8(x, M: int, K: int, ldx: int, q, s, stream=None) -> None:
     _check(load().q4k_quantize_x8(_ptr(x), M, K, ldx, _ptr(q), _ptr(s), _stream(stream)), "q4k_quantize_x8")
 
 
-def q4k_gemm_x8(w, N: int, K: int, q, s, M: int, y, ldy: int, stream=None) -> None:
-    """y = (s * q) . W^T over int8 activations, M in [1, 16]."""
-    _check(load().q4k_gemm_x8(_ptr(w), N, K, _ptr(q), _ptr(s), M, _ptr(y), ldy, _stream(stream)), "q4k_gemm_x8")
+def q4k_gemm_x8_workspace_size(M: int, K: int) -> int:
+    return load().q4k_gemm_x8_workspace_size(M, K)
+
+
+def q4k_gemm_x8(w, N: int, K: int, q, s, M: int, y, ldy: int, ws=None, ws_bytes: int = 0, stream=None) -> None:
+    """y = (s * q) . W^T over int8 activations (M > 16 needs a workspace of
+    q4k_gemm_x8_workspace_size(M, K) bytes)."""
+    _check(load().q4k_gemm_x8(_ptr(w), N, K, _ptr(q), _ptr(s), M, _ptr(y), ldy, _ptr(ws), ws_bytes,
+                              _stream(stream)), "q4k_gemm_x8")
 
 
 def q4k_nvfp4_dequant(w, g: float, N: int, K: int, out, stream=None) -> None:

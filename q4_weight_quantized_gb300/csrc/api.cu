@@ -340,17 +340,36 @@ q4k_status q4k_quantize_x8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 
+size_t q4k_gemm_x8_workspace_size(int64_t M, int64_t K) {
+    if (M <= 16 || M < 1 || !k_ok(K)) return 0;
+    return (size_t)M * (size_t)K * 2;  // the bf16 operand xh [M][K]
+}
+
 q4k_status q4k_gemm_x8(const void *w, int64_t N, int64_t K, const int8_t *q, const float *s, int64_t M, float *y,
-                       int64_t ldy, void *stream) {
+                       int64_t ldy, void *ws, size_t ws_bytes, void *stream) {
     if (!w || !q || !s || !y) return Q4K_ERR_NULL;
-    if (M < 1 || M > 16 || N < 1 || !k_ok(K) || ldy < N || N > ((int64_t)1 << 31) - 1) return Q4K_ERR_SHAPE;
+    if (M < 1 || N < 1 || !k_ok(K) || ldy < N || N > ((int64_t)1 << 31) - 1 || M > ((int64_t)1 << 31) - 1)
+        return Q4K_ERR_SHAPE;
     if (!aligned(w, 16) || !aligned(q, 16) || !aligned(s, 16) || !aligned(y, 4)) return Q4K_ERR_ALIGN;
+    if (M > 16 && (!aligned(y, 16) || (ldy % 4) != 0)) return Q4K_ERR_ALIGN;
+    const size_t need = q4k_gemm_x8_workspace_size(M, K);
+    if (need > 0 && (!ws || ws_bytes < need)) return Q4K_ERR_WORKSPACE;
+    if (need > 0 && !aligned(ws, 256)) return Q4K_ERR_ALIGN;
     DeviceInfo di;
     q4k_status st = check_device(&di);
     if (st != Q4K_OK) return st;
-    cudaError_t e = launch_smallm_x8(di, w, N, K, q, s, M, y, ldy,
-                                     g_static_weights.load(std::memory_order_relaxed) != 0,
-                                     static_cast<cudaStream_t>(stream));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (M <= 16) {
+        e = launch_smallm_x8(di, w, N, K, q, s, M, y, ldy, g_static_weights.load(std::memory_order_relaxed) != 0, cs);
+    } else {
+        // prefill: s * q rounded to bf16 in the workspace, then the tensor-core GEMM
+        uint16_t *xh = static_cast<uint16_t *>(ws);
+        e = launch_expand_x8(di, q, s, M, K, xh, cs);
+        if (e == cudaSuccess)
+            e = launch_gemm_tc(di, w, N, K, xh, M, K, y, ldy,
+                               g_batch_invariant.load(std::memory_order_relaxed) != 0, cs);
+    }
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 

@@ -61,6 +61,9 @@ cudaError_t launch_smallm_fp4(const DeviceInfo &di, const void *w, float g, int6
 // Per-32 int8 quantization of bf16 rows (x8.cu).
 cudaError_t launch_quantize_x8(const DeviceInfo &di, const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int8_t *q,
                                float *sx, cudaStream_t s);
+// xh[M][K] bf16 = bf16(s * q), the tensor-core operand of int8 activations (x8.cu)
+cudaError_t launch_expand_x8(const DeviceInfo &di, const int8_t *q, const float *sx, int64_t M, int64_t K,
+                             uint16_t *xh, cudaStream_t s);
 
 // M > 16: per-tile dequantization into shared memory + tcgen05 MMA (gemm_tc.cu).
 // invariant: the K split depends on (N, K, SM count) only, never on M.

@@ -913,7 +913,9 @@ def gpu_gemm_x8(blocks, N, K, q, sc, w_dev=None, ldy=None):
     ldy = ldy or N
     y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
     w = w_dev if w_dev is not None else G.dev(blocks)
-    q4k.q4k_gemm_x8(w, N, K, G.dev(np.ascontiguousarray(q)), G.dev(np.ascontiguousarray(sc)), M, y, ldy)
+    wsb = q4k.q4k_gemm_x8_workspace_size(M, K)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda") if wsb else None
+    q4k.q4k_gemm_x8(w, N, K, G.dev(np.ascontiguousarray(q)), G.dev(np.ascontiguousarray(sc)), M, y, ldy, ws, wsb)
     torch.cuda.synchronize()
     out = G.host(y)
     if ldy > N:
@@ -971,6 +973,31 @@ def test_gemm_x8_full_size(ref, shape, M):
     rows = G.sample_rows(N, 64, seed=M)
     want = ref.gemm_x8(G.rows_of(w, rows), len(rows), K, q, sc)
     assert G.rel_err(y[:, rows], want) <= TOL_X8
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 200, 1024), (129, 300, 768), (300, 1000, 4096)])
+def test_gemm_x8_prefill(ref, M, N, K):
+    # M > 16: bf16(s * q) in the workspace, then the tensor-core GEMM (ragged
+    # token tiles, the cluster K split at N = 300 and 1000)
+    w = G.weights(6, 7, N, K, outliers=True)
+    x = G.activations(6, 8, M, K)
+    q, sc = ref.quantize_x8(x)
+    y = gpu_gemm_x8(w, N, K, q, sc, ldy=N + 4 if N % 4 == 0 else N + 4 - N % 4)
+    assert G.rel_err(y, ref.gemm_x8(w, N, K, q, sc)) <= TOL_TC
+
+
+@pytest.mark.parametrize("M", [128, 4096])
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
+def test_gemm_x8_prefill_full_size(ref, N, K, M):
+    # the prefill shapes at 128 and 4096 tokens, sampled output rows and tokens
+    w = G.weights(3, 0, N, K, outliers=True)
+    x = G.activations(6, 9, M, K)
+    q, sc = ref.quantize_x8(x)
+    y = gpu_gemm_x8(w, N, K, q, sc)
+    rows = G.sample_rows(N, 24, seed=6)
+    toks = G.sample_rows(M, 32, seed=7)
+    want = ref.gemm_x8(G.rows_of(w, rows), len(rows), K, q[toks], sc[toks])
+    assert G.rel_err(y[np.ix_(toks, rows)], want) <= TOL_TC
 
 
 def test_gemm_x8_batch_invariant_and_close_to_bf16(ref):

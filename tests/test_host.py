@@ -117,10 +117,13 @@ A16 = 1 << 20  # a 16-byte aligned fake address; never dereferenced by these cal
     (lambda L: L.q4k_quantize_x8(A16, 2, 300, 300, A16, A16, None), q4k.Q4K_ERR_SHAPE),
     (lambda L: L.q4k_quantize_x8(A16, 2, 256, 128, A16, A16, None), q4k.Q4K_ERR_SHAPE),
     (lambda L: L.q4k_quantize_x8(A16, 2, 256, 256, A16 + 8, A16, None), q4k.Q4K_ERR_ALIGN),
-    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, None, 1, A16, 4, None), q4k.Q4K_ERR_NULL),
-    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 17, A16, 4, None), q4k.Q4K_ERR_SHAPE),
-    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 0, A16, 4, None), q4k.Q4K_ERR_SHAPE),
-    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16 + 4, 1, A16, 4, None), q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, None, 1, A16, 4, None, 0, None), q4k.Q4K_ERR_NULL),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 17, A16, 4, None, 0, None), q4k.Q4K_ERR_WORKSPACE),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 17, A16, 4, A16, 17 * 256 * 2 - 1, None), q4k.Q4K_ERR_WORKSPACE),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 17, A16, 4, A16 + 16, 1 << 20, None), q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 17, A16 + 4, 4, A16, 1 << 20, None), q4k.Q4K_ERR_ALIGN),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16, 0, A16, 4, None, 0, None), q4k.Q4K_ERR_SHAPE),
+    (lambda L: L.q4k_gemm_x8(A16, 4, 256, A16, A16 + 4, 1, A16, 4, None, 0, None), q4k.Q4K_ERR_ALIGN),
     (lambda L: L.q4k_nvfp4_dequant(None, 1.0, 4, 256, A16, None), q4k.Q4K_ERR_NULL),
     (lambda L: L.q4k_nvfp4_dequant(A16, 1.0, 4, 200, A16, None), q4k.Q4K_ERR_SHAPE),
     (lambda L: L.q4k_nvfp4_dequant(A16 + 4, 1.0, 4, 256, A16, None), q4k.Q4K_ERR_ALIGN),
