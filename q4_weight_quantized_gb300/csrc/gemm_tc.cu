@@ -13,9 +13,11 @@
 //     128-byte swizzle that the tensor core's K-major layout expects.
 //   * Warps 2-5 (dequant): thread t owns weight row t.  For each 64-wide stage
 //     (one Q4_K group: sub-blocks 2g and 2g+1) it turns 32 code bytes into 64
-//     bf16 weights, w = bf16(d*sc) * q - bf16(dmin*m) (one bf16 FMA per pair
-//     after an exact 128+q -> q subtraction), and stores them in the swizzled
-//     K-major layout; a proxy fence publishes them to the tensor core.
+//     bf16 weights, each the round-to-nearest-even bf16 of the fp32 weight
+//     fl32(q * d sc - dmin m) (packed fp32 FMAs, q * d sc exact inside them),
+//     i.e. the very value the standalone bf16 dequantization writes, and stores
+//     them in the swizzled K-major layout; a proxy fence publishes them to the
+//     tensor core.
 //   * Warp 1 (MMA): one elected thread issues four 128 x BN x 16 tcgen05.mma per
 //     stage into an fp32 accumulator in tensor memory and commits each stage's
 //     completion to the barrier that frees the stage.
@@ -68,16 +70,6 @@ struct Cfg {
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<__nv_bfloat162 *>(&u); }
 __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
 
-// 128+q pairs (natural element order) of one 32-bit word of codes
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t &lo23, uint32_t &hi01,
-                                            uint32_t &hi23) {
-    const uint32_t t01 = prmt(w, 0u, 0x4140u);
-    const uint32_t t23 = prmt(w, 0u, 0x4342u);
-    lo01 = lop3_and_or(t01, 0x000F000Fu, 0x43004300u);
-    lo23 = lop3_and_or(t23, 0x000F000Fu, 0x43004300u);
-    hi01 = lop3_and_or(t01 >> 4, 0x000F000Fu, 0x43004300u);
-    hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
-}
 
 // FP4: the weights are NVFP4 blocks (16 e4m3 scales, then 128 bytes of e2m1
 // pairs) instead of Q4_K; each operand element is the exact e2m1 * e4m3 product
@@ -209,7 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else {
         // ---------------------------------------------------- dequant warps
         const int t = threadIdx.x - 64;  // weight row within the tile
-        const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
         bool ok = true;
         for (int kb = 0; kb < KBs && ok; ++kb) {
             const int r = kb & 1;
@@ -271,8 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const int b0 = (2 * g) & 3, b1 = (2 * g + 1) & 3;
                 const float dsc0 = d * (float)((scw >> (8 * b0)) & 0xFFu), dm0 = dmin * (float)((mw >> (8 * b0)) & 0xFFu);
                 const float dsc1 = d * (float)((scw >> (8 * b1)) & 0xFFu), dm1 = dmin * (float)((mw >> (8 * b1)) & 0xFFu);
-                const __nv_bfloat162 s0 = __floats2bfloat162_rn(dsc0, dsc0), n0v = __floats2bfloat162_rn(-dm0, -dm0);
-                const __nv_bfloat162 s1 = __floats2bfloat162_rn(dsc1, dsc1), n1v = __floats2bfloat162_rn(-dm1, -dm1);
+                const GroupScales gs = group_scales(dsc0, dm0, dsc1, dm1);
                 const uint4 qa = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g);
                 const uint4 qb = *reinterpret_cast<const uint4 *>(rowp + 32 + 32 * g);
                 const uint32_t wds[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
@@ -280,13 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {  // chunk j: elements 8j..8j+7 of each sub-block
                     uint32_t lo[4], hi[4];
-                    unpack_word(wds[2 * j], lo[0], lo[1], hi[0], hi[1]);
-                    unpack_word(wds[2 * j + 1], lo[2], lo[3], hi[2], hi[3]);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        lo[q] = as_u32(__hfma2(__hsub2(as_bf2(lo[q]), k128), s0, n0v));
-                        hi[q] = as_u32(__hfma2(__hsub2(as_bf2(hi[q]), k128), s1, n1v));
-                    }
+q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
+                    q4k_word_to_bf16(wds[2 * j + 1], gs, lo[2], lo[3], hi[2], hi[3]);
                     *reinterpret_cast<uint4 *>(arow + ((j ^ (t & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     *reinterpret_cast<uint4 *>(arow + (((j + 4) ^ (t & 7)) << 4)) =
                         make_uint4(hi[0], hi[1], hi[2], hi[3]);

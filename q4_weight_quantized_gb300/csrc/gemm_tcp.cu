@@ -67,21 +67,6 @@ struct Params {
     GluOut glu;            // SwiGLU epilogue (up projection of an expert FFN)
 };
 
-__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) { return *reinterpret_cast<__nv_bfloat162 *>(&u); }
-__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
-
-// 128+q pairs (natural element order) of one 32-bit word of codes: low nibbles
-// of bytes (0,1), (2,3) and high nibbles of the same bytes
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo01, uint32_t &lo23, uint32_t &hi01,
-                                            uint32_t &hi23) {
-    const uint32_t t01 = prmt(w, 0u, 0x4140u);
-    const uint32_t t23 = prmt(w, 0u, 0x4342u);
-    lo01 = lop3_and_or(t01, 0x000F000Fu, 0x43004300u);
-    lo23 = lop3_and_or(t23, 0x000F000Fu, 0x43004300u);
-    hi01 = lop3_and_or(t01 >> 4, 0x000F000Fu, 0x43004300u);
-    hi23 = lop3_and_or(t23 >> 4, 0x000F000Fu, 0x43004300u);
-}
-
 __device__ __forceinline__ Tile tile_of(const Params &p, int k) {
     const int tile = blockIdx.x + k * gridDim.x;
     const int nt = tile % p.tiles_n, mt = tile / p.tiles_n;
@@ -246,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
         const int t = threadIdx.x - 64;
         const int row = t & (kTileRows - 1);  // weight row within the tile
         const int h = t >> 7;                 // which 16 code bytes of each group: elements 16h..16h+15
-        const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
         bool ok = true;
         for (int b = 0; b < nblocks && ok; ++b) {
             const int r = b & 1;
@@ -273,21 +257,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 const int b0 = (2 * g) & 3, b1 = (2 * g + 1) & 3;
                 const float dsc0 = d * (float)((scw >> (8 * b0)) & 0xFFu), dm0 = dmin * (float)((mw >> (8 * b0)) & 0xFFu);
                 const float dsc1 = d * (float)((scw >> (8 * b1)) & 0xFFu), dm1 = dmin * (float)((mw >> (8 * b1)) & 0xFFu);
-                const __nv_bfloat162 s0 = __floats2bfloat162_rn(dsc0, dsc0), n0v = __floats2bfloat162_rn(-dm0, -dm0);
-                const __nv_bfloat162 s1 = __floats2bfloat162_rn(dsc1, dsc1), n1v = __floats2bfloat162_rn(-dm1, -dm1);
+                const GroupScales gs = group_scales(dsc0, dm0, dsc1, dm1);
                 const uint4 qw = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g + 16 * h);
                 const uint32_t wds[4] = {qw.x, qw.y, qw.z, qw.w};
                 uint8_t *arow = as + s * kAB + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {  // chunk 2h+j: elements 16h+8j .. +7 of each sub-block
                     uint32_t lo[4], hi[4];
-                    unpack_word(wds[2 * j], lo[0], lo[1], hi[0], hi[1]);
-                    unpack_word(wds[2 * j + 1], lo[2], lo[3], hi[2], hi[3]);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        lo[q] = as_u32(__hfma2(__hsub2(as_bf2(lo[q]), k128), s0, n0v));
-                        hi[q] = as_u32(__hfma2(__hsub2(as_bf2(hi[q]), k128), s1, n1v));
-                    }
+                    q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
+                    q4k_word_to_bf16(wds[2 * j + 1], gs, lo[2], lo[3], hi[2], hi[3]);
                     const int cl = 2 * h + j;
                     *reinterpret_cast<uint4 *>(arow + ((cl ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     *reinterpret_cast<uint4 *>(arow + (((cl + 4) ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);

@@ -381,4 +381,59 @@ __device__ __forceinline__ uint32_t elect_one() {
     return pred;
 }
 
+
+// ------------------------------------------- Q4_K -> tensor-core operand
+// packed fp32 pairs: a * b + c and a + b, each element rounded once
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
+// The scales of one 64-weight group of a Q4_K block: sub-block 2g (low nibbles,
+// d sc and -dmin m as fp32 pairs) and 2g+1 (high nibbles).
+struct GroupScales {
+    float2 ds0, dmn0, ds1, dmn1;
+};
+__device__ __forceinline__ GroupScales group_scales(float dsc0, float dm0, float dsc1, float dm1) {
+    return {make_float2(dsc0, dsc0), make_float2(-dm0, -dm0), make_float2(dsc1, dsc1), make_float2(-dm1, -dm1)};
+}
+
+// One 32-bit word of codes (4 bytes = elements e..e+3 of sub-blocks 2g and 2g+1)
+// -> the bf16 operand pairs (e, e+1), (e+2, e+3) of each sub-block, each weight
+// the round-to-nearest-even bf16 of the fp32 dequantized value
+// fl32(q * d sc - dmin m): q * d sc is exact inside the FMA (21 significant
+// bits), so the fp32 value is the one rounding of the exact weight, the same
+// value the standalone dequantization writes.  The nibbles become the floats
+// 2^23 + q by one byte permute each; q = that - 2^23 exactly.
+__device__ __forceinline__ void q4k_word_to_bf16(uint32_t w, const GroupScales &c, uint32_t &lo01, uint32_t &lo23,
+                                                 uint32_t &hi01, uint32_t &hi23) {
+    const uint32_t lw = w & 0x0F0F0F0Fu, hw = (w >> 4) & 0x0F0F0F0Fu;
+    const float2 k23n = make_float2(-8388608.0f, -8388608.0f);
+    uint32_t out[4];
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+        const float l0 = __uint_as_float(prmt(lw, 0x4B000000u, 0x7650u + 2 * pr));
+        const float l1 = __uint_as_float(prmt(lw, 0x4B000000u, 0x7651u + 2 * pr));
+        const float h0 = __uint_as_float(prmt(hw, 0x4B000000u, 0x7650u + 2 * pr));
+        const float h1 = __uint_as_float(prmt(hw, 0x4B000000u, 0x7651u + 2 * pr));
+        const float2 wl = fma2(add2(make_float2(l0, l1), k23n), c.ds0, c.dmn0);
+        const float2 wh = fma2(add2(make_float2(h0, h1), k23n), c.ds1, c.dmn1);
+        const __nv_bfloat162 bl = __floats2bfloat162_rn(wl.x, wl.y), bh = __floats2bfloat162_rn(wh.x, wh.y);
+        out[pr] = *reinterpret_cast<const uint32_t *>(&bl);
+        out[2 + pr] = *reinterpret_cast<const uint32_t *>(&bh);
+    }
+    lo01 = out[0], lo23 = out[1], hi01 = out[2], hi23 = out[3];
+}
+
 }  // namespace q4k

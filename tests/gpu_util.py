@@ -80,9 +80,9 @@ def _bf16(a: np.ndarray) -> np.ndarray:
 def tc_weights(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
     """Model of the tensor-core kernels' bf16 weight operand, float64 [N, K].
 
-    Those kernels form each weight as one bf16 fused multiply-add of the code q
-    with the sub-block's scale and offset, both first rounded to bf16:
-    w = bf16(q * bf16(d*sc) - bf16(dmin*m)).  The field layout follows the Q4_K
+    Those kernels feed each weight as the round-to-nearest-even bf16 of its fp32
+    dequantized value: w = bf16(fl32(q * d*sc - dmin*m)), where d*sc, dmin*m and
+    q * d*sc are exact in fp32.  The field layout follows the Q4_K
     block (fp16 d and dmin, twelve bytes of 6-bit scale/offset pairs, 128 bytes
     of codes: sub-blocks 2g and 2g+1 are the low and high nibbles of bytes
     32g..32g+31).  Used only to separate that rounding from other errors."""
@@ -98,7 +98,7 @@ def tc_weights(blocks: np.ndarray, N: int, K: int) -> np.ndarray:
     mm[..., 4:] = (s[..., 8:12] >> 4) | ((s[..., 4:8] >> 6) << 4)
     codes = b[..., 16:].astype(np.int32).reshape(N, nb, 4, 32)
     q = np.stack([codes & 15, codes >> 4], axis=3).reshape(N, nb, 8, 32)
-    dsc = _bf16(d[..., None] * sc.astype(np.float32))
-    dm = _bf16(dmin[..., None] * mm.astype(np.float32))
-    w = q * dsc[..., None] - dm[..., None]
+    dsc = (d[..., None] * sc.astype(np.float32)).astype(np.float32)
+    dm = (dmin[..., None] * mm.astype(np.float32)).astype(np.float32)
+    w = q.astype(np.float32) * dsc[..., None] - dm[..., None]   # float32: one rounding
     return _bf16(w.astype(np.float32)).reshape(N, K)
