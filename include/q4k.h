@@ -123,13 +123,15 @@ int q4k_set_static_weights(int enable);
  *   on: M = 1 runs the 2..16-token kernel as well, so row m of any call with
  *       M <= 16 equals the one-token call on row m bit for bit.  Calls with
  *       M > 16 (the tensor-core path of q4k_gemm and q4k_nvfp4_gemm) split K
- *       over a thread-block cluster as the weight shape alone dictates (never
- *       by M) and split off no last-wave launch, so a token's row has the same
- *       bits in every call of 17 tokens or more, wherever it sits in the batch.
+ *       in two or not at all, as the weight shape alone dictates (never by M),
+ *       and split off no last-wave launch, so a token's row has the same bits
+ *       in every call of 17 tokens or more, wherever it sits in the batch.  The
+ *       two K halves are summed over a thread-block cluster when the call's
+ *       tiles leave SMs idle, else in two accumulators of one CTA; both add
+ *       half 0 and half 1 in that order.
  *       Cost: none where the weight rows fill the GPU without a K split (the
  *       K 5120 -> N 17408 prefill shape); on the narrow K 17408 -> N 5120 shape
- *       the K split stays on at every M (+30 % time at 1024 tokens, +51 % at
- *       4096 on one GB300).
+ *       +36 % time at 128 tokens, +30 % at 1024, +10 % at 4096 on one GB300.
  * The boundary between the two paths stays: rows of calls with M <= 16 and
  * M > 16 differ in rounding (different kernels, each within its bar).
  * Process-wide; applies to calls enqueued after it returns.  Returns the previous

@@ -78,7 +78,10 @@ template <int BN, bool FP4 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
                                                               int64_t ldy, int M, int N, int KB, float gscale,
-                                                              int late_wait, unsigned int *status) {
+                                                              int late_wait, int nacc, unsigned int *status) {
+    // nacc = 2 (no cluster split): the first and the second half of K, as a 2-way K
+    // split would divide it, accumulate into two tensor-memory accumulators that the
+    // epilogue adds in that order - the bits of the 2-way split, without a cluster.
     // late_wait: this launch is the remainder of a split problem, queued right after
     // the main launch, which waited for the producers of x and w before letting it
     // start; it waits for the main launch only before it ends, so that a later
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int kbeg = (int)((int64_t)KB * split / S);
     const int KBs = (int)((int64_t)KB * (split + 1) / S) - kbeg;
     const int total = KBs * 4;  // 64-wide stages
+    const int imid = nacc == 2 ? (KB / 2) * 4 : total;  // first stage of the second accumulator
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -129,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), BN);
+        tmem_alloc(smem_u32(tmem_holder), BN * nacc);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -188,9 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 tc_fence_after();
                 const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kABytes));
                 const uint64_t bd = umma_desc_sw128(smem_u32(xs + sx * C::XB));
+                const bool second = i >= imid;
+                const uint32_t dacc = tmem + (second ? (uint32_t)BN : 0u);
+                const int i0 = second ? imid : 0;  // the accumulator's first stage
 #pragma unroll
                 for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
-                    umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
+                    umma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
                 umma_commit(empty0 + 8 * s);
                 umma_commit(xempty0 + 8 * sx);
             }
@@ -297,6 +304,13 @@ q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
                 tmem_ld_wait();
+                if (nacc == 2) {  // + the second half of K, in split-rank order
+                    uint32_t v2[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + BN + 32 * cc, v2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
+                }
                 if (S > 1) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) part[(32 * cc + j) * kTileRows + rl] = __uint_as_float(v[j]);
@@ -336,7 +350,7 @@ q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
         // a bounded wait for the MMAs still running) before the columns are freed
         (void)mbar_wait(accfull, 0, status);
         tc_fence_after();
-        tmem_dealloc(tmem, BN);
+        tmem_dealloc(tmem, BN * nacc);
     }
     if (late_wait) pdl_wait();
 }
@@ -355,10 +369,12 @@ int k_split(const DeviceInfo &di, int64_t tiles, int KB) {
     return S;
 }
 
-// S: the cluster K split (1: none).
+// S: the cluster K split (1: none); nacc = 2: two accumulators in place of a 2-way
+// split (S = 1 then).
 template <int BN, bool FP4>
 cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int S, int late_wait = 0) {
+                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int S, int late_wait = 0,
+                      int nacc = 1) {
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
     if (e != cudaSuccess) return e;
@@ -371,7 +387,7 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     const int KB = (int)(K / kQK);
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
     return launch_pdl(gemm_tc_kernel<BN, FP4>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
-                      tmX, y, ldy, (int)M, (int)N, KB, g, late_wait, di.status);
+                      tmX, y, ldy, (int)M, (int)N, KB, g, late_wait, nacc, di.status);
 }
 
 // One CTA per SM: when the tiles' last wave would run mostly empty and a row of
@@ -398,9 +414,13 @@ cudaError_t launch_split(const DeviceInfo &di, const void *w, int64_t N, int64_t
     const int KB = (int)(K / kQK);
     const int64_t tn = (N + kTileRows - 1) / kTileRows;
     if (invariant) {
-        const int S = k_split(di, tn, KB);
-        return M <= 128 ? launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S)
-                        : launch_bn<256, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
+        // at most 2 ways, so that one CTA can hold both halves' 256-column
+        // accumulators when the tiles alone fill the GPU
+        const int S = k_split(di, tn, KB) > 1 ? 2 : 1;
+        if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
+        if (S == 2 && 2 * tn * ((M + 255) / 256) > di.sm_count)
+            return launch_bn<256, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, 1, 0, 2);
+        return launch_bn<256, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
     }
     if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, k_split(di, tn, KB));
     const int64_t m1 = main_part(di, N, M);

@@ -422,7 +422,9 @@ def test_prefill_batch_invariant_mode(ref, N, K):
     # q4k_set_batch_invariant(1) on the tensor-core path (M > 16): the K split is
     # chosen from the weight shape alone and no last-wave launch is split off, so a
     # token's output row has the same bits in calls of 17 to 4096 tokens at any
-    # offset in the batch (the down projection's shape runs the cluster K split)
+    # offset in the batch.  On the down projection's shape the split is 2-way: over a
+    # cluster for calls whose tiles leave SMs idle (17, 128, 129 tokens), in two
+    # accumulators of one CTA otherwise (300 tokens and up)
     b = G.weights(3, 0, N, K, outliers=True)
     w = G.dev(b)
     x = G.activations(3, 1, 4096, K)
@@ -1135,12 +1137,14 @@ def test_static_weights_activations_from_the_previous_kernel(ref, N, K, M, fp4):
 
 def test_nvfp4_batch_invariant_mode(ref):
     # the NVFP4 tensor-core path in batch-invariant mode: rows independent of M
-    N, K = 1000, 4096   # 8 row tiles: the cluster K split runs
+    # 8 row tiles: calls of up to 9 token tiles split K 2 ways over a cluster, the
+    # 2600-token call keeps the two halves in two accumulators of one CTA instead
+    N, K = 1000, 4096
     w, g = fp4_weights(2, N, K)
-    x = G.activations(7, 9, 700, K)
+    x = G.activations(7, 9, 2600, K)
     with batch_invariant():
         yfull = gpu_nvfp4_gemm(w, float(g), N, K, x)
-        for m0, M in ((0, 40), (300, 300), (699 - 130, 130)):
+        for m0, M in ((0, 40), (300, 300), (2599 - 130, 130), (1000, 1500)):
             y = gpu_nvfp4_gemm(w, float(g), N, K, x[m0:m0 + M])
             assert np.array_equal(y.view(np.uint32), yfull[m0:m0 + M].view(np.uint32)), (m0, M)
     want = ref.nvfp4_gemm(w, float(g), N, K, x[:32], threads=16)
