@@ -8,24 +8,31 @@
 //   * A CTA owns 128 weight rows x BN tokens (BN = 256, or 128 for short
 //     prompts).  The weight rows are the MMA's M dimension, the tokens its N.
 //   * Warp 0 (TMA): per 256-wide K block, one bulk-tensor copy of the raw Q4_K
-//     tile (128 rows x 144 bytes) into one of two raw slots; per 64-wide K
-//     stage, one copy of the activation tile (BN tokens x 64 bf16) with the
-//     128-byte swizzle that the tensor core's K-major layout expects.
-//   * Warps 2-5 (dequant): thread t owns weight row t.  For each 64-wide stage
-//     (one Q4_K group: sub-blocks 2g and 2g+1) it turns 32 code bytes into 64
-//     bf16 weights, each the round-to-nearest-even bf16 of the fp32 weight
-//     fl32(q * d sc - dmin m) (packed fp32 FMAs, q * d sc exact inside them),
-//     i.e. the very value the standalone bf16 dequantization writes, and stores
-//     them in the swizzled K-major layout; a proxy fence publishes them to the
-//     tensor core.
+//     tile (128 rows x 144 bytes) into a ring of raw slots, refilled as soon as
+//     a slot's codes are in the dequant warps' registers.  Warp 2 (TMA): per
+//     64-wide K stage, one copy of the activation tile (BN tokens x 64 bf16)
+//     with the 128-byte swizzle that the tensor core's K-major layout expects.
+//   * Warps 4-11 (dequant): two threads per weight row.  Once per K block each
+//     loads the 64 code bytes it will convert (16 of each group), then for each
+//     64-wide stage (one Q4_K group: sub-blocks 2g and 2g+1) it turns its 16
+//     code bytes into 32 bf16 weights, each the round-to-nearest-even bf16 of
+//     the fp32 weight fl32(q * d sc - dmin m) (packed fp32 FMAs, q * d sc exact
+//     inside them), i.e. the very value the standalone bf16 dequantization
+//     writes.  They go to tensor memory, not shared memory: the row's lane, two
+//     weights per column (tcgen05.st), where the MMA reads its A operand.  The
+//     tensor core's operand reads, the activation and raw copies and the
+//     dequant stores would otherwise all share the SM's shared-memory bandwidth,
+//     which then set the pace of every stage.
 //   * Warp 1 (MMA): one elected thread issues four 128 x BN x 16 tcgen05.mma per
-//     stage into an fp32 accumulator in tensor memory and commits each stage's
-//     completion to the barrier that frees the stage.
-//   * Warps 2-5 then read the accumulator (tcgen05.ld, one 32-lane quarter per
-//     warp) and store fp32 rows of y with coalesced 128-byte writes.
+//     stage (A from tensor memory, B from shared memory) into an fp32
+//     accumulator in tensor memory and commits each stage's completion to the
+//     barriers that free the operand stage and the activation stage.
+//   * Warps 4-11 then read the accumulator (tcgen05.ld, one 32-lane quarter and
+//     half the columns per warp) and store fp32 rows of y with coalesced
+//     128-byte writes.
 //   * When the output has too few tiles to occupy the GPU (short prompts on the
 //     narrow down projection), a thread-block cluster splits K: each CTA parks
-//     its partial tile in its idle stage buffers and every rank sums one slice of
+//     its partial tile in its idle activation stages and every rank sums one slice of
 //     columns over the cluster's distributed shared memory, in rank order - no
 //     workspace, no atomics.
 // Every wait is bounded.  After one gives up, the producer waits (bounded) for
@@ -44,24 +51,37 @@ namespace {
 
 constexpr int kTileRows = 128;                    // weight rows per CTA (MMA M)
 constexpr int kStageK = 64;                       // K per pipeline stage (one swizzle row of bf16)
-constexpr int kABytes = kTileRows * kStageK * 2;  // 16 KiB dequantized operand per stage
 constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K tile per block
-constexpr int kThreads = 192;
+constexpr int kDqWarp0 = 4;                       // first dequant warp: warp w may use tensor-memory lanes 32 (w % 4) ..
+constexpr int kDqWarps = 8;                       // two threads per weight row
+constexpr int kTPR = kDqWarps / 4;                // dequant threads per weight row
+constexpr int kEPT = 32 / kTPR;                   // code bytes of a group per dequant thread and stage
+constexpr int kWPT = kEPT / 4;                    // the same in 32-bit words
+constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
+constexpr int kStageCols = kStageK / 2;           // tensor-memory columns of one stage's operand (bf16 pairs)
+constexpr int kABytes = kTileRows * kStageK * 2;  // 16 KiB: one stage's operand in shared memory
+constexpr uint32_t kTmemCols = 512;               // accumulator(s) + operand stages, whole allocation
 
-// Two stage rings: activations (XS deep) and dequantized weights (NS deep).  The
-// activation copy of stage i can only start once the MMAs of stage i - XS are
-// done, and it crosses L2, so that ring is the deeper one: XS stages of MMA
-// time must cover an L2 round trip under load.
-template <int BN>
+// Three rings: activations (XS stages, shared memory), dequantized weights
+// (NS stages: tensor memory when TA, else shared memory) and raw Q4_K blocks
+// (RS slots, shared memory).  The activation copy of stage i can only start
+// once the MMAs of stage i - XS are done, and it crosses L2, so that ring is the
+// deeper one: XS stages of MMA time must cover an L2 round trip under load.  A
+// raw slot is free again as soon as the dequant warps have read its codes into
+// registers, and its own producer refills it at once, RS - 1 blocks ahead.
+// TA = false serves the one launch whose two accumulators fill all 512
+// tensor-memory columns (batch-invariant mode, 256-token tiles).
+template <int BN, bool TA>
 struct Cfg {
-    static constexpr int NS = BN == 256 ? 3 : 4;  // dequantized-weight stages
-    static constexpr int XS = BN == 256 ? 4 : 6;  // activation stages
-    static constexpr int XB = BN * kStageK * 2;   // activation bytes per stage
+    static constexpr int NS = TA || BN == 128 ? 4 : 3;  // dequantized-weight stages
+    static constexpr int XS = BN == 256 ? 4 : 6;        // activation stages
+    static constexpr int RS = TA ? 3 : 2;               // raw Q4_K slots
+    static constexpr int XB = BN * kStageK * 2;         // activation bytes per stage
     static constexpr int x_off = 0;
-    static constexpr int a_off = XS * XB;
-    static constexpr int raw_off = a_off + NS * kABytes;
-    static constexpr int bar_off = raw_off + 2 * kRawBytes;
-    static constexpr int n_bars = 2 * NS + 2 * XS + 5;
+    static constexpr int a_off = x_off + XS * XB;       // shared-memory operand stages (TA = false)
+    static constexpr int raw_off = a_off + (TA ? 0 : NS * kABytes);
+    static constexpr int bar_off = raw_off + RS * kRawBytes;
+    static constexpr int n_bars = 2 * NS + 2 * XS + 2 * RS + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;  // + slack to align the base to 1024
     static_assert(bytes <= 227 * 1024, "dynamic shared memory per CTA");
@@ -74,7 +94,7 @@ __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpr
 // FP4: the weights are NVFP4 blocks (16 e4m3 scales, then 128 bytes of e2m1
 // pairs) instead of Q4_K; each operand element is the exact e2m1 * e4m3 product
 // in bf16, and the epilogue multiplies by the tensor scale gscale.
-template <int BN, bool FP4 = false>
+template <int BN, bool FP4, bool TA>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
                                                               int64_t ldy, int M, int N, int KB, float gscale,
@@ -88,20 +108,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // kernel that waits on this one also sees the main launch's outputs
     if (!late_wait) pdl_wait();  // the activations may come from the previous kernel
     pdl_trigger();
-    using C = Cfg<BN>;
-    constexpr int NS = C::NS, XS = C::XS;
+    using C = Cfg<BN, TA>;
+    constexpr int NS = C::NS, XS = C::XS, RS = C::RS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *xs = base + C::x_off;
     uint8_t *as = base + C::a_off;
     uint8_t *raw = base + C::raw_off;
     const uint32_t bar = smem_u32(base + C::bar_off);
-    // full: the four dequant warps wrote the stage's operand; empty: the MMAs reading
+    // full: the dequant warps wrote the stage's operand; empty: the MMAs reading
     // it are done; xfull: an activation stage's copy landed (tx bytes); xempty: the
     // MMAs reading it are done; rfull / rempty: the raw tile ring; accfull: all MMAs
     // of the tile are done
     const uint32_t full0 = bar, empty0 = bar + 8 * NS, xfull0 = bar + 16 * NS, xempty0 = xfull0 + 8 * XS,
-                   rfull0 = xempty0 + 8 * XS, rempty0 = rfull0 + 16, accfull = rempty0 + 16;
+                   rfull0 = xempty0 + 8 * XS, rempty0 = rfull0 + 8 * RS, accfull = rempty0 + 8 * RS;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + C::misc_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::misc_off + 4);
 
@@ -117,66 +137,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8 * s, 4);   // the four dequant warps
+            mbar_init(full0 + 8 * s, kDqWarps);  // the dequant warps
             mbar_init(empty0 + 8 * s, 1);  // tcgen05.commit
         }
         for (int s = 0; s < XS; ++s) {
             mbar_init(xfull0 + 8 * s, 1);   // producer (+ tx bytes)
             mbar_init(xempty0 + 8 * s, 1);  // tcgen05.commit
         }
-        for (int r = 0; r < 2; ++r) {
+        for (int r = 0; r < RS; ++r) {
             mbar_init(rfull0 + 8 * r, 1);
-            mbar_init(rempty0 + 8 * r, 4);
+            mbar_init(rempty0 + 8 * r, kDqWarps);
         }
         mbar_init(accfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), BN * nacc);
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // columns [0, BN * nacc): the accumulator(s); then (TA) NS operand stages of kStageCols
+    const uint32_t a_col0 = (uint32_t)(BN * nacc);
 
     if (warp == 0) {
-        // ------------------------------------------------------------- TMA
+        // ------------------------------------------------------- TMA: raw Q4_K
         if (lane == 0) {
             prefetch_tmap(&tmW);
-            prefetch_tmap(&tmX);
-            mbar_arrive_expect_tx(rfull0, kRawBytes);
-            tma_load_2d(smem_u32(raw), &tmW, kbeg * (kBlockBytes / 4), n0, rfull0);
-            int raw_issued = 1, x_issued = 0;
-            for (int i = 0; i < total && !*abort_flag; ++i) {
-                const int kb = i >> 2, g = i & 3, s = i % XS;
-                if (g == 0 && kb + 1 < KBs) {  // raw tile of the next block, one block ahead
-                    const int r = (kb + 1) & 1;
-                    if (kb + 1 >= 2 && !mbar_wait(rempty0 + 8 * r, (((kb + 1) >> 1) - 1) & 1, status)) {
-                        *abort_flag = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
-                    tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kbeg + kb + 1) * (kBlockBytes / 4), n0,
-                                rfull0 + 8 * r);
-                    ++raw_issued;
-                }
-                if (i >= XS && !mbar_wait(xempty0 + 8 * s, ((i / XS) - 1) & 1, status)) {
+            int issued = 0;
+            for (int kb = 0; kb < KBs && !*abort_flag; ++kb) {
+                const int r = kb % RS;
+                if (kb >= RS && !mbar_wait(rempty0 + 8 * r, ((kb / RS) - 1) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(xfull0 + 8 * s, C::XB);
-                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, xfull0 + 8 * s);
-                ++x_issued;
+                mbar_arrive_expect_tx(rfull0 + 8 * r, kRawBytes);
+                tma_load_2d(smem_u32(raw + r * kRawBytes), &tmW, (kbeg + kb) * (kBlockBytes / 4), n0, rfull0 + 8 * r);
+                ++issued;
             }
-            if (*abort_flag) {
-                // a wait gave up somewhere: wait (bounded) for this CTA's copies still in flight
-                for (int j = raw_issued > 2 ? raw_issued - 2 : 0; j < raw_issued; ++j)
-                    (void)mbar_wait(rfull0 + 8 * (j & 1), (j >> 1) & 1, status);
-                for (int j = x_issued > XS ? x_issued - XS : 0; j < x_issued; ++j)
-                    (void)mbar_wait(xfull0 + 8 * (j % XS), (j / XS) & 1, status);
-            }
+            // no copy may still be landing when the CTA leaves (bounded waits; on the
+            // normal path the dequant warps have consumed every block already)
+            for (int j = issued > RS ? issued - RS : 0; j < issued; ++j)
+                (void)mbar_wait(rfull0 + 8 * (j % RS), (j / RS) & 1, status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
@@ -190,14 +195,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kABytes));
                 const uint64_t bd = umma_desc_sw128(smem_u32(xs + sx * C::XB));
                 const bool second = i >= imid;
                 const uint32_t dacc = tmem + (second ? (uint32_t)BN : 0u);
                 const int i0 = second ? imid : 0;  // the accumulator's first stage
+                if constexpr (TA) {
+                    const uint32_t at = tmem + a_col0 + (uint32_t)(kStageCols * s);
 #pragma unroll
-                for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
-                    umma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
+                    for (int kk = 0; kk < kStageK / 16; ++kk)  // A: +8 columns, B: +32 bytes per 16-wide step
+                        umma_bf16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
+                } else {
+                    const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kABytes));
+#pragma unroll
+                    for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
+                        umma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
+                }
                 umma_commit(empty0 + 8 * s);
                 umma_commit(xempty0 + 8 * sx);
             }
@@ -205,17 +217,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // that tensor memory is freed only after the MMAs that write it)
             umma_commit(accfull);
         }
-    } else {
+    } else if (warp >= kDqWarp0) {
         // ---------------------------------------------------- dequant warps
-        const int t = threadIdx.x - 64;  // weight row within the tile
+        const int t = threadIdx.x - 32 * kDqWarp0;
+        const int row = t & (kTileRows - 1);  // weight row within the tile = tensor-memory lane
+        const int h = t >> 7;                 // which kEPT code bytes of each group: elements kEPT h ..
+        const uint32_t arow0 = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + a_col0;
         bool ok = true;
         for (int kb = 0; kb < KBs && ok; ++kb) {
-            const int r = kb & 1;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(rfull0 + 8 * r, (kb >> 1) & 1, status))) {
+            const int r = kb % RS;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(rfull0 + 8 * r, (kb / RS) & 1, status))) {
                 ok = false;
                 break;
             }
-            const uint8_t *rowp = raw + r * kRawBytes + t * kBlockBytes;
+            // the block's header and this thread's code bytes, read once; the raw slot
+            // is free for the next copy as soon as every dequant warp has them
+            const uint8_t *rowp = raw + r * kRawBytes + row * kBlockBytes;
+            const uint4 hd = *reinterpret_cast<const uint4 *>(rowp);
+            uint32_t qv[4][kWPT];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint8_t *src = rowp + 16 + 32 * g + kEPT * h;
+                if constexpr (kWPT == 4) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src);
+                    qv[g][0] = v.x, qv[g][1] = v.y, qv[g][2] = v.z, qv[g][3] = v.w;
+                } else {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(src);
+                    qv[g][0] = v.x, qv[g][1] = v.y;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rempty0 + 8 * r);
             if constexpr (FP4) {
                 for (int g4 = 0; g4 < 4; ++g4) {
                     const int i = kb * 4 + g4, s = i % NS;
@@ -224,40 +256,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         ok = false;
                         break;
                     }
-                    // stage g4: weights 64*g4 .. +63 of the block, scales 4*g4 .. +3 (16 weights each)
-                    const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(rowp + 4 * g4);
-                    __nv_bfloat162 sv[4];
+                    // stage g4: weights 64*g4 .. +63 of the block, scales 4*g4 .. +3 (16 weights
+                    // each); this thread takes weights 2 kEPT h .. +2 kEPT - 1 of the stage
+                    // (code word j: scale kEPT h / 8 + j / 2)
+                    const uint32_t scw = g4 == 0 ? hd.x : g4 == 1 ? hd.y : g4 == 2 ? hd.z : hd.w;
+                    __nv_bfloat162 sv[kEPT / 8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float f = e4m3_to_f32(sc4 >> (8 * q));
+                    for (int q = 0; q < kEPT / 8; ++q) {
+                        const float f = e4m3_to_f32(scw >> (8 * (kEPT * h / 8 + q)));
                         sv[q] = __floats2bfloat162_rn(f, f);  // exact: e4m3 values are bf16 values
                     }
-                    const uint4 va = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g4);
-                    const uint4 vb = *reinterpret_cast<const uint4 *>(rowp + 32 + 32 * g4);
-                    const uint32_t wds[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-                    uint8_t *arow = as + s * kABytes + (t >> 3) * 1024 + (t & 7) * 128;
+                    uint32_t p[2 * kEPT / 2];  // stage columns kEPT h .. : two weights each
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {  // chunk j: weights 8j..8j+7 of the stage, scale j / 2
-                        uint32_t p[4];
-                        e2m1x8_to_bf16(wds[j], p[0], p[1], p[2], p[3]);
+                    for (int j = 0; j < kWPT; ++j) {
+                        e2m1x8_to_bf16(qv[g4][j], p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) p[q] = as_u32(__hmul2(as_bf2(p[q]), sv[j >> 1]));  // exact
-                        *reinterpret_cast<uint4 *>(arow + ((j ^ (t & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+                        for (int q = 0; q < 4; ++q) p[4 * j + q] = as_u32(__hmul2(as_bf2(p[4 * j + q]), sv[j >> 1]));  // exact
                     }
-                    fence_proxy_async_smem();  // make the stores visible to the tensor core
+                    if constexpr (TA) {
+                        tc_fence_after();  // after the wait for the MMAs that read this stage
+                        tmem_st(arow0 + (uint32_t)(kStageCols * s + kEPT * h), p);
+                        tmem_st_wait();
+                        tc_fence_before();
+                    } else {
+                        // 128-byte-swizzled K-major rows: 16-byte chunk c of row `row` at (c ^ row % 8)
+                        uint8_t *arow = as + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                        for (int j = 0; j < kEPT / 4; ++j)
+                            *reinterpret_cast<uint4 *>(arow + ((((kEPT / 4) * h + j) ^ (row & 7)) << 4)) =
+                                make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+                        fence_proxy_async_smem();  // make the stores visible to the tensor core
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(full0 + 8 * s);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(rempty0 + 8 * r);
                 continue;
             }
-            const uint4 h = *reinterpret_cast<const uint4 *>(rowp);
-            const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
-            const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-            const uint32_t sc_lo = h.y & 0x3F3F3F3Fu, m_lo = h.z & 0x3F3F3F3Fu;
-            const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
-            const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+            const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+            const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+            const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
+            const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+            const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
             for (int g = 0; g < 4; ++g) {
                 const int i = kb * 4 + g, s = i % NS;
                 if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status))) {
@@ -270,25 +309,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const float dsc0 = d * (float)((scw >> (8 * b0)) & 0xFFu), dm0 = dmin * (float)((mw >> (8 * b0)) & 0xFFu);
                 const float dsc1 = d * (float)((scw >> (8 * b1)) & 0xFFu), dm1 = dmin * (float)((mw >> (8 * b1)) & 0xFFu);
                 const GroupScales gs = group_scales(dsc0, dm0, dsc1, dm1);
-                const uint4 qa = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g);
-                const uint4 qb = *reinterpret_cast<const uint4 *>(rowp + 32 + 32 * g);
-                const uint32_t wds[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-                uint8_t *arow = as + s * kABytes + (t >> 3) * 1024 + (t & 7) * 128;
+                // elements kEPT h .. of sub-block 2g (stage columns kEPT h / 2 ..) and of 2g+1
+                // (16 + kEPT h / 2 ..)
+                uint32_t lo[2 * kWPT], hi[2 * kWPT];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {  // chunk j: elements 8j..8j+7 of each sub-block
-                    uint32_t lo[4], hi[4];
-q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
-                    q4k_word_to_bf16(wds[2 * j + 1], gs, lo[2], lo[3], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(arow + ((j ^ (t & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<uint4 *>(arow + (((j + 4) ^ (t & 7)) << 4)) =
-                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                for (int j = 0; j < kWPT; ++j)
+                    q4k_word_to_bf16(qv[g][j], gs, lo[2 * j], lo[2 * j + 1], hi[2 * j], hi[2 * j + 1]);
+                if constexpr (TA) {
+                    tc_fence_after();  // after the wait for the MMAs that read this stage
+                    const uint32_t at = arow0 + (uint32_t)(kStageCols * s + kEPT / 2 * h);
+                    tmem_st(at, lo);
+                    tmem_st(at + 16, hi);
+                    tmem_st_wait();
+                    tc_fence_before();
+                } else {
+                    // 128-byte-swizzled K-major rows: 16-byte chunk c of row `row` at (c ^ row % 8);
+                    // chunks (kEPT / 8) h .. hold these elements of sub-block 2g, 4 + (kEPT / 8) h .. of 2g+1
+                    uint8_t *arow = as + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                    for (int j = 0; j < kEPT / 8; ++j) {
+                        const int cl = (kEPT / 8) * h + j;
+                        *reinterpret_cast<uint4 *>(arow + ((cl ^ (row & 7)) << 4)) =
+                            make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+                        *reinterpret_cast<uint4 *>(arow + (((cl + 4) ^ (row & 7)) << 4)) =
+                            make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                    }
+                    fence_proxy_async_smem();  // make the stores visible to the tensor core
                 }
-                fence_proxy_async_smem();  // make the stores visible to the tensor core
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full0 + 8 * s);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(rempty0 + 8 * r);
         }
         if (!ok && lane == 0) *abort_flag = 1;
         // ------------------------------------------------------- epilogue
@@ -296,11 +346,13 @@ q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
             tc_fence_after();
             const int q = warp & 3;  // tensor-memory lane quarter this warp may read
             const int rl = 32 * q + lane, n = n0 + rl;
+            constexpr int kCC = BN / 32 / kTPR;           // 32-column chunks per warp
+            const int share = (warp - kDqWarp0) >> 2;     // which share of the columns this warp takes
             // with a K split, the partial tile goes to this CTA's (now idle) stage
             // buffers, column-major [BN][128], for the cluster reduction below
             float *part = reinterpret_cast<float *>(base);
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = share * kCC; cc < (share + 1) * kCC; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
                 tmem_ld_wait();
@@ -322,6 +374,24 @@ q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
                     }
                 }
             }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------ TMA: activations
+        if (lane == 0) {
+            prefetch_tmap(&tmX);
+            int issued = 0;
+            for (int i = 0; i < total && !*abort_flag; ++i) {
+                const int kb = i >> 2, g = i & 3, s = i % XS;
+                if (i >= XS && !mbar_wait(xempty0 + 8 * s, ((i / XS) - 1) & 1, status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(xfull0 + 8 * s, C::XB);
+                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, xfull0 + 8 * s);
+                ++issued;
+            }
+            for (int j = issued > XS ? issued - XS : 0; j < issued; ++j)
+                (void)mbar_wait(xfull0 + 8 * (j % XS), (j / XS) & 1, status);
         }
     }
     if (S > 1) {
@@ -350,7 +420,7 @@ q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
         // a bounded wait for the MMAs still running) before the columns are freed
         (void)mbar_wait(accfull, 0, status);
         tc_fence_after();
-        tmem_dealloc(tmem, BN * nacc);
+        tmem_dealloc(tmem, kTmemCols);
     }
     if (late_wait) pdl_wait();
 }
@@ -371,7 +441,7 @@ int k_split(const DeviceInfo &di, int64_t tiles, int KB) {
 
 // S: the cluster K split (1: none); nacc = 2: two accumulators in place of a 2-way
 // split (S = 1 then).
-template <int BN, bool FP4>
+template <int BN, bool FP4, bool TA = true>
 cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
                       int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int S, int late_wait = 0,
                       int nacc = 1) {
@@ -380,13 +450,17 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     if (e != cudaSuccess) return e;
     e = make_act_tmap_sw128(&tmX, x, M, K, ldx, BN);
     if (e != cudaSuccess) return e;
-    const int smem = Cfg<BN>::bytes;
-    static_assert(Cfg<BN>::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers");
-    e = ensure_smem((const void *)gemm_tc_kernel<BN, FP4>, smem);
+    using C = Cfg<BN, TA>;
+    const int smem = C::bytes;
+    static_assert(C::x_off + C::XS * C::XB >= BN * kTileRows * 4, "the partial tile fits in the activation stages");
+    constexpr int a_cols = TA ? C::NS * kStageCols : 0;  // tensor-memory operand stages
+    static_assert(BN + a_cols <= (int)kTmemCols, "the accumulator and the stages fit");
+    if (nacc < 1 || nacc > 2 || nacc * BN + a_cols > (int)kTmemCols) return cudaErrorInvalidValue;
+    e = ensure_smem((const void *)gemm_tc_kernel<BN, FP4, TA>, smem);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
-    return launch_pdl(gemm_tc_kernel<BN, FP4>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
+    return launch_pdl(gemm_tc_kernel<BN, FP4, TA>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
                       tmX, y, ldy, (int)M, (int)N, KB, g, late_wait, nacc, di.status);
 }
 
@@ -415,11 +489,12 @@ cudaError_t launch_split(const DeviceInfo &di, const void *w, int64_t N, int64_t
     const int64_t tn = (N + kTileRows - 1) / kTileRows;
     if (invariant) {
         // at most 2 ways, so that one CTA can hold both halves' 256-column
-        // accumulators when the tiles alone fill the GPU
+        // accumulators (the operand stages then in shared memory) when the
+        // tiles alone fill the GPU
         const int S = k_split(di, tn, KB) > 1 ? 2 : 1;
         if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
         if (S == 2 && 2 * tn * ((M + 255) / 256) > di.sm_count)
-            return launch_bn<256, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, 1, 0, 2);
+            return launch_bn<256, FP4, false>(di, w, N, K, x, M, ldx, y, ldy, g, s, 1, 0, 2);
         return launch_bn<256, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
     }
     if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, k_split(di, tn, KB));
