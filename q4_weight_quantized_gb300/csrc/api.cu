@@ -430,7 +430,7 @@ q4k_status q4k_moe_route(const int32_t *topk_ids, int64_t T, int32_t topk, int32
     return e == cudaSuccess ? Q4K_OK : cuda_fail(e);
 }
 
-// Many items per expert (32 or more on average): tensor-core tiles of up to 256
+// Many items per expert (32 or more on average): tensor-core tiles of up to 192
 // expert-sorted tokens; otherwise the small-M kernel over each expert's few tokens.
 static bool moe_uses_tc(int32_t E, int64_t T, int32_t topk) { return T * (int64_t)topk >= 32 * (int64_t)E; }
 

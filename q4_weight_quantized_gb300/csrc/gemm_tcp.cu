@@ -8,17 +8,22 @@
 //   * warp 0    TMA: per 256-wide K block the raw Q4_K tile of 128 weight rows
 //               (two slots, issued one block ahead, across tile boundaries), per
 //               64-wide stage the token tile's activation rows (128-byte swizzle;
-//               one or two 128-row boxes, as the tile's count needs);
-//   * warp 1    MMA: one thread issues 4 x tcgen05.mma (128 x N x 16) per stage
-//               into one of two 256-column accumulators in tensor memory;
-//   * warps 2-9 dequant: two threads per weight row, each taking 16 of the 32
-//               code bytes of stage g (both its sub-blocks, 2g and 2g+1), writing
-//               the K-major 128-byte-swizzled bf16 operand;
+//               one or two 96-row boxes, as the tile's count needs);
+//   * warp 1    MMA: one thread issues 4 x tcgen05.mma (128 x N x 16) per stage,
+//               A from tensor memory, B from shared memory, into one of two
+//               192-column accumulators in tensor memory;
+//   * warps 2-9 dequant: two threads per weight row.  Each reads the 64 code
+//               bytes it converts once per block (16 of each group: elements
+//               16h .. 16h+15 of both sub-blocks 2g and 2g+1) and writes the bf16
+//               operand of each stage into tensor memory (tcgen05.st: the row's
+//               lane, two weights per column, four stages after the
+//               accumulators), off the shared-memory bandwidth that the
+//               activation copies and the tensor core's B reads use;
 //   * warps 10-13 epilogue: tcgen05.ld of the finished accumulator and fp32
 //               stores, while the MMA warp already fills the other accumulator.
 // Tiles are (128-row weight tile, token tile of the routing's list) pairs taken
 // round-robin (tile = CTA + k * grid).  A token tile is (expert, first item,
-// count <= 256) of the expert-sorted activation rows; the MMA width is the count
+// count <= 192) of the expert-sorted activation rows; the MMA width is the count
 // rounded up to 16, and output column j goes to the row of item perm[first + j].
 // Every wait is bounded; the sum per output element runs in a fixed order, so
 // results are run-to-run deterministic.
@@ -33,22 +38,25 @@ namespace q4k {
 namespace {
 
 constexpr int kTileRows = 128;                      // weight rows per tile (MMA M)
-constexpr int kBN = 256;                            // tokens per tile (MMA N at most)
+constexpr int kBN = kMoeTileItems;                  // tokens per tile (MMA N at most): 192
 constexpr int kStageK = 64;                         // K per stage: one 128-byte swizzle row of bf16
-constexpr int kNS = 3;                              // stages
-constexpr int kXB = kBN * kStageK * 2;              // 32 KiB activations per stage
+constexpr int kNS = 4;                              // stages
+constexpr int kXB = kBN * kStageK * 2;              // 24 KiB activations per stage
 constexpr int kXBox = kBN / 2;                      // activation rows per TMA box
-constexpr int kXBoxBytes = kXBox * kStageK * 2;     // 16 KiB: rows kXBox.. land right after, as one 256-row box would
-constexpr int kAB = kTileRows * kStageK * 2;        // 16 KiB dequantized weights per stage
+constexpr int kXBoxBytes = kXBox * kStageK * 2;     // 12 KiB: rows kXBox.. land right after, as one 192-row box would
+constexpr int kStageCols = kStageK / 2;             // tensor-memory columns of one stage's operand (bf16 pairs)
 constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K per block
 constexpr int kDqWarps = 8, kEpWarps = 4;
 constexpr int kThreads = (2 + kDqWarps + kEpWarps) * 32;
-constexpr int kX = 0, kA = kNS * kXB, kRaw = kA + kNS * kAB, kBar = kRaw + 2 * kRawBytes;
+constexpr int kX = 0, kRaw = kNS * kXB, kBar = kRaw + 2 * kRawBytes;
 constexpr int kNBars = 3 * kNS + 2 + 2 + 2 + 2 + 1;
 constexpr int kMisc = kBar + kNBars * 8;
 constexpr int kOrow = kMisc + 16;                   // [2][kBN] output rows (MoE)
 constexpr int kSmem = kOrow + 2 * kBN * 4 + 1024;   // + slack to align the base to 1024
-constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr uint32_t kAcol0 = 2 * kBN;                // the operand stages follow the two accumulators
+constexpr uint32_t kTmemCols = 512;
+static_assert(kAcol0 + kNS * kStageCols <= kTmemCols, "accumulators and operand stages fit in tensor memory");
+static_assert(kBN % 16 == 0 && kXBoxBytes % 1024 == 0, "MMA width and 1024-byte swizzle atoms");
 
 struct Tile {
     int n0, m0, cnt, wrow0;
@@ -86,7 +94,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *xs = base + kX;
-    uint8_t *as = base + kA;
     uint8_t *raw = base + kRaw;
     const uint32_t bar = smem_u32(base + kBar);
     // full: the dequant warps wrote the stage's operand; xfull: its activation copy
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
-                    // one 128-row box for a tile of at most 128 tokens, two otherwise:
+                    // one kXBox-row box for a tile of at most kXBox tokens, two otherwise:
                     // the MMA reads only the tile's rows
                     const int nbox = t.cnt > kXBox ? 2 : 1;
                     mbar_arrive_expect_tx(xfull0 + 8 * s, nbox * kXBoxBytes);
@@ -214,11 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kAB));
+                    const uint32_t at = tmem + kAcol0 + (uint32_t)(kStageCols * s);
                     const uint64_t bd = umma_desc_sw128(smem_u32(xs + s * kXB));
 #pragma unroll
-                    for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
-                        umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (j | kk) != 0);
+                    for (int kk = 0; kk < kStageK / 16; ++kk)  // A: +8 columns, B: +32 bytes per 16-wide step
+                        umma_bf16_ts(d, at + 8 * kk, bd + 2 * kk, idesc, (j | kk) != 0);
                     umma_commit(empty0 + 8 * s);
                 }
                 if (ok) umma_commit(accfull0 + 8 * buf);
@@ -228,9 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
         }
     } else if (warp < 2 + kDqWarps) {
         // ---------------------------------------------------- dequant warps
-        const int t = threadIdx.x - 64;
-        const int row = t & (kTileRows - 1);  // weight row within the tile
-        const int h = t >> 7;                 // which 16 code bytes of each group: elements 16h..16h+15
+        // warp w may reach tensor-memory lanes 32 (w % 4) .. +31: its rows are those lanes
+        const int row = ((warp & 3) << 5) | lane;  // weight row within the tile
+        const int h = (warp - 2) >> 2;              // which 16 code bytes of each group: elements 16h..16h+15
+        const uint32_t arow0 = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kAcol0;
         bool ok = true;
         for (int b = 0; b < nblocks && ok; ++b) {
             const int r = b & 1;
@@ -238,8 +246,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 ok = false;
                 break;
             }
+            // the block's header and this thread's 64 code bytes, read once; the raw
+            // slot is free for the next copy as soon as every dequant warp has them
             const uint8_t *rowp = raw + r * kRawBytes + row * kBlockBytes;
             const uint4 hd = *reinterpret_cast<const uint4 *>(rowp);
+            uint4 qv[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) qv[g] = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g + 16 * h);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rempty0 + 8 * r);
             const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
             const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
             const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
@@ -258,24 +273,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 const float dsc0 = d * (float)((scw >> (8 * b0)) & 0xFFu), dm0 = dmin * (float)((mw >> (8 * b0)) & 0xFFu);
                 const float dsc1 = d * (float)((scw >> (8 * b1)) & 0xFFu), dm1 = dmin * (float)((mw >> (8 * b1)) & 0xFFu);
                 const GroupScales gs = group_scales(dsc0, dm0, dsc1, dm1);
-                const uint4 qw = *reinterpret_cast<const uint4 *>(rowp + 16 + 32 * g + 16 * h);
-                const uint32_t wds[4] = {qw.x, qw.y, qw.z, qw.w};
-                uint8_t *arow = as + s * kAB + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {  // chunk 2h+j: elements 16h+8j .. +7 of each sub-block
-                    uint32_t lo[4], hi[4];
-                    q4k_word_to_bf16(wds[2 * j], gs, lo[0], lo[1], hi[0], hi[1]);
-                    q4k_word_to_bf16(wds[2 * j + 1], gs, lo[2], lo[3], hi[2], hi[3]);
-                    const int cl = 2 * h + j;
-                    *reinterpret_cast<uint4 *>(arow + ((cl ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<uint4 *>(arow + (((cl + 4) ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                }
-                fence_proxy_async_smem();  // make the stores visible to the tensor core
+                // elements 16h .. 16h+15 of sub-block 2g (stage columns 8h ..) and of 2g+1 (16 + 8h ..)
+                uint32_t lo[8], hi[8];
+                q4k_word_to_bf16(qv[g].x, gs, lo[0], lo[1], hi[0], hi[1]);
+                q4k_word_to_bf16(qv[g].y, gs, lo[2], lo[3], hi[2], hi[3]);
+                q4k_word_to_bf16(qv[g].z, gs, lo[4], lo[5], hi[4], hi[5]);
+                q4k_word_to_bf16(qv[g].w, gs, lo[6], lo[7], hi[6], hi[7]);
+                tc_fence_after();  // after the wait for the MMAs that read this stage
+                const uint32_t at = arow0 + (uint32_t)(kStageCols * s + 8 * h);
+                tmem_st8(at, lo);
+                tmem_st8(at + 16, hi);
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full0 + 8 * s);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(rempty0 + 8 * r);
             if (*abort_flag) ok = false;
         }
         if (!ok && lane == 0) *abort_flag = 1;

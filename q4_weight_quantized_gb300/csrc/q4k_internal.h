@@ -122,13 +122,13 @@ cudaError_t launch_moe_smallm(const DeviceInfo &di, const void *w_experts, int E
 // tiles is given, it also lists every (expert, first item, item count) token
 // tile of at most kMoeTileItems items, and n_tiles[0..3] receives their number,
 // E, n_items and kRoutingStamp.
-constexpr int kMoeTileItems = 256;
+constexpr int kMoeTileItems = 192;
 size_t route_smem_bytes(int E);
 cudaError_t launch_moe_route(const int32_t *ids, int64_t n_items, int E, int32_t *offsets, int32_t *perm,
                              bool invalid_tail, int4 *tiles, int *n_tiles, cudaStream_t s);
 
 // Upper bound on the number of token tiles the routing can produce: an expert
-// with c > 0 items gives ceil(c / 256) <= 1 + (c - 1) / 256 tiles, and at most
+// with c > 0 items gives ceil(c / T) <= 1 + (c - 1) / T tiles (T = kMoeTileItems), and at most
 // min(E, n_items) experts have items.
 inline int64_t moe_max_tiles(int E, int64_t n_items) {
     return (n_items < E ? n_items : (int64_t)E) + (n_items + kMoeTileItems - 1) / kMoeTileItems;

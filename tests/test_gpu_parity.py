@@ -733,7 +733,7 @@ def test_moe_determinism(syn, moe_up):
 @pytest.mark.parametrize("E,T,topk,N,K", [(4, 64, 2, 256, 512), (3, 300, 2, 200, 768)])
 def test_moe_tensor_core_path(ref, syn, E, T, topk, N, K):
     # >= 32 items per expert on average: the tcgen05 path with expert-sorted rows;
-    # the second case has experts with more than 256 items (several token tiles)
+    # the second case has experts with more than 192 items (several token tiles)
     w = np.concatenate([G.weights(4, 60 + e, N, K, outliers=True) for e in range(E)])
     ids, gates = syn.routing(700 + T, 701 + T, T, E, topk)
     ids[3, 1] = -5                                   # an invalid id: zero row, no contribution
