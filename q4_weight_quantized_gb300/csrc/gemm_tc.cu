@@ -297,29 +297,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
             const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
             const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+            // all four stages of the block are converted first, in registers (they need
+            // only the codes), and handed to the MMA one by one as its stages free up:
+            // the conversions of the block overlap each other and those waits.
+            // Stage g: elements kEPT h .. of sub-block 2g (stage columns kEPT h / 2 ..)
+            // and of 2g+1 (16 + kEPT h / 2 ..)
+            uint32_t lo[4][2 * kWPT], hi[4][2 * kWPT];
+#pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const int i = kb * 4 + g, s = i % NS;
-                if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status))) {
-                    ok = false;
-                    break;
-                }
                 // scales of sub-blocks 2g (low nibbles) and 2g+1 (high nibbles)
                 const uint32_t scw = g < 2 ? sc_lo : sc_hi, mw = g < 2 ? m_lo : m_hi;
                 const int b0 = (2 * g) & 3, b1 = (2 * g + 1) & 3;
                 const float dsc0 = d * (float)((scw >> (8 * b0)) & 0xFFu), dm0 = dmin * (float)((mw >> (8 * b0)) & 0xFFu);
                 const float dsc1 = d * (float)((scw >> (8 * b1)) & 0xFFu), dm1 = dmin * (float)((mw >> (8 * b1)) & 0xFFu);
                 const GroupScales gs = group_scales(dsc0, dm0, dsc1, dm1);
-                // elements kEPT h .. of sub-block 2g (stage columns kEPT h / 2 ..) and of 2g+1
-                // (16 + kEPT h / 2 ..)
-                uint32_t lo[2 * kWPT], hi[2 * kWPT];
 #pragma unroll
                 for (int j = 0; j < kWPT; ++j)
-                    q4k_word_to_bf16(qv[g][j], gs, lo[2 * j], lo[2 * j + 1], hi[2 * j], hi[2 * j + 1]);
+                    q4k_word_to_bf16(qv[g][j], gs, lo[g][2 * j], lo[g][2 * j + 1], hi[g][2 * j], hi[g][2 * j + 1]);
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int i = kb * 4 + g, s = i % NS;
+                if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status))) {
+                    ok = false;
+                    break;
+                }
                 if constexpr (TA) {
                     tc_fence_after();  // after the wait for the MMAs that read this stage
                     const uint32_t at = arow0 + (uint32_t)(kStageCols * s + kEPT / 2 * h);
-                    tmem_st(at, lo);
-                    tmem_st(at + 16, hi);
+                    tmem_st(at, lo[g]);
+                    tmem_st(at + 16, hi[g]);
                     tmem_st_wait();
                     tc_fence_before();
                 } else {
@@ -330,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     for (int j = 0; j < kEPT / 8; ++j) {
                         const int cl = (kEPT / 8) * h + j;
                         *reinterpret_cast<uint4 *>(arow + ((cl ^ (row & 7)) << 4)) =
-                            make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+                            make_uint4(lo[g][4 * j], lo[g][4 * j + 1], lo[g][4 * j + 2], lo[g][4 * j + 3]);
                         *reinterpret_cast<uint4 *>(arow + (((cl + 4) ^ (row & 7)) << 4)) =
-                            make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                            make_uint4(hi[g][4 * j], hi[g][4 * j + 1], hi[g][4 * j + 2], hi[g][4 * j + 3]);
                     }
                     fence_proxy_async_smem();  // make the stores visible to the tensor core
                 }
