@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         umma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
                 }
                 umma_commit(empty0 + 8 * s);
-                umma_commit(xempty0 + 8 * sx);
+                if constexpr (NS != XS) umma_commit(xempty0 + 8 * sx);  // equal depths: one barrier frees both
             }
             // completes once every MMA issued above has (also after an abort, so
             // that tensor memory is freed only after the MMAs that write it)
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int issued = 0;
             for (int i = 0; i < total && !*abort_flag; ++i) {
                 const int kb = i >> 2, g = i & 3, s = i % XS;
-                if (i >= XS && !mbar_wait(xempty0 + 8 * s, ((i / XS) - 1) & 1, status)) {
+                if (i >= XS && !mbar_wait((NS == XS ? empty0 : xempty0) + 8 * s, ((i / XS) - 1) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
