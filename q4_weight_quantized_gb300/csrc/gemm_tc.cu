@@ -73,7 +73,7 @@ constexpr uint32_t kTmemCols = 512;               // accumulator(s) + operand st
 // tensor-memory columns (batch-invariant mode, 256-token tiles).
 template <int BN, bool TA>
 struct Cfg {
-    static constexpr int NS = TA || BN == 128 ? 4 : 3;  // dequantized-weight stages
+    static constexpr int NS = TA ? (BN == 128 ? 6 : 4) : (BN == 128 ? 4 : 3);  // dequantized-weight stages
     static constexpr int XS = BN == 256 ? 4 : 6;        // activation stages
     static constexpr int RS = TA ? 3 : 2;               // raw Q4_K slots
     static constexpr int XB = BN * kStageK * 2;         // activation bytes per stage
@@ -122,6 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // of the tile are done
     const uint32_t full0 = bar, empty0 = bar + 8 * NS, xfull0 = bar + 16 * NS, xempty0 = xfull0 + 8 * XS,
                    rfull0 = xempty0 + 8 * XS, rempty0 = rfull0 + 8 * RS, accfull = rempty0 + 8 * RS;
+    // rings of equal depth share their barriers: a stage is full once the dequant
+    // warps have arrived and its activation copy has landed, and one commit frees it
+    constexpr bool kOneRing = NS == XS;
+    const uint32_t xfull_b = kOneRing ? full0 : xfull0, xempty_b = kOneRing ? empty0 : xempty0;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + C::misc_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::misc_off + 4);
 
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8 * s, kDqWarps);  // the dequant warps
+            mbar_init(full0 + 8 * s, kDqWarps + (kOneRing ? 1 : 0));  // the dequant warps (+ the activation producer)
             mbar_init(empty0 + 8 * s, 1);  // tcgen05.commit
         }
         for (int s = 0; s < XS; ++s) {
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (int i = 0; i < total; ++i) {
                 const int s = i % NS, sx = i % XS;
                 if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status) ||
-                    !mbar_wait(xfull0 + 8 * sx, (i / XS) & 1, status)) {
+                    (!kOneRing && !mbar_wait(xfull0 + 8 * sx, (i / XS) & 1, status))) {
                     *abort_flag = 1;
                     break;
                 }
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         umma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
                 }
                 umma_commit(empty0 + 8 * s);
-                if constexpr (NS != XS) umma_commit(xempty0 + 8 * sx);  // equal depths: one barrier frees both
+                if constexpr (!kOneRing) umma_commit(xempty0 + 8 * sx);
             }
             // completes once every MMA issued above has (also after an abort, so
             // that tensor memory is freed only after the MMAs that write it)
@@ -389,16 +393,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int issued = 0;
             for (int i = 0; i < total && !*abort_flag; ++i) {
                 const int kb = i >> 2, g = i & 3, s = i % XS;
-                if (i >= XS && !mbar_wait((NS == XS ? empty0 : xempty0) + 8 * s, ((i / XS) - 1) & 1, status)) {
+                if (i >= XS && !mbar_wait(xempty_b + 8 * s, ((i / XS) - 1) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(xfull0 + 8 * s, C::XB);
-                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, xfull0 + 8 * s);
+                mbar_arrive_expect_tx(xfull_b + 8 * s, C::XB);
+                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, xfull_b + 8 * s);
                 ++issued;
             }
             for (int j = issued > XS ? issued - XS : 0; j < issued; ++j)
-                (void)mbar_wait(xfull0 + 8 * (j % XS), (j / XS) & 1, status);
+                (void)mbar_wait(xfull_b + 8 * (j % XS), (j / XS) & 1, status);
         }
     }
     if (S > 1) {
