@@ -32,7 +32,7 @@
 //     128-byte writes.
 //   * When the output has too few tiles to occupy the GPU (short prompts on the
 //     narrow down projection), a thread-block cluster splits K: each CTA parks
-//     its partial tile in its idle activation stages and every rank sums one slice of
+//     its partial tile in its idle stage buffers and every rank sums one slice of
 //     columns over the cluster's distributed shared memory, in rank order - no
 //     workspace, no atomics.
 // Every wait is bounded.  After one gives up, the producer waits (bounded) for
@@ -73,8 +73,11 @@ constexpr uint32_t kTmemCols = 512;               // accumulator(s) + operand st
 // tensor-memory columns (batch-invariant mode, 256-token tiles).
 template <int BN, bool TA>
 struct Cfg {
-    static constexpr int NS = TA ? (BN == 128 ? 6 : 4) : (BN == 128 ? 4 : 3);  // dequantized-weight stages
-    static constexpr int XS = BN == 256 ? 4 : 6;        // activation stages
+    // with the operand in tensor memory the two rings are equally deep, so that
+    // they share their barriers (in shared memory 3 operand stages leave room for
+    // 4 activation stages, which measured faster than 3 + 3)
+    static constexpr int NS = TA ? (BN == 128 ? 6 : 4) : 3;  // dequantized-weight stages
+    static constexpr int XS = TA ? NS : 4;                   // activation stages
     static constexpr int RS = TA ? 3 : 2;               // raw Q4_K slots
     static constexpr int XB = BN * kStageK * 2;         // activation bytes per stage
     static constexpr int x_off = 0;
@@ -463,7 +466,7 @@ cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K,
     if (e != cudaSuccess) return e;
     using C = Cfg<BN, TA>;
     const int smem = C::bytes;
-    static_assert(C::x_off + C::XS * C::XB >= BN * kTileRows * 4, "the partial tile fits in the activation stages");
+    static_assert(C::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers ahead of the raw slots");
     constexpr int a_cols = TA ? C::NS * kStageCols : 0;  // tensor-memory operand stages
     static_assert(BN + a_cols <= (int)kTmemCols, "the accumulator and the stages fit");
     if (nacc < 1 || nacc > 2 || nacc * BN + a_cols > (int)kTmemCols) return cudaErrorInvalidValue;

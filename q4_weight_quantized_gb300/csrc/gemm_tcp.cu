@@ -49,7 +49,7 @@ constexpr int kRawBytes = kTileRows * kBlockBytes;  // 18 KiB raw Q4_K per block
 constexpr int kDqWarps = 8, kEpWarps = 4;
 constexpr int kThreads = (2 + kDqWarps + kEpWarps) * 32;
 constexpr int kX = 0, kRaw = kNS * kXB, kBar = kRaw + 2 * kRawBytes;
-constexpr int kNBars = 3 * kNS + 2 + 2 + 2 + 2 + 1;
+constexpr int kNBars = 2 * kNS + 2 + 2 + 2 + 2 + 1;
 constexpr int kMisc = kBar + kNBars * 8;
 constexpr int kOrow = kMisc + 16;                   // [2][kBN] output rows (MoE)
 constexpr int kSmem = kOrow + 2 * kBN * 4 + 1024;   // + slack to align the base to 1024
@@ -96,10 +96,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
     uint8_t *xs = base + kX;
     uint8_t *raw = base + kRaw;
     const uint32_t bar = smem_u32(base + kBar);
-    // full: the dequant warps wrote the stage's operand; xfull: its activation copy
-    // landed; empty: its MMAs are done; rfull / rempty: raw Q4_K ring; accfull /
-    // accempty: the two tensor-memory accumulators; mmadone: every MMA issued
-    const uint32_t full0 = bar, empty0 = bar + 8 * kNS, xfull0 = bar + 16 * kNS, rfull0 = bar + 24 * kNS,
+    // full: the dequant warps wrote the stage's operand and its activation copy
+    // landed (one barrier, so that the MMA thread waits once per stage); empty: its
+    // MMAs are done; rfull / rempty: raw Q4_K ring; accfull / accempty: the two
+    // tensor-memory accumulators; mmadone: every MMA issued
+    const uint32_t full0 = bar, empty0 = bar + 8 * kNS, rfull0 = bar + 16 * kNS,
                    rempty0 = rfull0 + 16, accfull0 = rempty0 + 16, accempty0 = accfull0 + 16,
                    mmadone = accempty0 + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + kMisc);
@@ -120,8 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(full0 + 8 * s, kDqWarps);  // the dequant warps
-            mbar_init(xfull0 + 8 * s, 1);        // producer (+ tx bytes)
+            mbar_init(full0 + 8 * s, kDqWarps + 1);  // the dequant warps and the activation producer (+ tx bytes)
             mbar_init(empty0 + 8 * s, 1);        // tcgen05.commit
         }
         for (int r = 0; r < 2; ++r) {
@@ -182,10 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                     // one kXBox-row box for a tile of at most kXBox tokens, two otherwise:
                     // the MMA reads only the tile's rows
                     const int nbox = t.cnt > kXBox ? 2 : 1;
-                    mbar_arrive_expect_tx(xfull0 + 8 * s, nbox * kXBoxBytes);
+                    mbar_arrive_expect_tx(full0 + 8 * s, nbox * kXBoxBytes);
                     for (int q = 0; q < nbox; ++q)
                         tma_load_2d(smem_u32(xs + s * kXB + q * kXBoxBytes), &tmX, kb * kQK + kStageK * g,
-                                    t.m0 + q * kXBox, xfull0 + 8 * s);
+                                    t.m0 + q * kXBox, full0 + 8 * s);
                     ++x_issued;
                 }
             }
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 for (int j = raw_issued > 2 ? raw_issued - 2 : 0; j < raw_issued; ++j)
                     (void)mbar_wait(rfull0 + 8 * (j & 1), (j >> 1) & 1, status);
                 for (int j = x_issued > kNS ? x_issued - kNS : 0; j < x_issued; ++j)
-                    (void)mbar_wait(xfull0 + 8 * (j % kNS), (j / kNS) & 1, status);
+                    (void)mbar_wait(full0 + 8 * (j % kNS), (j / kNS) & 1, status);
             }
         }
     } else if (warp == 1) {
@@ -215,8 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 const uint32_t d = tmem + (uint32_t)(buf * kBN);
                 for (int j = 0; j < KB * 4; ++j) {
                     const int i = k * KB * 4 + j, s = i % kNS;
-                    if (!mbar_wait(full0 + 8 * s, (i / kNS) & 1, status) ||
-                        !mbar_wait(xfull0 + 8 * s, (i / kNS) & 1, status) || *abort_flag) {
+                    if (!mbar_wait(full0 + 8 * s, (i / kNS) & 1, status) || *abort_flag) {
                         ok = false;
                         break;
                     }
