@@ -76,7 +76,7 @@ struct Cfg {
     // with the operand in tensor memory the two rings are equally deep, so that
     // they share their barriers (in shared memory 3 operand stages leave room for
     // 4 activation stages, which measured faster than 3 + 3)
-    static constexpr int NS = TA ? (BN == 128 ? 6 : 4) : 3;  // dequantized-weight stages
+    static constexpr int NS = TA ? (BN == 128 ? 8 : 4) : 3;  // dequantized-weight stages
     static constexpr int XS = TA ? NS : 4;                   // activation stages
     static constexpr int RS = TA ? 3 : 2;               // raw Q4_K slots
     static constexpr int XB = BN * kStageK * 2;         // activation bytes per stage
