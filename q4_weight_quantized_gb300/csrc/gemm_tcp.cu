@@ -207,7 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 const int mma_n = (t.cnt + 15) & ~15;
                 const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, mma_n);
                 const int buf = k & 1;
-                if (k >= 2 && !mbar_wait(accempty0 + 8 * buf, ((k >> 1) - 1) & 1, status)) {
+                // another role that gave up is seen here, once per tile (a stage whose
+                // producers gave up never completes, and its wait is bounded)
+                if ((k >= 2 && !mbar_wait(accempty0 + 8 * buf, ((k >> 1) - 1) & 1, status)) || *abort_flag) {
                     ok = false;
                     break;
                 }
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
                 const uint32_t d = tmem + (uint32_t)(buf * kBN);
                 for (int j = 0; j < KB * 4; ++j) {
                     const int i = k * KB * 4 + j, s = i % kNS;
-                    if (!mbar_wait(full0 + 8 * s, (i / kNS) & 1, status) || *abort_flag) {
+                    if (!mbar_wait(full0 + 8 * s, (i / kNS) & 1, status)) {
                         ok = false;
                         break;
                     }
