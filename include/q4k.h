@@ -131,7 +131,8 @@ int q4k_set_static_weights(int enable);
  *       half 0 and half 1 in that order.
  *       Cost: none where the weight rows fill the GPU without a K split (the
  *       K 5120 -> N 17408 prefill shape); on the narrow K 17408 -> N 5120 shape
- *       +36 % time at 128 tokens, +30 % at 1024, +10 % at 4096 on one GB300.
+ *       +34 % time at 128 tokens, +68 % at 1024, +35 % at 4096 on one GB300
+ *       (the two-accumulator form keeps its weight operand in shared memory).
  * The boundary between the two paths stays: rows of calls with M <= 16 and
  * M > 16 differ in rounding (different kernels, each within its bar).
  * Process-wide; applies to calls enqueued after it returns.  Returns the previous
