@@ -126,13 +126,12 @@ int q4k_set_static_weights(int enable);
  *       in two or not at all, as the weight shape alone dictates (never by M),
  *       and split off no last-wave launch, so a token's row has the same bits
  *       in every call of 17 tokens or more, wherever it sits in the batch.  The
- *       two K halves are summed over a thread-block cluster when the call's
- *       tiles leave SMs idle, else in two accumulators of one CTA; both add
- *       half 0 and half 1 in that order.
+ *       two K halves are summed over a thread-block cluster pair, half 0 plus
+ *       half 1.
  *       Cost: none where the weight rows fill the GPU without a K split (the
  *       K 5120 -> N 17408 prefill shape); on the narrow K 17408 -> N 5120 shape
- *       +34 % time at 128 tokens, +68 % at 1024, +35 % at 4096 on one GB300
- *       (the two-accumulator form keeps its weight operand in shared memory).
+ *       about +34 % time at 128 tokens, +25 % at 1024, +22 % at 4096 on one
+ *       GB300.
  * The boundary between the two paths stays: rows of calls with M <= 16 and
  * M > 16 differ in rounding (different kernels, each within its bar).
  * Process-wide; applies to calls enqueued after it returns.  Returns the previous

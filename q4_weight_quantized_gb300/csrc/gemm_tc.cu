@@ -59,32 +59,27 @@ constexpr int kEPT = 32 / kTPR;                   // code bytes of a group per d
 constexpr int kWPT = kEPT / 4;                    // the same in 32-bit words
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr int kStageCols = kStageK / 2;           // tensor-memory columns of one stage's operand (bf16 pairs)
-constexpr int kABytes = kTileRows * kStageK * 2;  // 16 KiB: one stage's operand in shared memory
-constexpr uint32_t kTmemCols = 512;               // accumulator(s) + operand stages, whole allocation
+constexpr uint32_t kTmemCols = 512;               // accumulator + operand stages, whole allocation
 
-// Three rings: activations (XS stages, shared memory), dequantized weights
-// (NS stages: tensor memory when TA, else shared memory) and raw Q4_K blocks
-// (RS slots, shared memory).  The activation copy of stage i can only start
-// once the MMAs of stage i - XS are done, and it crosses L2, so that ring is the
-// deeper one: XS stages of MMA time must cover an L2 round trip under load.  A
-// raw slot is free again as soon as the dequant warps have read its codes into
-// registers, and its own producer refills it at once, RS - 1 blocks ahead.
-// TA = false serves the one launch whose two accumulators fill all 512
-// tensor-memory columns (batch-invariant mode, 256-token tiles).
-template <int BN, bool TA>
+// Rings: NS stages, each an activation tile in shared memory plus the
+// dequantized weight operand in tensor memory, and RS raw Q4_K slots in shared
+// memory.  A stage's activation copy can only start once the MMAs of the stage
+// NS before are done, and it crosses L2: NS stages of MMA time must cover an L2
+// round trip under load.  A stage is full once the dequant warps have written
+// its operand and its activation copy has landed (one barrier), and one commit
+// frees both halves, so that the MMA thread waits once and commits once per
+// stage.  A raw slot is free again as soon as the dequant warps have read its
+// codes into registers, and its own producer refills it at once, RS - 1 blocks
+// ahead.
+template <int BN>
 struct Cfg {
-    // with the operand in tensor memory the two rings are equally deep, so that
-    // they share their barriers (in shared memory 3 operand stages leave room for
-    // 4 activation stages, which measured faster than 3 + 3)
-    static constexpr int NS = TA ? (BN == 128 ? 8 : 4) : 3;  // dequantized-weight stages
-    static constexpr int XS = TA ? NS : 4;                   // activation stages
-    static constexpr int RS = TA ? 3 : 2;               // raw Q4_K slots
+    static constexpr int NS = BN == 128 ? 8 : 4;        // stages
+    static constexpr int RS = 3;                        // raw Q4_K slots
     static constexpr int XB = BN * kStageK * 2;         // activation bytes per stage
     static constexpr int x_off = 0;
-    static constexpr int a_off = x_off + XS * XB;       // shared-memory operand stages (TA = false)
-    static constexpr int raw_off = a_off + (TA ? 0 : NS * kABytes);
+    static constexpr int raw_off = x_off + NS * XB;
     static constexpr int bar_off = raw_off + RS * kRawBytes;
-    static constexpr int n_bars = 2 * NS + 2 * XS + 2 * RS + 1;
+    static constexpr int n_bars = 2 * NS + 2 * RS + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;  // + slack to align the base to 1024
     static_assert(bytes <= 227 * 1024, "dynamic shared memory per CTA");
@@ -97,38 +92,29 @@ __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) { return *reinterpr
 // FP4: the weights are NVFP4 blocks (16 e4m3 scales, then 128 bytes of e2m1
 // pairs) instead of Q4_K; each operand element is the exact e2m1 * e4m3 product
 // in bf16, and the epilogue multiplies by the tensor scale gscale.
-template <int BN, bool FP4, bool TA>
+template <int BN, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX, float *y,
                                                               int64_t ldy, int M, int N, int KB, float gscale,
-                                                              int late_wait, int nacc, unsigned int *status) {
-    // nacc = 2 (no cluster split): the first and the second half of K, as a 2-way K
-    // split would divide it, accumulate into two tensor-memory accumulators that the
-    // epilogue adds in that order - the bits of the 2-way split, without a cluster.
+                                                              int late_wait, unsigned int *status) {
     // late_wait: this launch is the remainder of a split problem, queued right after
     // the main launch, which waited for the producers of x and w before letting it
     // start; it waits for the main launch only before it ends, so that a later
     // kernel that waits on this one also sees the main launch's outputs
     if (!late_wait) pdl_wait();  // the activations may come from the previous kernel
     pdl_trigger();
-    using C = Cfg<BN, TA>;
-    constexpr int NS = C::NS, XS = C::XS, RS = C::RS;
+    using C = Cfg<BN>;
+    constexpr int NS = C::NS, RS = C::RS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *xs = base + C::x_off;
-    uint8_t *as = base + C::a_off;
     uint8_t *raw = base + C::raw_off;
     const uint32_t bar = smem_u32(base + C::bar_off);
-    // full: the dequant warps wrote the stage's operand; empty: the MMAs reading
-    // it are done; xfull: an activation stage's copy landed (tx bytes); xempty: the
-    // MMAs reading it are done; rfull / rempty: the raw tile ring; accfull: all MMAs
-    // of the tile are done
-    const uint32_t full0 = bar, empty0 = bar + 8 * NS, xfull0 = bar + 16 * NS, xempty0 = xfull0 + 8 * XS,
-                   rfull0 = xempty0 + 8 * XS, rempty0 = rfull0 + 8 * RS, accfull = rempty0 + 8 * RS;
-    // rings of equal depth share their barriers: a stage is full once the dequant
-    // warps have arrived and its activation copy has landed, and one commit frees it
-    constexpr bool kOneRing = NS == XS;
-    const uint32_t xfull_b = kOneRing ? full0 : xfull0, xempty_b = kOneRing ? empty0 : xempty0;
+    // full: the dequant warps wrote the stage's operand and its activation copy
+    // landed (tx bytes); empty: the MMAs reading the stage are done; rfull / rempty:
+    // the raw tile ring; accfull: all MMAs of the tile are done
+    const uint32_t full0 = bar, empty0 = bar + 8 * NS, rfull0 = empty0 + 8 * NS, rempty0 = rfull0 + 8 * RS,
+                   accfull = rempty0 + 8 * RS;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base + C::misc_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::misc_off + 4);
 
@@ -140,16 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int kbeg = (int)((int64_t)KB * split / S);
     const int KBs = (int)((int64_t)KB * (split + 1) / S) - kbeg;
     const int total = KBs * 4;  // 64-wide stages
-    const int imid = nacc == 2 ? (KB / 2) * 4 : total;  // first stage of the second accumulator
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8 * s, kDqWarps + (kOneRing ? 1 : 0));  // the dequant warps (+ the activation producer)
-            mbar_init(empty0 + 8 * s, 1);  // tcgen05.commit
-        }
-        for (int s = 0; s < XS; ++s) {
-            mbar_init(xfull0 + 8 * s, 1);   // producer (+ tx bytes)
-            mbar_init(xempty0 + 8 * s, 1);  // tcgen05.commit
+            mbar_init(full0 + 8 * s, kDqWarps + 1);  // the dequant warps and the activation producer
+            mbar_init(empty0 + 8 * s, 1);            // tcgen05.commit
         }
         for (int r = 0; r < RS; ++r) {
             mbar_init(rfull0 + 8 * r, 1);
@@ -167,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // columns [0, BN * nacc): the accumulator(s); then (TA) NS operand stages of kStageCols
-    const uint32_t a_col0 = (uint32_t)(BN * nacc);
+    // columns [0, BN): the accumulator; then NS operand stages of kStageCols
+    const uint32_t a_col0 = (uint32_t)BN;
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA: raw Q4_K
@@ -195,30 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, BN);
             for (int i = 0; i < total; ++i) {
-                const int s = i % NS, sx = i % XS;
-                if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status) ||
-                    (!kOneRing && !mbar_wait(xfull0 + 8 * sx, (i / XS) & 1, status))) {
+                const int s = i % NS;
+                if (!mbar_wait(full0 + 8 * s, (i / NS) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t bd = umma_desc_sw128(smem_u32(xs + sx * C::XB));
-                const bool second = i >= imid;
-                const uint32_t dacc = tmem + (second ? (uint32_t)BN : 0u);
-                const int i0 = second ? imid : 0;  // the accumulator's first stage
-                if constexpr (TA) {
-                    const uint32_t at = tmem + a_col0 + (uint32_t)(kStageCols * s);
+                const uint64_t bd = umma_desc_sw128(smem_u32(xs + s * C::XB));
+                const uint32_t at = tmem + a_col0 + (uint32_t)(kStageCols * s);
 #pragma unroll
-                    for (int kk = 0; kk < kStageK / 16; ++kk)  // A: +8 columns, B: +32 bytes per 16-wide step
-                        umma_bf16_ts(dacc, at + 8 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
-                } else {
-                    const uint64_t ad = umma_desc_sw128(smem_u32(as + s * kABytes));
-#pragma unroll
-                    for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes along K per 16-wide step
-                        umma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, ((i - i0) | kk) != 0);
-                }
+                for (int kk = 0; kk < kStageK / 16; ++kk)  // A: +8 columns, B: +32 bytes per 16-wide step
+                    umma_bf16_ts(tmem, at + 8 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
                 umma_commit(empty0 + 8 * s);
-                if constexpr (!kOneRing) umma_commit(xempty0 + 8 * sx);
             }
             // completes once every MMA issued above has (also after an abort, so
             // that tensor memory is freed only after the MMAs that write it)
@@ -280,20 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                         for (int q = 0; q < 4; ++q) p[4 * j + q] = as_u32(__hmul2(as_bf2(p[4 * j + q]), sv[j >> 1]));  // exact
                     }
-                    if constexpr (TA) {
-                        tc_fence_after();  // after the wait for the MMAs that read this stage
-                        tmem_st(arow0 + (uint32_t)(kStageCols * s + kEPT * h), p);
-                        tmem_st_wait();
-                        tc_fence_before();
-                    } else {
-                        // 128-byte-swizzled K-major rows: 16-byte chunk c of row `row` at (c ^ row % 8)
-                        uint8_t *arow = as + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                        for (int j = 0; j < kEPT / 4; ++j)
-                            *reinterpret_cast<uint4 *>(arow + ((((kEPT / 4) * h + j) ^ (row & 7)) << 4)) =
-                                make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-                        fence_proxy_async_smem();  // make the stores visible to the tensor core
-                    }
+                    tc_fence_after();  // after the wait for the MMAs that read this stage
+                    tmem_st(arow0 + (uint32_t)(kStageCols * s + kEPT * h), p);
+                    tmem_st_wait();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(full0 + 8 * s);
                 }
@@ -329,27 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     ok = false;
                     break;
                 }
-                if constexpr (TA) {
-                    tc_fence_after();  // after the wait for the MMAs that read this stage
-                    const uint32_t at = arow0 + (uint32_t)(kStageCols * s + kEPT / 2 * h);
-                    tmem_st(at, lo[g]);
-                    tmem_st(at + 16, hi[g]);
-                    tmem_st_wait();
-                    tc_fence_before();
-                } else {
-                    // 128-byte-swizzled K-major rows: 16-byte chunk c of row `row` at (c ^ row % 8);
-                    // chunks (kEPT / 8) h .. hold these elements of sub-block 2g, 4 + (kEPT / 8) h .. of 2g+1
-                    uint8_t *arow = as + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                    for (int j = 0; j < kEPT / 8; ++j) {
-                        const int cl = (kEPT / 8) * h + j;
-                        *reinterpret_cast<uint4 *>(arow + ((cl ^ (row & 7)) << 4)) =
-                            make_uint4(lo[g][4 * j], lo[g][4 * j + 1], lo[g][4 * j + 2], lo[g][4 * j + 3]);
-                        *reinterpret_cast<uint4 *>(arow + (((cl + 4) ^ (row & 7)) << 4)) =
-                            make_uint4(hi[g][4 * j], hi[g][4 * j + 1], hi[g][4 * j + 2], hi[g][4 * j + 3]);
-                    }
-                    fence_proxy_async_smem();  // make the stores visible to the tensor core
-                }
+                tc_fence_after();  // after the wait for the MMAs that read this stage
+                const uint32_t at = arow0 + (uint32_t)(kStageCols * s + kEPT / 2 * h);
+                tmem_st(at, lo[g]);
+                tmem_st(at + 16, hi[g]);
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full0 + 8 * s);
             }
@@ -370,13 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cc, v);
                 tmem_ld_wait();
-                if (nacc == 2) {  // + the second half of K, in split-rank order
-                    uint32_t v2[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + BN + 32 * cc, v2);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
-                }
                 if (S > 1) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) part[(32 * cc + j) * kTileRows + rl] = __uint_as_float(v[j]);
@@ -395,17 +332,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             prefetch_tmap(&tmX);
             int issued = 0;
             for (int i = 0; i < total && !*abort_flag; ++i) {
-                const int kb = i >> 2, g = i & 3, s = i % XS;
-                if (i >= XS && !mbar_wait(xempty_b + 8 * s, ((i / XS) - 1) & 1, status)) {
+                const int kb = i >> 2, g = i & 3, s = i % NS;
+                if (i >= NS && !mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status)) {
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(xfull_b + 8 * s, C::XB);
-                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, xfull_b + 8 * s);
+                mbar_arrive_expect_tx(full0 + 8 * s, C::XB);
+                tma_load_2d(smem_u32(xs + s * C::XB), &tmX, (kbeg + kb) * kQK + kStageK * g, m0, full0 + 8 * s);
                 ++issued;
             }
-            for (int j = issued > XS ? issued - XS : 0; j < issued; ++j)
-                (void)mbar_wait(xfull_b + 8 * (j % XS), (j / XS) & 1, status);
+            // (on the normal path the MMAs have consumed every stage already; after an
+            // abort these bounded waits may run out, the copies having landed or not)
+            for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
+                (void)mbar_wait(full0 + 8 * (j % NS), (j / NS) & 1, status);
         }
     }
     if (S > 1) {
@@ -453,29 +392,25 @@ int k_split(const DeviceInfo &di, int64_t tiles, int KB) {
     return S;
 }
 
-// S: the cluster K split (1: none); nacc = 2: two accumulators in place of a 2-way
-// split (S = 1 then).
-template <int BN, bool FP4, bool TA = true>
+// S: the cluster K split (1: none).
+template <int BN, bool FP4>
 cudaError_t launch_bn(const DeviceInfo &di, const void *w, int64_t N, int64_t K, const uint16_t *x, int64_t M,
-                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int S, int late_wait = 0,
-                      int nacc = 1) {
+                      int64_t ldx, float *y, int64_t ldy, float g, cudaStream_t s, int S, int late_wait = 0) {
     CUtensorMap tmW, tmX;
     cudaError_t e = make_weight_tmap(&tmW, w, N, K, kTileRows, kBlockBytes / 4);
     if (e != cudaSuccess) return e;
     e = make_act_tmap_sw128(&tmX, x, M, K, ldx, BN);
     if (e != cudaSuccess) return e;
-    using C = Cfg<BN, TA>;
+    using C = Cfg<BN>;
     const int smem = C::bytes;
-    static_assert(C::raw_off >= BN * kTileRows * 4, "the partial tile fits in the stage buffers ahead of the raw slots");
-    constexpr int a_cols = TA ? C::NS * kStageCols : 0;  // tensor-memory operand stages
-    static_assert(BN + a_cols <= (int)kTmemCols, "the accumulator and the stages fit");
-    if (nacc < 1 || nacc > 2 || nacc * BN + a_cols > (int)kTmemCols) return cudaErrorInvalidValue;
-    e = ensure_smem((const void *)gemm_tc_kernel<BN, FP4, TA>, smem);
+    static_assert(C::raw_off >= BN * kTileRows * 4, "the partial tile fits in the activation stages");
+    static_assert(BN + C::NS * kStageCols <= (int)kTmemCols, "the accumulator and the operand stages fit");
+    e = ensure_smem((const void *)gemm_tc_kernel<BN, FP4>, smem);
     if (e != cudaSuccess) return e;
     const int KB = (int)(K / kQK);
     const dim3 grid((unsigned)((N + kTileRows - 1) / kTileRows), (unsigned)((M + BN - 1) / BN), (unsigned)S);
-    return launch_pdl(gemm_tc_kernel<BN, FP4, TA>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
-                      tmX, y, ldy, (int)M, (int)N, KB, g, late_wait, nacc, di.status);
+    return launch_pdl(gemm_tc_kernel<BN, FP4>, grid, dim3(kThreads), (size_t)smem, s, dim3(1, 1, (unsigned)S), tmW,
+                      tmX, y, ldy, (int)M, (int)N, KB, g, late_wait, di.status);
 }
 
 // One CTA per SM: when the tiles' last wave would run mostly empty and a row of
@@ -502,13 +437,10 @@ cudaError_t launch_split(const DeviceInfo &di, const void *w, int64_t N, int64_t
     const int KB = (int)(K / kQK);
     const int64_t tn = (N + kTileRows - 1) / kTileRows;
     if (invariant) {
-        // at most 2 ways, so that one CTA can hold both halves' 256-column
-        // accumulators (the operand stages then in shared memory) when the
-        // tiles alone fill the GPU
+        // at most 2 ways over a cluster pair, at every M (3 ways measured slower
+        // at large M)
         const int S = k_split(di, tn, KB) > 1 ? 2 : 1;
         if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
-        if (S == 2 && 2 * tn * ((M + 255) / 256) > di.sm_count)
-            return launch_bn<256, FP4, false>(di, w, N, K, x, M, ldx, y, ldy, g, s, 1, 0, 2);
         return launch_bn<256, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, S);
     }
     if (M <= 128) return launch_bn<128, FP4>(di, w, N, K, x, M, ldx, y, ldy, g, s, k_split(di, tn, KB));

@@ -422,9 +422,9 @@ def test_prefill_batch_invariant_mode(ref, N, K):
     # q4k_set_batch_invariant(1) on the tensor-core path (M > 16): the K split is
     # chosen from the weight shape alone and no last-wave launch is split off, so a
     # token's output row has the same bits in calls of 17 to 4096 tokens at any
-    # offset in the batch.  On the down projection's shape the split is 2-way: over a
-    # cluster for calls whose tiles leave SMs idle (17, 128, 129 tokens), in two
-    # accumulators of one CTA otherwise (300 tokens and up)
+    # offset in the batch.  On the down projection's shape the split is 2-way over a
+    # cluster pair at every M (17, 128 and 129 tokens take 128-token tiles, the
+    # longer calls 256-token tiles)
     b = G.weights(3, 0, N, K, outliers=True)
     w = G.dev(b)
     x = G.activations(3, 1, 4096, K)
@@ -1137,8 +1137,8 @@ def test_static_weights_activations_from_the_previous_kernel(ref, N, K, M, fp4):
 
 def test_nvfp4_batch_invariant_mode(ref):
     # the NVFP4 tensor-core path in batch-invariant mode: rows independent of M
-    # 8 row tiles: calls of up to 9 token tiles split K 2 ways over a cluster, the
-    # 2600-token call keeps the two halves in two accumulators of one CTA instead
+    # 8 row tiles: every call splits K 2 ways over a cluster pair, from 40 tokens
+    # (128-token tiles) to the 2600-token call (11 tiles of 256, more CTAs than SMs)
     N, K = 1000, 4096
     w, g = fp4_weights(2, N, K)
     x = G.activations(7, 9, 2600, K)
