@@ -13,20 +13,22 @@
 //     64-wide K stage, one copy of the activation tile (BN tokens x 64 bf16)
 //     with the 128-byte swizzle that the tensor core's K-major layout expects.
 //   * Warps 4-11 (dequant): two threads per weight row.  Once per K block each
-//     loads the 64 code bytes it will convert (16 of each group), then for each
-//     64-wide stage (one Q4_K group: sub-blocks 2g and 2g+1) it turns its 16
-//     code bytes into 32 bf16 weights, each the round-to-nearest-even bf16 of
-//     the fp32 weight fl32(q * d sc - dmin m) (packed fp32 FMAs, q * d sc exact
+//     loads the 64 code bytes it will convert (16 of each group) and turns them
+//     into 128 bf16 weights for the block's four 64-wide stages (one Q4_K group
+//     each: sub-blocks 2g and 2g+1), each the round-to-nearest-even bf16 of the
+//     fp32 weight fl32(q * d sc - dmin m) (packed fp32 FMAs, q * d sc exact
 //     inside them), i.e. the very value the standalone bf16 dequantization
-//     writes.  They go to tensor memory, not shared memory: the row's lane, two
-//     weights per column (tcgen05.st), where the MMA reads its A operand.  The
+//     writes; then it hands the stages over one by one as the MMA frees them.
+//     They go to tensor memory, not shared memory: the row's lane, two weights
+//     per column (tcgen05.st), where the MMA reads its A operand.  The
 //     tensor core's operand reads, the activation and raw copies and the
 //     dequant stores would otherwise all share the SM's shared-memory bandwidth,
 //     which then set the pace of every stage.
 //   * Warp 1 (MMA): one elected thread issues four 128 x BN x 16 tcgen05.mma per
 //     stage (A from tensor memory, B from shared memory) into an fp32
-//     accumulator in tensor memory and commits each stage's completion to the
-//     barriers that free the operand stage and the activation stage.
+//     accumulator in tensor memory.  It waits on one barrier per stage (the
+//     dequant warps and the activation copy both arrive on it) and commits the
+//     stage's completion to one barrier that frees both halves of the stage.
 //   * Warps 4-11 then read the accumulator (tcgen05.ld, one 32-lane quarter and
 //     half the columns per warp) and store fp32 rows of y with coalesced
 //     128-byte writes.
