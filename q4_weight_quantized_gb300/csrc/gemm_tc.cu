@@ -227,16 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             __syncwarp();
             if (lane == 0) mbar_arrive(rempty0 + 8 * r);
             if constexpr (FP4) {
+                // all four stages of the block first (registers), then the hand-offs.
+                // Stage g4: weights 64*g4 .. +63 of the block, scales 4*g4 .. +3 (16
+                // weights each); this thread takes weights 2 kEPT h .. +2 kEPT - 1 of the
+                // stage (code word j: scale kEPT h / 8 + j / 2)
+                uint32_t p[4][2 * kEPT / 2];  // stage columns kEPT h .. : two weights each
+#pragma unroll
                 for (int g4 = 0; g4 < 4; ++g4) {
-                    const int i = kb * 4 + g4, s = i % NS;
-                    if (i >= NS &&
-                        !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status))) {
-                        ok = false;
-                        break;
-                    }
-                    // stage g4: weights 64*g4 .. +63 of the block, scales 4*g4 .. +3 (16 weights
-                    // each); this thread takes weights 2 kEPT h .. +2 kEPT - 1 of the stage
-                    // (code word j: scale kEPT h / 8 + j / 2)
                     const uint32_t scw = g4 == 0 ? hd.x : g4 == 1 ? hd.y : g4 == 2 ? hd.z : hd.w;
                     __nv_bfloat162 sv[kEPT / 8];
 #pragma unroll
@@ -244,15 +241,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         const float f = e4m3_to_f32(scw >> (8 * (kEPT * h / 8 + q)));
                         sv[q] = __floats2bfloat162_rn(f, f);  // exact: e4m3 values are bf16 values
                     }
-                    uint32_t p[2 * kEPT / 2];  // stage columns kEPT h .. : two weights each
 #pragma unroll
                     for (int j = 0; j < kWPT; ++j) {
-                        e2m1x8_to_bf16(qv[g4][j], p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+                        e2m1x8_to_bf16(qv[g4][j], p[g4][4 * j], p[g4][4 * j + 1], p[g4][4 * j + 2], p[g4][4 * j + 3]);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) p[4 * j + q] = as_u32(__hmul2(as_bf2(p[4 * j + q]), sv[j >> 1]));  // exact
+                        for (int q = 0; q < 4; ++q)
+                            p[g4][4 * j + q] = as_u32(__hmul2(as_bf2(p[g4][4 * j + q]), sv[j >> 1]));  // exact
+                    }
+                }
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const int i = kb * 4 + g4, s = i % NS;
+                    if (i >= NS &&
+                        !__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * s, ((i / NS) - 1) & 1, status))) {
+                        ok = false;
+                        break;
                     }
                     tc_fence_after();  // after the wait for the MMAs that read this stage
-                    tmem_st(arow0 + (uint32_t)(kStageCols * s + kEPT * h), p);
+                    tmem_st(arow0 + (uint32_t)(kStageCols * s + kEPT * h), p[g4]);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();

@@ -202,8 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcp_kernel(const __grid_cons
         // ------------------------------------------------------------- MMA
         if (lane == 0) {
             bool ok = true;
+            Tile tn = tile_of(p, 0);  // the next tile's record, loaded a tile ahead
             for (int k = 0; k < my_tiles && ok; ++k) {
-                const Tile t = tile_of(p, k);
+                const Tile t = tn;
+                if (k + 1 < my_tiles) tn = tile_of(p, k + 1);
                 const int mma_n = (t.cnt + 15) & ~15;
                 const uint32_t idesc = umma_idesc_bf16_f32(kTileRows, mma_n);
                 const int buf = k & 1;
